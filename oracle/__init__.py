@@ -1,0 +1,112 @@
+"""CPU oracle for causal varlen prefill attention (fp64).
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package.  The library's
+product path never imports, links or executes anything here, and this package
+imports nothing from the library.
+
+The arithmetic lives in ``oracle.c`` (plain C, fp64, OpenMP over query rows);
+this module compiles it with gcc and marshals numpy arrays into it.  Every
+floating-point input is a bf16 bit pattern (``numpy.uint16``); outputs are
+float64.  See ``oracle.c`` for the definition and the passages it follows.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from typing import Optional
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "liboracle.so")
+_lib = None
+
+ERRORS = {
+    -1: "bad sizes",
+    -2: "cu_seqlens_q does not start at 0 or decreases",
+    -3: "cu_seqlens_k != cumulative (cache_offsets + seqlen_q)",
+    -4: "a sequence does not fit its cache slot",
+    -5: "selected row out of range",
+    -6: "out of memory",
+}
+
+
+def build_command():
+    return ["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", _SRC, "-o", _LIB_PATH, "-lm"]
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into oracle/_build/liboracle.so (idempotent)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        subprocess.check_call(build_command())
+    return _LIB_PATH
+
+
+def load_library(path: str):
+    """Bind oracle_prefill_attention from a compiled oracle library."""
+    lib = ctypes.CDLL(path)
+    f = lib.oracle_prefill_attention
+    P = ctypes.c_void_p
+    I = ctypes.c_int
+    f.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, I,
+                  ctypes.c_double, I, P, ctypes.c_int64, I]
+    f.restype = I
+    return lib
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        _lib = load_library(build())
+    return _lib
+
+
+def _ptr(a: Optional[np.ndarray]):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def prefill_attention(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_offsets, cache_k, cache_v, *,
+                      n_heads: int, n_kv_heads: int, head_dim: int, max_cache_len: int,
+                      scale: float, causal: bool = True, rows: Optional[np.ndarray] = None,
+                      want_cache: bool = True, threads: int = 0, lib=None):
+    """Run the oracle.
+
+    q [T,H,d], k/v [T,Hk,d], cache_k/v [B,Hk,cap,d]: uint16 bf16 bit patterns.
+    cu_seqlens_q/k [B+1], cache_offsets [B]: int32.
+    rows: optional int64 array of flattened (token * n_heads + head) rows.
+
+    Returns (out float64 [T,H,d], lse float64 [T,H], cache_k', cache_v') where
+    unselected rows of out/lse are NaN and the cache images are None when
+    ``want_cache`` is false.
+    """
+    lib = lib or _load()
+    u16 = lambda a: np.ascontiguousarray(a, dtype=np.uint16)
+    i32 = lambda a: np.ascontiguousarray(a, dtype=np.int32)
+    q, k, v, cache_k, cache_v = map(u16, (q, k, v, cache_k, cache_v))
+    cu_q, cu_k, off = map(i32, (cu_seqlens_q, cu_seqlens_k, cache_offsets))
+    num_seqs = off.shape[0]
+    total_q = int(cu_q[-1]) if num_seqs else 0
+    assert q.size == total_q * n_heads * head_dim, "q size disagrees with cu_seqlens_q"
+    assert k.size == total_q * n_kv_heads * head_dim and v.size == k.size
+    assert cache_k.size == num_seqs * n_kv_heads * max_cache_len * head_dim == cache_v.size
+    out = np.full((total_q, n_heads, head_dim), np.nan, dtype=np.float64)
+    lse = np.full((total_q, n_heads), np.nan, dtype=np.float64)
+    ck = np.empty_like(cache_k) if want_cache else None
+    cv = np.empty_like(cache_v) if want_cache else None
+    sel = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+    rc = lib.oracle_prefill_attention(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(cu_q), _ptr(cu_k), _ptr(off), _ptr(cache_k), _ptr(cache_v),
+        _ptr(ck), _ptr(cv), _ptr(out), _ptr(lse),
+        num_seqs, max_cache_len, n_heads, n_kv_heads, head_dim, float(scale), int(bool(causal)),
+        _ptr(sel), 0 if sel is None else sel.shape[0], int(threads))
+    if rc != 0:
+        raise ValueError(f"oracle: {ERRORS.get(rc, rc)}")
+    if want_cache:
+        ck = ck.reshape(cache_k.shape)
+        cv = cv.reshape(cache_v.shape)
+    return out, lse, ck, cv

@@ -1,0 +1,239 @@
+/*
+ * oracle.c -- plain fp64 CPU definition of causal varlen prefill attention
+ * with the KV-cache write.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the library's product path may call,
+ * link or load this file; only the tests, the package's smoke check and the
+ * benchmark's CPU-baseline leg use it.  It shares no code, header or constant
+ * with the CUDA path.
+ *
+ * Pages cited (title, site), by short name:
+ *   [mhpn]   "Prefill不是热身：大模型推理的真正瓶颈与优化核心" (mhpn.cn)
+ *   [zskr]   "大模型推理优化：Prefill、Decode与KV Cache的工程实践" (zskr.cn)
+ *   [nxmr]   "大模型 Prompt Prefill 阶段的高效 Batching 与算子排布" (nxmr.cn)
+ *   [yfxerp] "大语言模型推理核心：Prefill与Decode原理及工程优化" (yfxerp.com)
+ *   [zwxr]   the untitled page on prefill/decode compute accounting (zwxr.cn)
+ *
+ * What it computes, written out as its definition (no tiling, no online
+ * softmax, no reordering beyond the plain loops below):
+ *
+ *  - Scaled dot-product attention softmax(Q K^T * scale) V, one query row at a
+ *    time ([yfxerp] §2.2; [mhpn] §3).  The softmax denominator runs over the
+ *    whole visible row ([yfxerp] §2.2: leaving out any key changes every
+ *    weight of the row).
+ *  - Varlen packing: sequence b owns query rows cu_seqlens_q[b] ..
+ *    cu_seqlens_q[b+1]-1 of the flattened stream and attends only inside
+ *    itself ([nxmr] §2, cu_seqlens = [0, 5, 7, 10]).
+ *  - Causal lower-triangular mask: a position sees itself and the positions
+ *    before it ([zwxr] §3.3).
+ *  - Chunked prefill: a chunk of n new tokens of sequence b follows
+ *    P = cache_offsets[b] tokens already in the cache; its keys are the P cached
+ *    keys followed by its own n keys, and new query i sits at absolute position
+ *    P + i ([zskr] §2.2; [nxmr] §3).  A decode row is the chunk n = 1: it sees
+ *    the cache plus itself ([zwxr] §1.2: the new token attends to all 301
+ *    positions after its K/V are appended).
+ *  - GQA: query head h reads KV head h / (n_heads / n_kv_heads)
+ *    ([zwxr] §2.4: 32 query heads over 8 KV heads; contiguous groups).
+ *  - KV-cache production: cache[b][kvh][P + i][:] = k[cu_q[b] + i][kvh][:] (and
+ *    the same for v), a bit copy into the (kv_heads, seq, head_dim) layout of
+ *    [yfxerp] §2.1 / §3.2; every other cache entry is left as it was.
+ *
+ * Inputs q, k, v and the caches are bf16 bit patterns (uint16); each value is
+ * widened exactly to fp64 before any arithmetic.  Outputs are fp64:
+ *   out[t][h][e]  = sum_j w_j V_j[e],  w_j = exp(s_j - m) / Z over visible j
+ *   lse[t][h]     = m + ln Z            (natural log of sum_j exp(s_j))
+ * with s_j = scale * <q, K_j>, m = max_j s_j, Z = sum_j exp(s_j - m).
+ * Subtracting m is a mathematical identity that keeps exp() finite.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Exact widening of a bf16 bit pattern: it is the top half of an IEEE fp32. */
+static double bf16_to_double(uint16_t bits)
+{
+    uint32_t u = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+typedef struct {
+    const uint16_t *q, *k, *v;            /* [T][H][d], [T][Hk][d], [T][Hk][d] */
+    const uint16_t *cache_k, *cache_v;     /* [B][Hk][cap][d], read for the prefix */
+    const int32_t *cu_q, *off;
+    double *out, *lse;
+    int num_seqs, cap, n_heads, n_kv_heads, d;
+    double scale;
+    int causal;
+} problem;
+
+/* Key j of sequence b, KV head kvh: the cached prefix, then the new tokens. */
+static const uint16_t *key_row(const problem *pb, const uint16_t *cache, const uint16_t *fresh,
+                               int b, int kvh, int j)
+{
+    int P = pb->off[b];
+    if (j < P)
+        return cache + (((size_t)b * pb->n_kv_heads + kvh) * pb->cap + (size_t)j) * pb->d;
+    return fresh + ((size_t)(pb->cu_q[b] + (j - P)) * pb->n_kv_heads + kvh) * pb->d;
+}
+
+/* One query row (sequence b, new token i, head h).  `s` has room for P+n doubles. */
+static void attend_row(const problem *pb, int b, int i, int h, double *s)
+{
+    const int d = pb->d;
+    const int P = pb->off[b];
+    const int n = pb->cu_q[b + 1] - pb->cu_q[b];
+    const int Lk = P + n;
+    const int kvh = h / (pb->n_heads / pb->n_kv_heads);
+    const size_t t = (size_t)pb->cu_q[b] + (size_t)i;
+    const uint16_t *qrow = pb->q + (t * pb->n_heads + h) * d;
+    /* visible keys: 0 .. last (inclusive) */
+    const int last = pb->causal ? P + i : Lk - 1;
+
+    double m = -INFINITY;
+    for (int j = 0; j <= last; ++j) {
+        const uint16_t *kr = key_row(pb, pb->cache_k, pb->k, b, kvh, j);
+        double dot = 0.0;
+        for (int e = 0; e < d; ++e)
+            dot += bf16_to_double(qrow[e]) * bf16_to_double(kr[e]);
+        s[j] = pb->scale * dot;
+        if (s[j] > m)
+            m = s[j];
+    }
+    double Z = 0.0;
+    for (int j = 0; j <= last; ++j)
+        Z += exp(s[j] - m);
+
+    double *orow = pb->out + (t * pb->n_heads + h) * d;
+    for (int e = 0; e < d; ++e)
+        orow[e] = 0.0;
+    for (int j = 0; j <= last; ++j) {
+        const double w = exp(s[j] - m) / Z;
+        const uint16_t *vr = key_row(pb, pb->cache_v, pb->v, b, kvh, j);
+        for (int e = 0; e < d; ++e)
+            orow[e] += w * bf16_to_double(vr[e]);
+    }
+    if (pb->lse)
+        pb->lse[t * pb->n_heads + h] = m + log(Z);
+}
+
+/* Sequence that owns flattened token t (cu_q is non-decreasing). */
+static int owner(const int32_t *cu_q, int num_seqs, int64_t t)
+{
+    int lo = 0, hi = num_seqs - 1;
+    while (lo < hi) {
+        int mid = (lo + hi + 1) / 2;
+        if (cu_q[mid] <= t)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    return lo; /* the last sequence starting at or before t owns it */
+}
+
+/*
+ * Returns 0 on success, a negative code for inconsistent metadata:
+ *  -1 bad sizes, -2 cu_seqlens_q not starting at 0 or decreasing,
+ *  -3 cu_seqlens_k inconsistent with cache_offsets + seqlen_q,
+ *  -4 a sequence does not fit its cache slot, -5 a selected row out of range,
+ *  -6 out of memory.
+ *
+ * rows: optional list of (t * n_heads + h) query rows to compute; NULL = all.
+ * Only the selected rows of out/lse are written.  The cache image
+ * (cache_k_out/cache_v_out, may be NULL) is written in full: a copy of the
+ * input cache with every new token's K/V stored at its slot position.
+ */
+int oracle_prefill_attention(
+    const uint16_t *q, const uint16_t *k, const uint16_t *v,
+    const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, const int32_t *cache_offsets,
+    const uint16_t *cache_k, const uint16_t *cache_v,
+    uint16_t *cache_k_out, uint16_t *cache_v_out,
+    double *out, double *lse,
+    int num_seqs, int max_cache_len, int n_heads, int n_kv_heads, int head_dim,
+    double scale, int causal,
+    const int64_t *rows, int64_t n_rows, int n_threads)
+{
+    if (num_seqs < 0 || max_cache_len < 0 || n_heads <= 0 || n_kv_heads <= 0 || head_dim <= 0 ||
+        n_heads % n_kv_heads != 0)
+        return -1;
+    if (num_seqs > 0 && cu_seqlens_q[0] != 0)
+        return -2;
+    for (int b = 0; b < num_seqs; ++b) {
+        int n = cu_seqlens_q[b + 1] - cu_seqlens_q[b];
+        if (n < 0)
+            return -2;
+        if (cu_seqlens_k[b + 1] - cu_seqlens_k[b] != cache_offsets[b] + n)
+            return -3;
+        if (cache_offsets[b] < 0 || cache_offsets[b] + n > max_cache_len)
+            return -4;
+    }
+    const int64_t total_q = num_seqs > 0 ? cu_seqlens_q[num_seqs] : 0;
+
+    problem pb = {q, k, v, cache_k, cache_v, cu_seqlens_q, cache_offsets, out, lse,
+                  num_seqs, max_cache_len, n_heads, n_kv_heads, head_dim, scale, causal};
+
+    const int64_t n_all = total_q * n_heads;
+    const int64_t n_work = rows ? n_rows : n_all;
+    if (rows) {
+        for (int64_t r = 0; r < n_rows; ++r)
+            if (rows[r] < 0 || rows[r] >= n_all)
+                return -5;
+    }
+#ifdef _OPENMP
+    if (n_threads > 0)
+        omp_set_num_threads(n_threads);
+#else
+    (void)n_threads;
+#endif
+    int failed = 0;
+#pragma omp parallel
+    {
+        double *s = (double *)malloc(sizeof(double) * (size_t)(max_cache_len > 0 ? max_cache_len : 1));
+        if (!s) {
+#pragma omp atomic write
+            failed = 1;
+        }
+#pragma omp for schedule(dynamic, 16)
+        for (int64_t w = 0; w < n_work; ++w) {
+            if (!s)
+                continue;
+            const int64_t r = rows ? rows[w] : w;
+            const int64_t t = r / n_heads;
+            const int h = (int)(r % n_heads);
+            const int b = owner(cu_seqlens_q, num_seqs, t);
+            attend_row(&pb, b, (int)(t - cu_seqlens_q[b]), h, s);
+        }
+        free(s);
+    }
+    if (failed)
+        return -6;
+
+    /* The cache image: everything as it was, plus the new tokens at P + i. */
+    const size_t slot = (size_t)max_cache_len * head_dim;
+    const size_t cache_elems = (size_t)num_seqs * n_kv_heads * slot;
+    for (int c = 0; c < 2; ++c) {
+        uint16_t *dst = c == 0 ? cache_k_out : cache_v_out;
+        const uint16_t *src = c == 0 ? cache_k : cache_v;
+        const uint16_t *fresh = c == 0 ? k : v;
+        if (!dst)
+            continue;
+        if (dst != src)
+            memcpy(dst, src, cache_elems * sizeof(uint16_t));
+        for (int b = 0; b < num_seqs; ++b) {
+            const int P = cache_offsets[b];
+            const int n = cu_seqlens_q[b + 1] - cu_seqlens_q[b];
+            for (int kvh = 0; kvh < n_kv_heads; ++kvh)
+                for (int i = 0; i < n; ++i)
+                    memcpy(dst + (((size_t)b * n_kv_heads + kvh) * max_cache_len + (size_t)(P + i)) * head_dim,
+                           fresh + ((size_t)(cu_seqlens_q[b] + i) * n_kv_heads + kvh) * head_dim,
+                           (size_t)head_dim * sizeof(uint16_t));
+        }
+    }
+    return 0;
+}

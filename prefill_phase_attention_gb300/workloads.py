@@ -1,0 +1,211 @@
+"""Seeded synthetic inputs for causal varlen prefill attention.
+
+This module only *builds inputs*: sequence lengths, cumulative offsets, cache
+prefixes and N(0,1) bf16 tensors.  It holds none of the attention arithmetic,
+so the CUDA path and the CPU oracle can both be fed from it without sharing any
+of the method.
+
+Shapes follow the flattened varlen layout of "大模型 Prompt Prefill 阶段的高效
+Batching 与算子排布" (nxmr.cn, §2: prompts packed head-to-tail into one
+[Total_Tokens, ...] stream indexed by cu_seqlens, e.g. lengths 5, 2, 3 give
+cu_seqlens [0, 5, 7, 10]) and the per-sequence cache layout
+(num_heads, seq_len, head_dim) of "Prefill 阶段" worked example (yfxerp.com,
+§2.1).  The five named workloads are the ones this library is measured on:
+
+=================  ===========================================================
+tiny_packed        lengths [5, 2, 3], 4/4 heads, head_dim 32, empty cache
+layer512           one 512-token prompt, 32/32 heads, head_dim 128
+varlen16           16 prompts, lengths ~ U{10..2048}, 32/32 heads, head_dim 128
+chunked_decode     8192-token prompt as 16 chunks of 512, each step packed with
+                   64 one-token decode rows over cached contexts ~ U{256..4096};
+                   GQA 32/8 heads, head_dim 128 (16 launches)
+long32k            one 32768-token prompt, 32/32 heads, head_dim 128
+=================  ===========================================================
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import List, Optional, Sequence
+
+import numpy as np
+import torch
+
+# bf16 pattern used to mark cache entries that no call may read or write
+# (a quiet NaN with a recognisable payload).
+CACHE_SENTINEL_BITS = 0x7FC5
+
+
+@dataclasses.dataclass
+class Step:
+    """One launch: the sequences packed into one flattened batch."""
+
+    seqlens_q: List[int]        # new tokens of each sequence in this launch
+    cache_offsets: List[int]    # tokens already cached for each sequence
+
+    @property
+    def num_seqs(self) -> int:
+        return len(self.seqlens_q)
+
+    @property
+    def total_q(self) -> int:
+        return int(sum(self.seqlens_q))
+
+    def cu_seqlens_q(self) -> List[int]:
+        return [0] + list(np.cumsum(self.seqlens_q, dtype=np.int64).tolist())
+
+    def cu_seqlens_k(self) -> List[int]:
+        lk = [p + n for p, n in zip(self.cache_offsets, self.seqlens_q)]
+        return [0] + list(np.cumsum(lk, dtype=np.int64).tolist())
+
+    def visible_pairs(self, causal: bool = True) -> int:
+        """Number of (query, key) pairs that the causal mask leaves visible."""
+        tot = 0
+        for n, p in zip(self.seqlens_q, self.cache_offsets):
+            tot += n * p + (n * (n + 1) // 2 if causal else n * n)
+        return tot
+
+
+@dataclasses.dataclass
+class Workload:
+    name: str
+    n_heads: int
+    n_kv_heads: int
+    head_dim: int
+    max_cache_len: int
+    steps: List[Step]
+    prefilled: List[int]        # cache tokens already present per slot before step 0
+    seed: int
+    causal: bool = True
+    scale: Optional[float] = None
+
+    def __post_init__(self):
+        if self.scale is None:
+            # 1/sqrt(d) rounded once to fp32, as the kernel receives it.
+            self.scale = float(np.float32(1.0 / math.sqrt(self.head_dim)))
+
+    @property
+    def num_seqs(self) -> int:
+        return self.steps[0].num_seqs
+
+    def flops(self) -> int:
+        """Causal attention FLOPs: 4 * head_dim * n_heads per visible pair."""
+        return 4 * self.head_dim * self.n_heads * sum(s.visible_pairs(self.causal) for s in self.steps)
+
+    def tokens(self) -> int:
+        return sum(s.total_q for s in self.steps)
+
+
+def _tiny_packed() -> Workload:
+    return Workload("tiny_packed", 4, 4, 32, 8, [Step([5, 2, 3], [0, 0, 0])], [0, 0, 0], seed=1)
+
+
+def _layer512() -> Workload:
+    return Workload("layer512", 32, 32, 128, 512, [Step([512], [0])], [0], seed=2)
+
+
+def _varlen16() -> Workload:
+    rng = np.random.default_rng(3)
+    lens = rng.integers(10, 2048, size=16, endpoint=True).tolist()
+    return Workload("varlen16", 32, 32, 128, 2048, [Step(lens, [0] * 16)], [0] * 16, seed=3)
+
+
+def _chunked_decode(prompt: int = 8192, chunk: int = 512, n_decode: int = 64,
+                    lo: int = 256, hi: int = 4096) -> Workload:
+    rng = np.random.default_rng(4)
+    ctx = rng.integers(lo, hi, size=n_decode, endpoint=True).tolist()
+    n_chunks = prompt // chunk
+    steps = []
+    for s in range(n_chunks):
+        steps.append(Step([chunk] + [1] * n_decode, [chunk * s] + [c + s for c in ctx]))
+    cap = max(prompt, max(ctx) + n_chunks)
+    return Workload("chunked_decode", 32, 8, 128, cap, steps, [0] + ctx, seed=4)
+
+
+def _long32k() -> Workload:
+    return Workload("long32k", 32, 32, 128, 32768, [Step([32768], [0])], [0], seed=5)
+
+
+WORKLOADS = {
+    "tiny_packed": _tiny_packed,
+    "layer512": _layer512,
+    "varlen16": _varlen16,
+    "chunked_decode": _chunked_decode,
+    "long32k": _long32k,
+}
+
+
+def get(name: str) -> Workload:
+    return WORKLOADS[name]()
+
+
+def random_workload(seed: int, *, head_dim: int, group: int, n_kv_heads: int = 2,
+                    max_seqs: int = 5, max_len: int = 300, max_prefix: int = 300,
+                    causal: bool = True, allow_empty: bool = True) -> Workload:
+    """Small random varlen batch with random cached prefixes (parity tests)."""
+    rng = np.random.default_rng(seed)
+    b = int(rng.integers(1, max_seqs, endpoint=True))
+    lens = rng.integers(0 if allow_empty else 1, max_len, size=b, endpoint=True).tolist()
+    if sum(lens) == 0:
+        lens[0] = 1
+    pref = rng.integers(0, max_prefix, size=b, endpoint=True).tolist()
+    cap = max(p + n for p, n in zip(pref, lens)) + int(rng.integers(0, 8))
+    return Workload(f"random{seed}", n_kv_heads * group, n_kv_heads, head_dim, cap,
+                    [Step(lens, pref)], pref, seed=1000 + seed, causal=causal)
+
+
+# ---------------------------------------------------------------------------
+# tensors
+# ---------------------------------------------------------------------------
+
+def _randn_bf16(g: torch.Generator, shape: Sequence[int]) -> torch.Tensor:
+    return torch.randn(tuple(shape), generator=g, dtype=torch.float32).to(torch.bfloat16)
+
+
+def make_cache(wl: Workload, g: torch.Generator, sentinel: bool = True):
+    """Cache [num_seqs, n_kv_heads, max_cache_len, head_dim] bf16 (CPU).
+
+    Slot b holds ``wl.prefilled[b]`` seeded N(0,1) tokens; every other entry
+    holds the NaN sentinel (or zero), so a read or a stray write is visible.
+    """
+    shape = (wl.num_seqs, wl.n_kv_heads, wl.max_cache_len, wl.head_dim)
+    caches = []
+    for _ in range(2):
+        c = torch.empty(shape, dtype=torch.bfloat16)
+        if sentinel:
+            c.view(torch.int16).fill_(CACHE_SENTINEL_BITS)
+        else:
+            c.zero_()
+        for b, p in enumerate(wl.prefilled):
+            if p:
+                c[b, :, :p] = _randn_bf16(g, (wl.n_kv_heads, p, wl.head_dim))
+        caches.append(c)
+    return caches[0], caches[1]
+
+
+def make_step_inputs(wl: Workload, step: Step, g: torch.Generator):
+    """q [T,H,d], k/v [T,Hk,d] bf16 and the int32 metadata of one launch (CPU)."""
+    t = step.total_q
+    q = _randn_bf16(g, (t, wl.n_heads, wl.head_dim))
+    k = _randn_bf16(g, (t, wl.n_kv_heads, wl.head_dim))
+    v = _randn_bf16(g, (t, wl.n_kv_heads, wl.head_dim))
+    return dict(
+        q=q, k=k, v=v,
+        cu_seqlens_q=torch.tensor(step.cu_seqlens_q(), dtype=torch.int32),
+        cu_seqlens_k=torch.tensor(step.cu_seqlens_k(), dtype=torch.int32),
+        cache_offsets=torch.tensor(step.cache_offsets, dtype=torch.int32),
+    )
+
+
+def make_inputs(wl: Workload, sentinel: bool = True):
+    """All inputs of a workload: (cache_k, cache_v, [per-step input dicts])."""
+    g = torch.Generator().manual_seed(wl.seed)
+    cache_k, cache_v = make_cache(wl, g, sentinel=sentinel)
+    steps = [make_step_inputs(wl, s, g) for s in wl.steps]
+    return cache_k, cache_v, steps
+
+
+def bf16_bits(t: torch.Tensor) -> np.ndarray:
+    """The raw bf16 bit patterns of a CPU tensor as a uint16 numpy array (no copy)."""
+    assert t.dtype == torch.bfloat16
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)

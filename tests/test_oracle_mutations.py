@@ -1,0 +1,71 @@
+"""The oracle's pins must catch plausible slips.
+
+Each case plants one mistake in a copy of oracle.c (compiled on the CPU into a
+temporary directory), runs the pin tests against the mutant and requires at
+least one of them to fail.  The mutations never move a memory access out of
+bounds.
+"""
+import functools
+import os
+import subprocess
+import types
+
+import pytest
+
+import oracle
+from tests import test_oracle_pins as pins
+
+MUTATIONS = {
+    "causal_bound_drops_self": ("const int last = pb->causal ? P + i : Lk - 1;",
+                                "const int last = pb->causal ? (i > 0 ? P + i - 1 : P + i) : Lk - 1;"),
+    "gqa_interleaved_heads": ("const int kvh = h / (pb->n_heads / pb->n_kv_heads);",
+                              "const int kvh = h % pb->n_kv_heads;"),
+    "scale_dropped": ("s[j] = pb->scale * dot;", "s[j] = dot;"),
+    "scale_divides": ("s[j] = pb->scale * dot;", "s[j] = dot / pb->scale;"),
+    "first_key_dropped_from_sum": ("for (int j = 0; j <= last; ++j)\n        Z += exp(s[j] - m);",
+                                   "for (int j = (last > 0); j <= last; ++j)\n        Z += exp(s[j] - m);"),
+    "value_read_from_keys": ("key_row(pb, pb->cache_v, pb->v, b, kvh, j)",
+                             "key_row(pb, pb->cache_k, pb->k, b, kvh, j)"),
+    "lse_without_max": ("pb->lse[t * pb->n_heads + h] = m + log(Z);",
+                        "pb->lse[t * pb->n_heads + h] = log(Z);"),
+    "cache_written_at_zero": ("* max_cache_len + (size_t)(P + i)) * head_dim",
+                              "* max_cache_len + (size_t)(i)) * head_dim"),
+    "prefix_keys_shifted": ("return cache + (((size_t)b * pb->n_kv_heads + kvh) * pb->cap + (size_t)j) * pb->d;",
+                            "return cache + (((size_t)b * pb->n_kv_heads + kvh) * pb->cap + (size_t)(j > 0 ? j - 1 : 0)) * pb->d;"),
+}
+
+PIN_TESTS = [
+    pins.test_packed_equals_each_sequence_alone,
+    pins.test_length_one_returns_v_and_score,
+    pins.test_two_keys_is_a_logistic_blend,
+    pins.test_causal_rows_sum_to_one,
+    pins.test_equal_keys_give_prefix_mean,
+    pins.test_gqa_contiguous_head_groups,
+    pins.test_causality,
+    pins.test_cache_write_closed_form,
+    pins.test_toy_shapes_and_decode_append,
+    functools.partial(pins.test_matches_torch_sdpa_float64, case="r3", causal=True),
+]
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_pins_catch_mutation(name, tmp_path):
+    old, new = MUTATIONS[name]
+    src = open(oracle._SRC).read()
+    assert src.count(old) >= 1, f"mutation anchor for {name} not found"
+    mutant_src = tmp_path / "oracle_mutant.c"
+    mutant_src.write_text(src.replace(old, new))
+    so = tmp_path / "liboracle_mutant.so"
+    cmd = oracle.build_command()
+    cmd[cmd.index(oracle._SRC)] = str(mutant_src)
+    cmd[cmd.index(oracle._LIB_PATH)] = str(so)
+    subprocess.check_call(cmd)
+    lib = oracle.load_library(str(so))
+    mutant = types.SimpleNamespace(prefill_attention=functools.partial(oracle.prefill_attention, lib=lib))
+    failures = 0
+    for t in PIN_TESTS:
+        try:
+            t(mutant)
+        except Exception:  # an assertion, a rejected call or an overflow all count
+            failures += 1
+    assert failures >= 1, f"no pin caught mutation {name}"

@@ -1,0 +1,334 @@
+"""Pins of the fp64 CPU oracle to facts that do not come from the oracle itself.
+
+Each test fixes the oracle against something the pages or the mathematics
+determine: the printed packing example, closed forms of special cases, the
+row-sum invariant of softmax, isolation and causality invariants, chunked ==
+one-shot, and an independent library routine (PyTorch's float64
+scaled_dot_product_attention).  A plausible slip in the oracle (a dropped
+visible key, a wrong sign or scale, the wrong KV head, a key read from the
+wrong token, a transposed operand) fails at least one of them.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from prefill_phase_attention_gb300 import workloads as W
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def run_oracle(oracle_mod, wl, cache_k, cache_v, inp, rows=None, causal=None):
+    return oracle_mod.prefill_attention(
+        W.bf16_bits(inp["q"]), W.bf16_bits(inp["k"]), W.bf16_bits(inp["v"]),
+        inp["cu_seqlens_q"].numpy(), inp["cu_seqlens_k"].numpy(), inp["cache_offsets"].numpy(),
+        W.bf16_bits(cache_k), W.bf16_bits(cache_v),
+        n_heads=wl.n_heads, n_kv_heads=wl.n_kv_heads, head_dim=wl.head_dim,
+        max_cache_len=wl.max_cache_len, scale=wl.scale,
+        causal=wl.causal if causal is None else causal, rows=rows)
+
+
+def f64(t):
+    return t.to(torch.float64).numpy()
+
+
+def _custom(name, H, Hk, d, lens, pref, cap=None, seed=7, causal=True):
+    cap = cap or max(p + n for p, n in zip(pref, lens))
+    return W.Workload(name, H, Hk, d, cap, [W.Step(list(lens), list(pref))], list(pref),
+                      seed=seed, causal=causal)
+
+
+# ---------------------------------------------------------------- packing ---
+
+def test_packing_example_from_page():
+    g = json.load(open(os.path.join(GOLDEN, "varlen_packing_nxmr.json")))
+    step = W.Step(g["lengths"], [0, 0, 0])
+    assert step.cu_seqlens_q() == g["cu_seqlens"]
+    assert step.total_q == g["total_tokens"]
+    longest = max(g["lengths"])
+    waste = [(longest - n) / longest for n in g["lengths"]]
+    assert np.allclose(waste, g["padded_waste"])
+    ex = g["second_example"]["lengths"]
+    sec = g["second_example"]
+    assert 1 - sum(ex) / (len(ex) * max(ex)) == pytest.approx(sec["batch_waste_approx"], abs=sec["abs_tol"])
+    wl = W.get("tiny_packed")
+    assert wl.steps[0].cu_seqlens_q() == g["cu_seqlens"]
+
+
+def test_packed_equals_each_sequence_alone(oracle_mod):
+    """Bitwise: the oracle does the same per-row arithmetic packed or alone."""
+    wl = W.get("tiny_packed")
+    ck, cv, (inp,) = W.make_inputs(wl)
+    out, lse, _, _ = run_oracle(oracle_mod, wl, ck, cv, inp)
+    cu = inp["cu_seqlens_q"].tolist()
+    for b in range(wl.num_seqs):
+        n = cu[b + 1] - cu[b]
+        sl = slice(cu[b], cu[b + 1])
+        one = _custom("one", wl.n_heads, wl.n_kv_heads, wl.head_dim, [n], [0], cap=wl.max_cache_len)
+        sub = dict(q=inp["q"][sl], k=inp["k"][sl], v=inp["v"][sl],
+                   cu_seqlens_q=torch.tensor([0, n], dtype=torch.int32),
+                   cu_seqlens_k=torch.tensor([0, n], dtype=torch.int32),
+                   cache_offsets=torch.tensor([0], dtype=torch.int32))
+        o1, l1, _, _ = run_oracle(oracle_mod, one, ck[b:b + 1], cv[b:b + 1], sub)
+        assert np.array_equal(o1, out[sl]) and np.array_equal(l1, lse[sl])
+
+
+# ----------------------------------------------------------- closed forms ---
+
+def test_length_one_returns_v_and_score(oracle_mod):
+    """One key: the weight is exactly 1, so out = v and lse = scale * q.k."""
+    wl = _custom("len1", 4, 2, 64, [1, 1, 1], [0, 0, 0])
+    ck, cv, (inp,) = W.make_inputs(wl)
+    out, lse, _, _ = run_oracle(oracle_mod, wl, ck, cv, inp)
+    G = wl.n_heads // wl.n_kv_heads
+    for t in range(3):
+        for h in range(wl.n_heads):
+            assert np.array_equal(out[t, h], f64(inp["v"][t, h // G]))
+            s = wl.scale * float(np.dot(f64(inp["q"][t, h]), f64(inp["k"][t, h // G])))
+            assert lse[t, h] == pytest.approx(s, abs=1e-13)
+
+
+def test_two_keys_is_a_logistic_blend(oracle_mod):
+    """One cached key plus the token itself: w1 = 1 / (1 + exp(s0 - s1))."""
+    wl = _custom("two", 2, 1, 32, [1], [1])
+    ck, cv, (inp,) = W.make_inputs(wl)
+    out, lse, _, _ = run_oracle(oracle_mod, wl, ck, cv, inp)
+    k0, v0 = f64(ck[0, 0, 0]), f64(cv[0, 0, 0])
+    k1, v1 = f64(inp["k"][0, 0]), f64(inp["v"][0, 0])
+    for h in range(2):
+        q = f64(inp["q"][0, h])
+        s0, s1 = wl.scale * q @ k0, wl.scale * q @ k1
+        w1 = 1.0 / (1.0 + math.exp(s0 - s1))
+        assert np.allclose(out[0, h], (1 - w1) * v0 + w1 * v1, rtol=0, atol=1e-13)
+        assert lse[0, h] == pytest.approx(max(s0, s1) + math.log1p(math.exp(-abs(s0 - s1))), abs=1e-13)
+
+
+def test_causal_rows_sum_to_one(oracle_mod):
+    """With every V row equal to 1 the output is the row sum of the weights."""
+    wl = W.random_workload(11, head_dim=64, group=4, n_kv_heads=2, max_prefix=60, max_len=70)
+    ck, cv, (inp,) = W.make_inputs(wl)
+    ones = torch.ones_like(inp["v"])
+    inp = dict(inp, v=ones)
+    cv = torch.ones_like(cv)
+    out, _, _, _ = run_oracle(oracle_mod, wl, ck, cv, inp)
+    assert np.all(np.abs(out - 1.0) <= 1e-15)
+
+
+def test_equal_keys_give_prefix_mean(oracle_mod):
+    """All keys equal: uniform weights over the P+i+1 visible keys."""
+    wl = _custom("eq", 4, 2, 32, [9, 5], [6, 0], cap=20)
+    ck, cv, (inp,) = W.make_inputs(wl)
+    key = inp["k"][0, 0].clone()
+    inp = dict(inp, k=key.expand_as(inp["k"]).contiguous())
+    ck = key.expand_as(ck).contiguous()
+    out, lse, _, _ = run_oracle(oracle_mod, wl, ck, cv, inp)
+    G = wl.n_heads // wl.n_kv_heads
+    cu = inp["cu_seqlens_q"].tolist()
+    for b, P in enumerate([6, 0]):
+        for i in range(cu[b + 1] - cu[b]):
+            t = cu[b] + i
+            for h in range(wl.n_heads):
+                kvh = h // G
+                vals = np.concatenate([f64(cv[b, kvh, :P]), f64(inp["v"][cu[b]:t + 1, kvh])])
+                assert vals.shape[0] == P + i + 1
+                assert np.allclose(out[t, h], vals.mean(axis=0), rtol=0, atol=1e-14)
+                s = wl.scale * float(f64(inp["q"][t, h]) @ f64(key))
+                assert lse[t, h] == pytest.approx(s + math.log(P + i + 1), abs=1e-13)
+
+
+def test_gqa_contiguous_head_groups(oracle_mod):
+    """KV head j holds constant V = j+1: q head h must return h // G + 1."""
+    wl = _custom("gqa", 8, 2, 32, [7, 3], [4, 2], cap=12)
+    ck, cv, (inp,) = W.make_inputs(wl)
+    v = torch.empty_like(inp["v"])
+    for j in range(2):
+        v[:, j] = float(j + 1)
+        cv[:, j] = float(j + 1)
+    out, _, _, _ = run_oracle(oracle_mod, wl, ck, cv, dict(inp, v=v))
+    for h in range(8):
+        assert np.allclose(out[:, h], h // 4 + 1, rtol=0, atol=1e-14)
+
+
+# ------------------------------------------------------------- invariants ---
+
+def test_sequences_are_isolated(oracle_mod):
+    wl = W.get("tiny_packed")
+    ck, cv, (inp,) = W.make_inputs(wl)
+    out, lse, _, _ = run_oracle(oracle_mod, wl, ck, cv, inp)
+    k2, v2 = inp["k"].clone(), inp["v"].clone()
+    k2[5:7] = -k2[5:7] * 3
+    v2[5:7] = v2[5:7] + 1
+    out2, lse2, _, _ = run_oracle(oracle_mod, wl, ck, cv, dict(inp, k=k2, v=v2))
+    keep = np.r_[0:5, 7:10]
+    assert np.array_equal(out[keep], out2[keep]) and np.array_equal(lse[keep], lse2[keep])
+    assert not np.allclose(out[5:7], out2[5:7])
+
+
+def test_causality(oracle_mod):
+    """Changing key/value of new token i leaves rows < i untouched and moves row i."""
+    wl = _custom("causal", 2, 2, 32, [12], [5], cap=17)
+    ck, cv, (inp,) = W.make_inputs(wl)
+    out, _, _, _ = run_oracle(oracle_mod, wl, ck, cv, inp)
+    i = 6
+    k2, v2 = inp["k"].clone(), inp["v"].clone()
+    k2[i] = k2[i] * -2
+    v2[i] = v2[i] + 3
+    out2, _, _, _ = run_oracle(oracle_mod, wl, ck, cv, dict(inp, k=k2, v=v2))
+    assert np.array_equal(out[:i], out2[:i])
+    assert not np.allclose(out[i:], out2[i:])
+    # non-causal: every row sees every key, so the last row is the same either way
+    outn, _, _, _ = run_oracle(oracle_mod, wl, ck, cv, inp, causal=False)
+    assert np.array_equal(outn[-1], out[-1])
+    assert not np.allclose(outn[0], out[0])
+
+
+def test_chunked_equals_one_shot(oracle_mod):
+    """A prompt in 4 chunks over the cache == one launch: outputs and cache, bitwise."""
+    H, Hk, d, n, c = 4, 2, 32, 384, 96
+    one = _custom("one", H, Hk, d, [n], [0], cap=n)
+    ck, cv, (inp,) = W.make_inputs(one)
+    out1, lse1, ck1, cv1 = run_oracle(oracle_mod, one, ck, cv, inp)
+    cur_k, cur_v = W.bf16_bits(ck), W.bf16_bits(cv)
+    outs, lses = [], []
+    for s in range(n // c):
+        sl = slice(s * c, (s + 1) * c)
+        o, l, cur_k, cur_v = oracle_mod.prefill_attention(
+            W.bf16_bits(inp["q"][sl]), W.bf16_bits(inp["k"][sl]), W.bf16_bits(inp["v"][sl]),
+            np.array([0, c], np.int32), np.array([0, s * c + c], np.int32), np.array([s * c], np.int32),
+            cur_k, cur_v, n_heads=H, n_kv_heads=Hk, head_dim=d, max_cache_len=n, scale=one.scale)
+        outs.append(o)
+        lses.append(l)
+    assert np.array_equal(np.concatenate(outs), out1)
+    assert np.array_equal(np.concatenate(lses), lse1)
+    assert np.array_equal(cur_k, ck1) and np.array_equal(cur_v, cv1)
+
+
+def test_row_subset_matches_full_run(oracle_mod):
+    wl = W.random_workload(5, head_dim=32, group=2)
+    ck, cv, (inp,) = W.make_inputs(wl)
+    out, lse, _, _ = run_oracle(oracle_mod, wl, ck, cv, inp)
+    rows = np.arange(0, wl.steps[0].total_q * wl.n_heads, 7, dtype=np.int64)
+    o2, l2, _, _ = run_oracle(oracle_mod, wl, ck, cv, inp, rows=rows)
+    t, h = rows // wl.n_heads, rows % wl.n_heads
+    assert np.array_equal(o2[t, h], out[t, h]) and np.array_equal(l2[t, h], lse[t, h])
+
+
+def test_cache_write_closed_form(oracle_mod):
+    wl = _custom("cache", 4, 2, 32, [3, 0, 5], [2, 4, 0], cap=9)
+    ck, cv, (inp,) = W.make_inputs(wl)
+    _, _, ck2, cv2 = run_oracle(oracle_mod, wl, ck, cv, inp)
+    exp_k, exp_v = W.bf16_bits(ck).copy(), W.bf16_bits(cv).copy()
+    cu = inp["cu_seqlens_q"].tolist()
+    for b, P in enumerate([2, 4, 0]):
+        for i in range(cu[b + 1] - cu[b]):
+            exp_k[b, :, P + i] = W.bf16_bits(inp["k"][cu[b] + i])
+            exp_v[b, :, P + i] = W.bf16_bits(inp["v"][cu[b] + i])
+    assert np.array_equal(ck2, exp_k) and np.array_equal(cv2, exp_v)
+    # entries past each sequence's end still hold the sentinel
+    assert np.all(ck2[0, :, 5:] == W.CACHE_SENTINEL_BITS)
+    assert np.all(cv2[2, :, 5:] == W.CACHE_SENTINEL_BITS)
+
+
+def test_bad_metadata_is_rejected(oracle_mod):
+    wl = _custom("bad", 2, 2, 32, [3, 2], [1, 0], cap=4)
+    ck, cv, (inp,) = W.make_inputs(wl)
+    bad_k = inp["cu_seqlens_k"].clone()
+    bad_k[1] += 1
+    with pytest.raises(ValueError, match="cu_seqlens_k"):
+        run_oracle(oracle_mod, wl, ck, cv, dict(inp, cu_seqlens_k=bad_k))
+    with pytest.raises(ValueError, match="slot"):
+        run_oracle(oracle_mod, wl, ck, cv, dict(inp, cache_offsets=torch.tensor([2, 0], dtype=torch.int32),
+                                                cu_seqlens_k=torch.tensor([0, 5, 7], dtype=torch.int32)))
+
+
+# ------------------------------------------------ toy shapes from the page ---
+
+def test_toy_shapes_and_decode_append(oracle_mod):
+    g = json.load(open(os.path.join(GOLDEN, "toy_cache_shapes_yfxerp.json")))
+    H, d, T = g["num_heads"], g["head_dim"], g["tokens"]
+    assert H * d == g["hidden_size"]
+    wl = _custom("toy", H, H, d, [T], [0], cap=T + 1)
+    ck, cv, (inp,) = W.make_inputs(wl)
+    key = inp["k"][0].clone()
+    inp = dict(inp, k=key.expand_as(inp["k"]).contiguous())
+    out, lse, ck1, cv1 = run_oracle(oracle_mod, wl, ck, cv, inp)
+    assert list(ck1[0, :, :T].shape) == g["cache_shape_after_prefill"]
+    assert list(out[T - 1, 0][None].shape) == g["head_output_shape"]
+    # equal keys: lse - score = ln(#visible keys) -> the last prompt row scores 3 keys
+    s = wl.scale * float(f64(inp["q"][T - 1, 0]) @ f64(key[0]))
+    assert math.exp(lse[T - 1, 0] - s) == pytest.approx(g["last_prompt_row_scores"], rel=1e-12)
+    # decode step: one new token over the 3 cached ones; the cache grows to 4
+    q1 = torch.randn(1, H, d, generator=torch.Generator().manual_seed(3)).to(torch.bfloat16)
+    o, l, ck2, _ = oracle_mod.prefill_attention(
+        W.bf16_bits(q1), W.bf16_bits(key[None]), W.bf16_bits(inp["v"][:1]),
+        np.array([0, 1], np.int32), np.array([0, T + 1], np.int32), np.array([T], np.int32),
+        ck1, cv1, n_heads=H, n_kv_heads=H, head_dim=d, max_cache_len=T + 1, scale=wl.scale)
+    assert np.array_equal(ck2[0, :, :T + 1][:, -1], W.bf16_bits(key))
+    assert ck2[0, :, :T + 1].shape[1] == g["cache_len_after_append"]
+    s = wl.scale * float(f64(q1[0, 0]) @ f64(key[0]))
+    assert math.exp(l[0, 0] - s) == pytest.approx(g["decode_row_scores"], rel=1e-12)
+
+
+def test_flop_and_kv_accounting_matches_pages():
+    g = json.load(open(os.path.join(GOLDEN, "flop_and_kv_accounting.json")))
+    a = g["attention_flops"]
+    for c in a["cases"]:
+        # the pages count full (unmasked) T x T attention: 4 * T^2 * hidden per layer
+        step = W.Step([c["T"]], [0])
+        flops = 4 * step.visible_pairs(causal=False) * a["d"] * a["layers"]
+        assert flops == pytest.approx(c["flops"], rel=c["rel_tol"])
+        # the causal count keeps the lower triangle only (diagonal included)
+        assert step.visible_pairs(causal=True) == c["T"] * (c["T"] + 1) // 2
+    kv = g["kv_bytes_per_token"]
+    for c in kv["cases"]:
+        assert 2 * c["n_kv_heads"] * kv["head_dim"] * kv["bytes_per_elem"] * kv["layers"] == c["bytes"]
+    pl = g["kv_bytes_per_layer"]
+    assert 2 * pl["n_kv_heads"] * pl["tokens"] * pl["head_dim"] * 2 == pl["bytes"]
+
+
+# ------------------------------------------- independent library routine ---
+
+def _sdpa_reference(wl, ck, cv, inp, causal):
+    """PyTorch float64 SDPA per (sequence, head) with an explicit bottom-right mask."""
+    import torch.nn.functional as F
+    T = inp["q"].shape[0]
+    out = torch.full((T, wl.n_heads, wl.head_dim), float("nan"), dtype=torch.float64)
+    cu = inp["cu_seqlens_q"].tolist()
+    off = inp["cache_offsets"].tolist()
+    G = wl.n_heads // wl.n_kv_heads
+    for b in range(len(off)):
+        n, P = cu[b + 1] - cu[b], off[b]
+        if n == 0:
+            continue
+        K = torch.cat([ck[b, :, :P].permute(1, 0, 2), inp["k"][cu[b]:cu[b + 1]]], 0).double()
+        V = torch.cat([cv[b, :, :P].permute(1, 0, 2), inp["v"][cu[b]:cu[b + 1]]], 0).double()
+        Q = inp["q"][cu[b]:cu[b + 1]].double()
+        mask = torch.ones(n, P + n, dtype=torch.bool)
+        if causal:
+            mask = torch.arange(P + n)[None, :] <= (P + torch.arange(n))[:, None]
+        for h in range(wl.n_heads):
+            o = F.scaled_dot_product_attention(Q[None, :, h], K[None, :, h // G], V[None, :, h // G],
+                                               attn_mask=mask[None], scale=wl.scale)
+            out[cu[b]:cu[b + 1], h] = o[0]
+    return out.numpy()
+
+
+@pytest.mark.parametrize("case", ["tiny_packed", "r1", "r2", "r3", "r4"])
+@pytest.mark.parametrize("causal", [True, False])
+def test_matches_torch_sdpa_float64(oracle_mod, case, causal):
+    if case == "tiny_packed":
+        wl = W.get(case)
+    else:
+        i = int(case[1:])
+        wl = W.random_workload(40 + i, head_dim=[32, 64, 128, 32][i - 1], group=[1, 2, 4, 8][i - 1],
+                               max_len=80, max_prefix=90)
+    ck, cv, (inp,) = W.make_inputs(wl)
+    ck = ck.nan_to_num(0.0)
+    cv = cv.nan_to_num(0.0)
+    out, _, _, _ = run_oracle(oracle_mod, wl, ck, cv, inp, causal=causal)
+    ref = _sdpa_reference(wl, ck, cv, inp, causal)
+    assert np.nanmax(np.abs(out - ref)) < 1e-12
+    assert np.array_equal(np.isnan(out), np.isnan(ref))
