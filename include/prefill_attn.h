@@ -1,0 +1,162 @@
+/*
+ * prefill_attn.h -- C ABI of the GB300 (sm_103a) causal varlen prefill-attention
+ * library.
+ *
+ * One call computes, for every sequence b of a flattened varlen batch,
+ *     out = softmax(Q K^T * scale) V
+ * under a causal mask, where the keys/values of b are its P_b = cache_offsets[b]
+ * cached tokens followed by its own n_b new tokens, and writes each new
+ * token's K and V once into the per-sequence KV cache.
+ *
+ * Passages this interface follows (page title, section):
+ *   - flattened [Total_Tokens, ...] stream with cumulative offsets cu_seqlens
+ *     (e.g. [0, 5, 7, 10] for prompts of 5, 2 and 3 tokens); the kernel reads
+ *     cu_seqlens and attends only within one request:
+ *     "大模型 Prompt Prefill 阶段的高效 Batching 与算子排布" (nxmr.cn), §2.
+ *   - chunked prefill: a chunk attends to its cached prefix plus itself, packed
+ *     with one-token decode rows in the same batch: same page §3;
+ *     "大模型推理优化：Prefill、Decode与KV Cache的工程实践" (zskr.cn), §2.2.
+ *   - attention softmax(QK^T/sqrt(d_k))V and the (num_heads, seq_len, head_dim)
+ *     cache layout: "大语言模型推理核心：Prefill与Decode原理及工程优化"
+ *     (yfxerp.com), §2.1-§2.2 and §3.2.
+ *   - causal lower-triangular mask with the masked upper triangle skipped;
+ *     GQA (query heads sharing fewer KV heads): untitled page on prefill/decode
+ *     compute accounting (zwxr.cn), §3.3 and §2.4.
+ *   - prefill as the producer of the KV cache: "Prefill不是热身：大模型推理的真正
+ *     瓶颈与优化核心" (mhpn.cn), §1 and §4.
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers on the current CUDA device, dense
+ *     and row-major in the layout stated; bf16 means IEEE bfloat16 (2 bytes).
+ *     Every pointer must be 16-byte aligned.  The caller owns every buffer and
+ *     the stream; the library keeps only a small per-(device, stream) schedule
+ *     workspace, freed by prefill_attn_release().
+ *   - Functions return a pa_status and never throw.  Arguments checkable on the
+ *     host are checked before anything is launched; on PA_ERR_* nothing was
+ *     launched.  prefill_attn_last_error() gives a one-line reason.
+ *   - Device metadata (cu_seqlens_*, cache_offsets) is read only on the device
+ *     by prefill_attn_varlen.  It is trusted for speed but clamped: a sequence
+ *     whose metadata is inconsistent is skipped (nothing of it is written) and
+ *     the device error word records it (prefill_attn_device_status).
+ *   - out must not alias q, k or v; the caches must not alias k or v.
+ *   - Inputs are assumed finite.  Cache entries outside [0, P_b) of each slot are
+ *     never read, so an uninitialised cache is fine.
+ */
+#ifndef PREFILL_ATTN_H
+#define PREFILL_ATTN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; 0 means the legacy default stream. */
+struct CUstream_st;
+typedef struct CUstream_st *pa_stream_t;
+
+typedef enum {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1,     /* a host-checkable argument is wrong */
+    PA_ERR_UNSUPPORTED = 2,     /* valid, but outside what this build implements */
+    PA_ERR_CUDA = 3,            /* a CUDA runtime/driver call failed */
+    PA_ERR_DEVICE_TIMEOUT = 4,  /* a kernel gave up waiting (bounded wait) */
+    PA_ERR_DEVICE_METADATA = 5  /* device metadata was inconsistent; sequences skipped */
+} pa_status;
+
+/* Bits of the device error word (prefill_attn_device_status). */
+#define PA_DEVERR_METADATA 0x1  /* a sequence's cu_seqlens/cache_offsets were inconsistent */
+#define PA_DEVERR_TIMEOUT 0x2   /* an mbarrier wait ran out of its iteration budget */
+#define PA_DEVERR_OVERFLOW 0x4  /* more work units than the workspace holds */
+
+/*
+ * prefill_attn_varlen -- causal varlen prefill attention with the KV-cache write.
+ *
+ *   q             [total_q, n_heads, head_dim] bf16: queries of the new tokens,
+ *                 sequences packed head to tail (token-major).
+ *   k, v          [total_q, n_kv_heads, head_dim] bf16: keys/values of the NEW
+ *                 tokens only, same packing.
+ *   cu_seqlens_q  [num_seqs + 1] int32: cu_seqlens_q[0] = 0, non-decreasing,
+ *                 cu_seqlens_q[num_seqs] = total_q; sequence b owns rows
+ *                 cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1.  Empty sequences allowed.
+ *   cu_seqlens_k  [num_seqs + 1] int32: cumulative key counts; key count of b is
+ *                 cache_offsets[b] + n_b (prefix + new).
+ *   cache_k/v     [num_seqs, n_kv_heads, max_cache_len, head_dim] bf16: slot b is
+ *                 sequence b.  Positions [0, P_b) are read as the prefix;
+ *                 positions [P_b, P_b + n_b) receive the new k/v (bit copies);
+ *                 nothing else is read or written.
+ *   cache_offsets [num_seqs] int32: P_b, tokens already cached for b, which is
+ *                 also where b's first new token is written.  Requires
+ *                 P_b + n_b <= max_cache_len.
+ *   out           [total_q, n_heads, head_dim] bf16: attention output, rounded to
+ *                 nearest even from fp32.
+ *   lse           [total_q, n_heads] fp32 or NULL: natural log of
+ *                 sum_j exp(scale * q . k_j) over the visible keys.
+ *   num_seqs      batch size (>= 0; 0 is a no-op).
+ *   total_q       rows of q/k/v/out (= cu_seqlens_q[num_seqs]; the tensor maps need it).
+ *   max_cache_len slot capacity of the caches (>= 1).
+ *   n_heads, n_kv_heads  n_heads % n_kv_heads == 0; query head h reads KV head
+ *                 h / (n_heads / n_kv_heads).  n_heads / n_kv_heads <= 128.
+ *   head_dim      32, 64 or 128.
+ *   scale         finite, > 0; usually 1/sqrt(head_dim).
+ *   causal        1: query i of b sits at absolute position P_b + i and sees keys
+ *                 0 .. P_b + i; 0: every query of b sees all P_b + n_b keys.
+ *   stream        the CUDA stream everything is enqueued on.
+ *
+ * Asynchronous: PA_OK means the work was enqueued on `stream`, not that it has
+ * finished.  The call allocates (stream-ordered) only when the schedule
+ * workspace for this (device, stream) must grow.
+ */
+pa_status prefill_attn_varlen(
+    const void *q, const void *k, const void *v,
+    const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+    void *cache_k, void *cache_v, const int32_t *cache_offsets,
+    void *out, float *lse,
+    int num_seqs, int total_q, int max_cache_len,
+    int n_heads, int n_kv_heads, int head_dim,
+    float scale, int causal, pa_stream_t stream);
+
+/*
+ * prefill_attn_varlen_validate -- strict host-side check of the same arguments.
+ * Copies the three metadata arrays to the host (synchronises `stream`) and
+ * checks every rule stated above: PA_OK or PA_ERR_INVALID_ARG with the reason
+ * in prefill_attn_last_error().  Launches nothing.  Meant for tests and debug
+ * builds of callers; the fast path does not call it.
+ */
+pa_status prefill_attn_varlen_validate(
+    const void *q, const void *k, const void *v,
+    const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+    void *cache_k, void *cache_v, const int32_t *cache_offsets,
+    void *out, float *lse,
+    int num_seqs, int total_q, int max_cache_len,
+    int n_heads, int n_kv_heads, int head_dim,
+    float scale, int causal, pa_stream_t stream);
+
+/*
+ * prefill_attn_device_status -- synchronise `stream`, then read and clear the
+ * device error word of the current device's (device, stream) workspace.
+ * *flags receives the PA_DEVERR_* bits (may be NULL).  Returns PA_OK when the
+ * word was zero, PA_ERR_DEVICE_TIMEOUT if the timeout bit was set, else
+ * PA_ERR_DEVICE_METADATA.
+ */
+pa_status prefill_attn_device_status(pa_stream_t stream, int32_t *flags);
+
+/* Free every workspace this library allocated (all devices, all streams).
+ * The caller must make sure no launch that uses them is still running. */
+void prefill_attn_release(void);
+
+/* Static string naming a status code. */
+const char *prefill_attn_status_string(pa_status s);
+
+/* Reason for the last PA_ERR_* returned on this thread ("" if none). */
+const char *prefill_attn_last_error(void);
+
+/* Number of kernel launches the last successful prefill_attn_varlen call on
+ * this thread enqueued (0 for an empty batch). */
+int prefill_attn_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PREFILL_ATTN_H */

@@ -1,0 +1,138 @@
+"""ctypes binding of include/prefill_attn.h (argument marshalling only).
+
+Every function here has the name of the C entry point it calls.  Tensors are
+PyTorch CUDA tensors; their data pointers, sizes and the current CUDA stream
+are passed straight to the library, which does all of the work on the GPU.
+There is no fallback: if the compiled library is missing, loading fails.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+PA_OK = 0
+STATUS = {0: "PA_OK", 1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED", 3: "PA_ERR_CUDA",
+          4: "PA_ERR_DEVICE_TIMEOUT", 5: "PA_ERR_DEVICE_METADATA"}
+DEVERR_METADATA, DEVERR_TIMEOUT, DEVERR_OVERFLOW = 0x1, 0x2, 0x4
+
+# Entry points declared in include/prefill_attn.h: name -> (restype, argtypes)
+_P, _I, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+_VARLEN_ARGS = [_P] * 10 + [_I] * 6 + [_F, _I, _P]
+SIGNATURES = {
+    "prefill_attn_varlen": (_I, _VARLEN_ARGS),
+    "prefill_attn_varlen_validate": (_I, _VARLEN_ARGS),
+    "prefill_attn_device_status": (_I, [_P, ctypes.POINTER(ctypes.c_int32)]),
+    "prefill_attn_release": (None, []),
+    "prefill_attn_status_string": (ctypes.c_char_p, [_I]),
+    "prefill_attn_last_error": (ctypes.c_char_p, []),
+    "prefill_attn_last_launch_count": (_I, []),
+}
+
+_lib = None
+
+
+class PrefillAttnError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load(path: Optional[str] = None):
+    """Load (once) the compiled library and bind every declared entry point."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or library_path()
+    if not os.path.exists(p):
+        raise RuntimeError(f"prefill_attn library not built: {p} is missing "
+                           "(run prefill_phase_attention_gb300.build.build())")
+    lib = ctypes.CDLL(p)
+    for name, (res, args) in SIGNATURES.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def _check(status: int):
+    if status != PA_OK:
+        raise PrefillAttnError(status, load().prefill_attn_last_error().decode())
+
+
+def _stream_handle(stream) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _varlen_args(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_k, cache_v, cache_offsets, out, lse,
+                 scale, causal, stream):
+    for name, t, dt in (("q", q, torch.bfloat16), ("k", k, torch.bfloat16), ("v", v, torch.bfloat16),
+                        ("cache_k", cache_k, torch.bfloat16), ("cache_v", cache_v, torch.bfloat16),
+                        ("out", out, torch.bfloat16), ("cu_seqlens_q", cu_seqlens_q, torch.int32),
+                        ("cu_seqlens_k", cu_seqlens_k, torch.int32), ("cache_offsets", cache_offsets, torch.int32)):
+        if t.dtype != dt or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA {dt} tensor")
+    if lse is not None and (lse.dtype != torch.float32 or not lse.is_cuda or not lse.is_contiguous()):
+        raise ValueError("lse must be a contiguous CUDA float32 tensor")
+    if q.dim() != 3 or k.dim() != 3 or cache_k.dim() != 4:
+        raise ValueError("q/k/v are [total_q, heads, head_dim]; caches are [num_seqs, kv_heads, cap, head_dim]")
+    total_q, n_heads, head_dim = q.shape
+    n_kv_heads = k.shape[1]
+    num_seqs = cache_offsets.numel()
+    if scale is None:
+        scale = head_dim ** -0.5
+    return (q.data_ptr(), k.data_ptr(), v.data_ptr(), cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr(),
+            cache_k.data_ptr(), cache_v.data_ptr(), cache_offsets.data_ptr(), out.data_ptr(),
+            None if lse is None else lse.data_ptr(),
+            num_seqs, total_q, cache_k.shape[2], n_heads, n_kv_heads, head_dim,
+            float(scale), int(bool(causal)), _stream_handle(stream))
+
+
+def prefill_attn_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_k, cache_v, cache_offsets, out,
+                        lse=None, *, scale: Optional[float] = None, causal: bool = True, stream=None) -> None:
+    """Enqueue causal varlen prefill attention + the KV-cache write on `stream`.
+
+    Shapes: q/out [total_q, n_heads, head_dim], k/v [total_q, n_kv_heads, head_dim] (bf16),
+    cache_k/v [num_seqs, n_kv_heads, max_cache_len, head_dim] (bf16), cu_seqlens_q/k
+    [num_seqs+1], cache_offsets [num_seqs] (int32), lse [total_q, n_heads] fp32 or None.
+    """
+    args = _varlen_args(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_k, cache_v, cache_offsets, out, lse,
+                        scale, causal, stream)
+    _check(load().prefill_attn_varlen(*args))
+
+
+def prefill_attn_varlen_validate(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_k, cache_v, cache_offsets,
+                                 out, lse=None, *, scale: Optional[float] = None, causal: bool = True,
+                                 stream=None) -> None:
+    """Strict (host-synchronising) check of the same arguments; raises on failure."""
+    args = _varlen_args(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_k, cache_v, cache_offsets, out, lse,
+                        scale, causal, stream)
+    _check(load().prefill_attn_varlen_validate(*args))
+
+
+def prefill_attn_device_status(stream=None) -> int:
+    """Synchronise, read and clear the device error word; returns its PA_DEVERR_* bits."""
+    flags = ctypes.c_int32(0)
+    st = load().prefill_attn_device_status(_stream_handle(stream), ctypes.byref(flags))
+    if st not in (PA_OK, 4, 5):
+        _check(st)
+    return flags.value
+
+
+def prefill_attn_release() -> None:
+    load().prefill_attn_release()
+
+
+def prefill_attn_last_launch_count() -> int:
+    return load().prefill_attn_last_launch_count()

@@ -1,0 +1,286 @@
+// api.cu -- the C ABI (include/prefill_attn.h): argument checks, the
+// per-(device, stream) schedule workspace, and the launch sequence.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <utility>
+#include <vector>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "prefill_attn.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+thread_local int g_last_launches = 0;
+
+pa_status fail(pa_status s, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return s;
+}
+
+pa_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(PA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+struct Workspace {
+    void* ptr = nullptr;
+    size_t bytes = 0;
+    int max_units = 0;
+    int max_seqs = 0;
+};
+
+std::mutex g_mu;
+std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+size_t ws_bytes(int max_seqs, int max_units) {
+    return align_up(sizeof(pa::WorkspaceHeader), 16) + (size_t)max_seqs * sizeof(pa::SeqInfo) +
+           (size_t)max_units * sizeof(pa::Unit);
+}
+
+pa::SeqInfo* ws_seqs(const Workspace& w) {
+    return reinterpret_cast<pa::SeqInfo*>(static_cast<char*>(w.ptr) + align_up(sizeof(pa::WorkspaceHeader), 16));
+}
+
+pa::Unit* ws_units(const Workspace& w) { return reinterpret_cast<pa::Unit*>(ws_seqs(w) + w.max_seqs); }
+
+// Returns the workspace of (device, stream), growing it (stream-ordered) when needed.
+pa_status get_workspace(int dev, cudaStream_t st, int num_seqs, int max_units, Workspace** out) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    Workspace& w = g_ws[std::make_pair(dev, st)];
+    if (w.ptr && w.max_seqs >= num_seqs && w.max_units >= max_units) {
+        *out = &w;
+        return PA_OK;
+    }
+    Workspace nw;
+    nw.max_seqs = std::max(num_seqs, std::max(w.max_seqs, 64));
+    nw.max_units = std::max(max_units, std::max(w.max_units, 4096));
+    nw.bytes = ws_bytes(nw.max_seqs, nw.max_units);
+    cudaError_t e = cudaMallocAsync(&nw.ptr, nw.bytes, st);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync(workspace)");
+    e = cudaMemsetAsync(nw.ptr, 0, sizeof(pa::WorkspaceHeader), st);
+    if (e == cudaSuccess && w.ptr)  // keep sticky error bits across a regrow
+        e = cudaMemcpyAsync(nw.ptr, w.ptr, sizeof(int), cudaMemcpyDeviceToDevice, st);
+    if (e != cudaSuccess) {
+        cudaFreeAsync(nw.ptr, st);
+        return cuda_fail(e, "workspace init");
+    }
+    if (w.ptr) cudaFreeAsync(w.ptr, st);
+    w = nw;
+    *out = &w;
+    return PA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+pa_status check_args(const void* q, const void* k, const void* v, const int32_t* cu_q, const int32_t* cu_k,
+                     const void* cache_k, const void* cache_v, const int32_t* off, const void* out,
+                     const float* lse, int num_seqs, int total_q, int max_cache_len, int n_heads,
+                     int n_kv_heads, int head_dim, float scale, int causal) {
+    if (num_seqs < 0) return fail(PA_ERR_INVALID_ARG, "num_seqs must be >= 0 (got %d)", num_seqs);
+    if (total_q < 0) return fail(PA_ERR_INVALID_ARG, "total_q must be >= 0 (got %d)", total_q);
+    if (max_cache_len < 1) return fail(PA_ERR_INVALID_ARG, "max_cache_len must be >= 1 (got %d)", max_cache_len);
+    if (n_heads < 1 || n_kv_heads < 1 || n_heads % n_kv_heads != 0)
+        return fail(PA_ERR_INVALID_ARG, "n_heads (%d) must be a positive multiple of n_kv_heads (%d)", n_heads,
+                    n_kv_heads);
+    if (n_heads / n_kv_heads > pa::kBlockM)
+        return fail(PA_ERR_UNSUPPORTED, "n_heads / n_kv_heads = %d exceeds %d", n_heads / n_kv_heads, pa::kBlockM);
+    if (head_dim != 32 && head_dim != 64 && head_dim != 128)
+        return fail(PA_ERR_UNSUPPORTED, "head_dim must be 32, 64 or 128 (got %d)", head_dim);
+    if (!(scale > 0.f) || !std::isfinite(scale))
+        return fail(PA_ERR_INVALID_ARG, "scale must be finite and > 0 (got %g)", (double)scale);
+    if (causal != 0 && causal != 1) return fail(PA_ERR_INVALID_ARG, "causal must be 0 or 1 (got %d)", causal);
+    if (num_seqs == 0 || total_q == 0) return PA_OK;  // nothing is read or written
+    const void* ptrs[] = {q, k, v, cu_q, cu_k, cache_k, cache_v, off, out};
+    const char* names[] = {"q", "k", "v", "cu_seqlens_q", "cu_seqlens_k", "cache_k", "cache_v", "cache_offsets", "out"};
+    for (int i = 0; i < 9; ++i) {
+        if (!ptrs[i]) return fail(PA_ERR_INVALID_ARG, "%s is NULL", names[i]);
+        if (i != 3 && i != 4 && i != 7 && !aligned16(ptrs[i]))
+            return fail(PA_ERR_INVALID_ARG, "%s must be 16-byte aligned", names[i]);
+    }
+    if ((reinterpret_cast<uintptr_t>(cu_q) | reinterpret_cast<uintptr_t>(cu_k) | reinterpret_cast<uintptr_t>(off)) & 3u)
+        return fail(PA_ERR_INVALID_ARG, "metadata arrays must be 4-byte aligned");
+    if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return fail(PA_ERR_INVALID_ARG, "lse must be 4-byte aligned");
+    if (out == q || out == k || out == v) return fail(PA_ERR_INVALID_ARG, "out must not alias q, k or v");
+    if (cache_k == k || cache_k == v || cache_v == k || cache_v == v || cache_k == cache_v)
+        return fail(PA_ERR_INVALID_ARG, "caches must be distinct and must not alias k or v");
+    // Row counts used by 32-bit kernel index arithmetic.
+    if ((long long)total_q * n_heads >= (1LL << 31))
+        return fail(PA_ERR_UNSUPPORTED, "total_q * n_heads must be < 2^31");
+    if ((long long)num_seqs * n_kv_heads * max_cache_len >= (1LL << 31))
+        return fail(PA_ERR_UNSUPPORTED, "num_seqs * n_kv_heads * max_cache_len must be < 2^31");
+    return PA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* prefill_attn_status_string(pa_status s) {
+    switch (s) {
+        case PA_OK: return "PA_OK";
+        case PA_ERR_INVALID_ARG: return "PA_ERR_INVALID_ARG";
+        case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED";
+        case PA_ERR_CUDA: return "PA_ERR_CUDA";
+        case PA_ERR_DEVICE_TIMEOUT: return "PA_ERR_DEVICE_TIMEOUT";
+        case PA_ERR_DEVICE_METADATA: return "PA_ERR_DEVICE_METADATA";
+    }
+    return "PA_ERR_UNKNOWN";
+}
+
+const char* prefill_attn_last_error(void) { return g_last_error.c_str(); }
+
+int prefill_attn_last_launch_count(void) { return g_last_launches; }
+
+pa_status prefill_attn_varlen(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q,
+                              const int32_t* cu_seqlens_k, void* cache_k, void* cache_v,
+                              const int32_t* cache_offsets, void* out, float* lse, int num_seqs, int total_q,
+                              int max_cache_len, int n_heads, int n_kv_heads, int head_dim, float scale,
+                              int causal, pa_stream_t stream_) {
+    g_last_error.clear();
+    g_last_launches = 0;
+    pa_status s = check_args(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_k, cache_v, cache_offsets, out, lse,
+                             num_seqs, total_q, max_cache_len, n_heads, n_kv_heads, head_dim, scale, causal);
+    if (s != PA_OK) return s;
+    if (num_seqs == 0 || total_q == 0) return PA_OK;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+
+    const int group = n_heads / n_kv_heads;
+    const int tpu = pa::kBlockM / group;
+    const long long max_units_ll = (long long)n_kv_heads * ((total_q + tpu - 1) / tpu + num_seqs);
+    if (max_units_ll >= (1LL << 31)) return fail(PA_ERR_UNSUPPORTED, "too many work units");
+    Workspace* ws = nullptr;
+    s = get_workspace(dev, stream, num_seqs, (int)max_units_ll, &ws);
+    if (s != PA_OK) return s;
+
+    pa::ScheduleArgs sa;
+    sa.cu_seqlens_q = cu_seqlens_q;
+    sa.cu_seqlens_k = cu_seqlens_k;
+    sa.cache_offsets = cache_offsets;
+    sa.hdr = static_cast<pa::WorkspaceHeader*>(ws->ptr);
+    sa.seqs = ws_seqs(*ws);
+    sa.units = ws_units(*ws);
+    sa.num_seqs = num_seqs;
+    sa.total_q = total_q;
+    sa.max_cache_len = max_cache_len;
+    sa.n_kv_heads = n_kv_heads;
+    sa.group = group;
+    sa.causal = causal;
+    sa.max_units = ws->max_units;
+    e = pa::launch_build_schedule(sa, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "schedule launch");
+
+    pa::SimpleParams p;
+    p.q = static_cast<const __nv_bfloat16*>(q);
+    p.k = static_cast<const __nv_bfloat16*>(k);
+    p.v = static_cast<const __nv_bfloat16*>(v);
+    p.cache_k = static_cast<__nv_bfloat16*>(cache_k);
+    p.cache_v = static_cast<__nv_bfloat16*>(cache_v);
+    p.out = static_cast<__nv_bfloat16*>(out);
+    p.lse = lse;
+    p.hdr = sa.hdr;
+    p.seqs = sa.seqs;
+    p.units = sa.units;
+    p.n_heads = n_heads;
+    p.n_kv_heads = n_kv_heads;
+    p.group = group;
+    p.max_cache_len = max_cache_len;
+    p.scale = scale;
+    p.causal = causal;
+    e = pa::launch_attn_simple(p, head_dim, (int)max_units_ll, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "attention launch");
+    g_last_launches = 2;
+    return PA_OK;
+}
+
+pa_status prefill_attn_varlen_validate(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q,
+                                       const int32_t* cu_seqlens_k, void* cache_k, void* cache_v,
+                                       const int32_t* cache_offsets, void* out, float* lse, int num_seqs,
+                                       int total_q, int max_cache_len, int n_heads, int n_kv_heads, int head_dim,
+                                       float scale, int causal, pa_stream_t stream_) {
+    g_last_error.clear();
+    pa_status s = check_args(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_k, cache_v, cache_offsets, out, lse,
+                             num_seqs, total_q, max_cache_len, n_heads, n_kv_heads, head_dim, scale, causal);
+    if (s != PA_OK || num_seqs == 0) return s;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    std::vector<int32_t> cq(num_seqs + 1), ck(num_seqs + 1), of(num_seqs);
+    cudaError_t e = cudaMemcpyAsync(cq.data(), cu_seqlens_q, cq.size() * 4, cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(ck.data(), cu_seqlens_k, ck.size() * 4, cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(of.data(), cache_offsets, of.size() * 4, cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(e, "reading metadata");
+    if (cq[0] != 0) return fail(PA_ERR_INVALID_ARG, "cu_seqlens_q[0] = %d, must be 0", cq[0]);
+    if (cq[num_seqs] != total_q)
+        return fail(PA_ERR_INVALID_ARG, "cu_seqlens_q[num_seqs] = %d but total_q = %d", cq[num_seqs], total_q);
+    for (int b = 0; b < num_seqs; ++b) {
+        const long long n = (long long)cq[b + 1] - cq[b];
+        if (n < 0) return fail(PA_ERR_INVALID_ARG, "cu_seqlens_q decreases at sequence %d", b);
+        if (of[b] < 0) return fail(PA_ERR_INVALID_ARG, "cache_offsets[%d] = %d < 0", b, of[b]);
+        if ((long long)ck[b + 1] - ck[b] != (long long)of[b] + n)
+            return fail(PA_ERR_INVALID_ARG,
+                        "sequence %d: cu_seqlens_k gives %lld keys, cache_offsets + seqlen_q = %lld", b,
+                        (long long)ck[b + 1] - ck[b], (long long)of[b] + n);
+        if ((long long)of[b] + n > max_cache_len)
+            return fail(PA_ERR_INVALID_ARG, "sequence %d: %lld tokens exceed max_cache_len %d", b,
+                        (long long)of[b] + n, max_cache_len);
+    }
+    return PA_OK;
+}
+
+pa_status prefill_attn_device_status(pa_stream_t stream_, int32_t* flags) {
+    g_last_error.clear();
+    if (flags) *flags = 0;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    void* ptr = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        auto it = g_ws.find(std::make_pair(dev, stream));
+        if (it == g_ws.end() || !it->second.ptr) return PA_OK;
+        ptr = it->second.ptr;
+    }
+    int32_t word = 0, zero = 0;
+    e = cudaMemcpy(&word, ptr, sizeof word, cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess) e = cudaMemcpy(ptr, &zero, sizeof zero, cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+    if (flags) *flags = word;
+    if (word == 0) return PA_OK;
+    if (word & PA_DEVERR_TIMEOUT) return fail(PA_ERR_DEVICE_TIMEOUT, "device error word 0x%x", word);
+    return fail(PA_ERR_DEVICE_METADATA, "device error word 0x%x", word);
+}
+
+void prefill_attn_release(void) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    int cur = 0;
+    cudaGetDevice(&cur);
+    for (auto& kv : g_ws) {
+        if (!kv.second.ptr) continue;
+        cudaSetDevice(kv.first.first);
+        cudaFree(kv.second.ptr);
+    }
+    cudaSetDevice(cur);
+    g_ws.clear();
+}
+
+}  // extern "C"

@@ -1,0 +1,82 @@
+"""The C ABI: the library loads, exports every declared entry point, and
+rejects host-checkable argument errors before touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from prefill_phase_attention_gb300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load()
+
+
+def declared_functions():
+    names = []
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"\b(prefill_attn_\w+)\s*\(", src)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert "prefill_attn_varlen" in names and len(names) >= 7
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+    assert set(binding.SIGNATURES) >= set(names), "binding lacks a declared entry point"
+
+
+def test_status_strings(lib):
+    for code, name in binding.STATUS.items():
+        assert lib.prefill_attn_status_string(code).decode() == name
+
+
+def _call(lib, **kw):
+    a = dict(q=16, k=32, v=48, cu_q=64, cu_k=80, ck=96, cv=112, off=128, out=144, lse=None,
+             num_seqs=1, total_q=4, cap=8, H=4, Hk=2, d=64, scale=0.125, causal=1, stream=None)
+    a.update(kw)
+    return lib.prefill_attn_varlen(a["q"], a["k"], a["v"], a["cu_q"], a["cu_k"], a["ck"], a["cv"], a["off"],
+                                   a["out"], a["lse"], a["num_seqs"], a["total_q"], a["cap"], a["H"], a["Hk"],
+                                   a["d"], a["scale"], a["causal"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,status,msg", [
+    (dict(d=48), 2, "head_dim"),
+    (dict(H=6, Hk=4), 1, "multiple"),
+    (dict(H=258, Hk=1), 2, "exceeds"),
+    (dict(scale=0.0), 1, "scale"),
+    (dict(scale=float("inf")), 1, "scale"),
+    (dict(causal=2), 1, "causal"),
+    (dict(num_seqs=-1), 1, "num_seqs"),
+    (dict(cap=0), 1, "max_cache_len"),
+    (dict(q=None), 1, "q is NULL"),
+    (dict(k=33), 1, "aligned"),
+    (dict(out=16), 1, "alias"),
+    (dict(ck=32), 1, "alias"),
+])
+def test_host_checks_reject_before_launch(lib, kw, status, msg):
+    assert _call(lib, **kw) == status
+    assert msg in lib.prefill_attn_last_error().decode()
+
+
+def test_empty_batch_is_a_no_op(lib):
+    assert _call(lib, num_seqs=0, q=None, k=None, v=None) == 0
+    assert lib.prefill_attn_last_launch_count() == 0
+    assert _call(lib, total_q=0) == 0
+
+
+def test_python_binding_refuses_cpu_tensors(lib):
+    import torch
+    t = torch.zeros(4, 2, 32, dtype=torch.bfloat16)
+    i = torch.zeros(2, dtype=torch.int32)
+    with pytest.raises(ValueError):
+        binding.prefill_attn_varlen(t, t, t, i, i, t[None], t[None], i[:1], t)

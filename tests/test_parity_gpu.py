@@ -1,0 +1,124 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 CPU oracle on the
+same seeded inputs.  out/lse within the stated tolerances, KV cache bit-exact,
+no write outside any output buffer."""
+import numpy as np
+import pytest
+import torch
+
+from prefill_phase_attention_gb300 import binding
+from prefill_phase_attention_gb300 import workloads as W
+from tests import parity as PT
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(oracle_mod):
+    from prefill_phase_attention_gb300 import build
+    build.build()
+    binding.load()
+    if not torch.cuda.is_available():
+        pytest.fail("GPU tests need CUDA")
+
+
+def _run_single_step(wl, rows=None):
+    ck, cv, (inp,) = W.make_inputs(wl)
+    ck_d = PT.Guarded(ck.shape, torch.bfloat16, fill=ck)
+    cv_d = PT.Guarded(cv.shape, torch.bfloat16, fill=cv)
+    out, lse = PT.run_step_gpu(wl, inp, ck_d.t, cv_d.t)
+    assert ck_d.guards_intact() and cv_d.guards_intact(), "write outside the cache"
+    ref_out, ref_lse, ref_ck, ref_cv = PT.oracle_step(wl, inp, W.bf16_bits(ck), W.bf16_bits(cv), rows=rows)
+    stats = PT.compare(out, lse, ref_out, ref_lse, rows=rows, label=wl.name)
+    assert np.array_equal(W.bf16_bits(ck_d.t.cpu()), ref_ck), "cache_k differs"
+    assert np.array_equal(W.bf16_bits(cv_d.t.cpu()), ref_cv), "cache_v differs"
+    return stats
+
+
+@pytest.mark.parametrize("name", ["tiny_packed", "layer512", "varlen16"])
+def test_named_workload_full(name):
+    _run_single_step(W.get(name))
+
+
+def test_long32k_sampled():
+    wl = W.get("long32k")
+    rows = PT.sample_rows(wl.steps[0], wl.n_heads, 96, seed=5)
+    _run_single_step(wl, rows=rows)
+
+
+def test_chunked_decode_all_steps():
+    """16 launches: each packs one 512-token chunk (prefix from the cache written by
+    the previous launches) with 64 one-token decode rows, GQA 32/8."""
+    wl = W.get("chunked_decode")
+    ck, cv, steps = W.make_inputs(wl)
+    ck_d, cv_d = ck.cuda(), cv.cuda()
+    ok, ov = W.bf16_bits(ck).copy(), W.bf16_bits(cv).copy()
+    for s, inp in enumerate(steps):
+        out, lse = PT.run_step_gpu(wl, inp, ck_d, cv_d)
+        st = wl.steps[s]
+        rows = PT.sample_rows(st, wl.n_heads, 24, seed=100 + s)
+        # every decode row of two heads as well
+        dec = np.arange(512, 512 + 64, dtype=np.int64)
+        rows = np.unique(np.concatenate([rows, dec * wl.n_heads + (s % wl.n_heads), dec * wl.n_heads + 31]))
+        ref_out, ref_lse, ok, ov = PT.oracle_step(wl, inp, ok, ov, rows=rows)
+        PT.compare(out, lse, ref_out, ref_lse, rows=rows, label=f"chunked step {s}")
+    assert np.array_equal(W.bf16_bits(ck_d.cpu()), ok)
+    assert np.array_equal(W.bf16_bits(cv_d.cpu()), ov)
+
+
+@pytest.mark.parametrize("seed", range(12))
+@pytest.mark.parametrize("d", [32, 64, 128])
+@pytest.mark.parametrize("group", [1, 2, 4, 8])
+def test_random_shapes(seed, d, group):
+    wl = W.random_workload(seed * 31 + d + group, head_dim=d, group=group, n_kv_heads=2,
+                           causal=(seed % 4 != 3))
+    _run_single_step(wl)
+
+
+def test_length_one_is_bit_exact():
+    """One visible key: weight 1, so out must be exactly bf16(v) for every head."""
+    wl = W.Workload("len1", 8, 2, 128, 4, [W.Step([1, 1, 1, 1], [0, 0, 0, 0])], [0, 0, 0, 0], seed=9)
+    ck, cv, (inp,) = W.make_inputs(wl)
+    out, _ = PT.run_step_gpu(wl, inp, ck.cuda(), cv.cuda())
+    exp = inp["v"].repeat_interleave(4, dim=1)
+    assert torch.equal(out.cpu().view(torch.int16), exp.view(torch.int16))
+
+
+def test_chunked_equals_one_shot_on_gpu():
+    H, Hk, d, n, c = 8, 2, 128, 1024, 256
+    one = W.Workload("one", H, Hk, d, n, [W.Step([n], [0])], [0], seed=21)
+    ck, cv, (inp,) = W.make_inputs(one)
+    ck1, cv1 = ck.cuda(), cv.cuda()
+    out1, lse1 = PT.run_step_gpu(one, inp, ck1, cv1)
+    ck2, cv2 = ck.cuda(), cv.cuda()
+    for s in range(n // c):
+        sl = slice(s * c, (s + 1) * c)
+        sub = dict(q=inp["q"][sl], k=inp["k"][sl], v=inp["v"][sl],
+                   cu_seqlens_q=torch.tensor([0, c], dtype=torch.int32),
+                   cu_seqlens_k=torch.tensor([0, s * c + c], dtype=torch.int32),
+                   cache_offsets=torch.tensor([s * c], dtype=torch.int32))
+        o, l = PT.run_step_gpu(one, sub, ck2, cv2)
+        assert (o.float() - out1[sl].float()).abs().max().item() <= PT.OUT_MAX_ABS
+        assert (l - lse1[sl]).abs().max().item() <= PT.LSE_MAX_ABS
+    assert torch.equal(ck1.view(torch.int16), ck2.view(torch.int16))
+    assert torch.equal(cv1.view(torch.int16), cv2.view(torch.int16))
+
+
+def test_inconsistent_device_metadata_is_flagged_and_skipped():
+    wl = W.get("tiny_packed")
+    ck, cv, (inp,) = W.make_inputs(wl)
+    dev = {k: v.cuda() for k, v in inp.items()}
+    bad_k = dev["cu_seqlens_k"].clone()
+    bad_k[2] += 1  # sequence 1 claims one key too many
+    out = torch.zeros(10, 4, 32, dtype=torch.bfloat16, device="cuda")
+    ck_d, cv_d = ck.cuda(), cv.cuda()
+    binding.prefill_attn_varlen(dev["q"], dev["k"], dev["v"], dev["cu_seqlens_q"], bad_k, ck_d, cv_d,
+                                dev["cache_offsets"], out, None, scale=wl.scale)
+    flags = binding.prefill_attn_device_status()
+    assert flags & binding.DEVERR_METADATA
+    assert binding.prefill_attn_device_status() == 0  # read clears it
+    # sequence 1 wrote nothing, sequences 0 and 2 were computed
+    assert (out[5:7] == 0).all() and (out[0:5] != 0).any()
+    assert (ck_d[1].view(torch.int16) == W.CACHE_SENTINEL_BITS).all()
+    with pytest.raises(binding.PrefillAttnError, match="cu_seqlens_k"):
+        binding.prefill_attn_varlen_validate(dev["q"], dev["k"], dev["v"], dev["cu_seqlens_q"], bad_k, ck_d,
+                                             cv_d, dev["cache_offsets"], out, None, scale=wl.scale)
