@@ -6,6 +6,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <algorithm>
 #include <map>
 #include <mutex>
 #include <string>
@@ -187,8 +188,7 @@ pa_status prefill_attn_varlen(const void* q, const void* k, const void* v, const
     e = pa::launch_build_schedule(sa, stream);
     if (e != cudaSuccess) return cuda_fail(e, "schedule launch");
 
-    pa::SimpleParams p;
-    p.q = static_cast<const __nv_bfloat16*>(q);
+    pa::FwdParams p;
     p.k = static_cast<const __nv_bfloat16*>(k);
     p.v = static_cast<const __nv_bfloat16*>(v);
     p.cache_k = static_cast<__nv_bfloat16*>(cache_k);
@@ -202,9 +202,15 @@ pa_status prefill_attn_varlen(const void* q, const void* k, const void* v, const
     p.n_kv_heads = n_kv_heads;
     p.group = group;
     p.max_cache_len = max_cache_len;
-    p.scale = scale;
+    p.scale_log2 = scale * 1.4426950408889634f;
     p.causal = causal;
-    e = pa::launch_attn_simple(p, head_dim, (int)max_units_ll, stream);
+    e = pa::encode_fwd_maps(p, q, total_q, num_seqs, head_dim);
+    if (e != cudaSuccess) return cuda_fail(e, "tensor map encoding");
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    const int grid = (int)std::min<long long>(sms, max_units_ll);
+    e = pa::launch_attn_fwd(p, head_dim, grid, stream);
     if (e != cudaSuccess) return cuda_fail(e, "attention launch");
     g_last_launches = 2;
     return PA_OK;

@@ -10,22 +10,38 @@ namespace pa {
 
 cudaError_t launch_build_schedule(const ScheduleArgs& a, cudaStream_t stream);
 
-struct SimpleParams {
-    const __nv_bfloat16* q;
-    const __nv_bfloat16* k;
+
+
+}  // namespace pa
+
+#include <cuda.h>
+
+namespace pa {
+
+// Parameters of the warp-specialised tcgen05 attention kernel.  The tensor
+// maps are encoded on the host per call.
+struct FwdParams {
+    CUtensorMap tm_q;        // q  [T, H, D]      viewed (D, H, T),        box (C, G, 128/G)
+    CUtensorMap tm_k;        // k  [T, Hk, D]     viewed (D, Hk, T),       box (C, 1, 128)
+    CUtensorMap tm_v;        // v  same as k
+    CUtensorMap tm_ck;       // cache_k [B, Hk, cap, D] viewed (D, cap, B*Hk), box (C, 128, 1)
+    CUtensorMap tm_cv;       // cache_v same
+    const __nv_bfloat16* k;  // raw pointers for the cache copy
     const __nv_bfloat16* v;
     __nv_bfloat16* cache_k;
     __nv_bfloat16* cache_v;
     __nv_bfloat16* out;
     float* lse;
-    const WorkspaceHeader* hdr;
+    WorkspaceHeader* hdr;
     const SeqInfo* seqs;
     const Unit* units;
     int n_heads, n_kv_heads, group, max_cache_len;
-    float scale;
+    float scale_log2;        // scale * log2(e)
     int causal;
 };
 
-cudaError_t launch_attn_simple(const SimpleParams& p, int head_dim, int grid, cudaStream_t st);
+// Encodes the tensor maps of `p` (the pointer fields and sizes must be set).
+cudaError_t encode_fwd_maps(FwdParams& p, const void* q, int total_q, int num_seqs, int head_dim);
+cudaError_t launch_attn_fwd(const FwdParams& p, int head_dim, int grid, cudaStream_t st);
 
 }  // namespace pa

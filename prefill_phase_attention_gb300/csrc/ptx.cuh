@@ -155,6 +155,15 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// Ties registers filled by tcgen05.ld to the preceding tcgen05.wait::ld: the
+// empty volatile asm "redefines" each register after the wait, so no use of it
+// can be scheduled above the wait.
+template <int N>
+__device__ __forceinline__ void reg_fence(uint32_t (&r)[N]) {
+#pragma unroll
+    for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
+}
+
 // 32 lanes x 32 bits, repeated 32 times along columns: thread t of the warp
 // receives columns [col, col+32) of lane (lane_base + t).
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
