@@ -1,0 +1,405 @@
+"""Benchmark: causal varlen prefill attention throughput on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step is one pass of the whole hot path over one batch of the workload: the
+device scheduler plus the attention/cache-write kernel, for every launch the
+workload has (long32k: one 32768-token prompt, one launch; chunked_decode: 16
+launches of a 512-token chunk packed with 64 decode rows).  Inputs are seeded
+synthetic N(0,1) bf16 tensors, resident in HBM before timing; q/k/v of the
+default workload (805 MB) exceed the 129 MB L2, so no flush is needed between
+steps.  The metric is causal-attention TFLOP/s (4 * head_dim * n_heads per
+visible (query, key) pair) -- the masked upper triangle is not counted.
+
+For N > 1 (torchrun, one process per GPU) every rank runs its own replica of
+the workload: the units of attention are independent, no collective is on
+the data path (weak scaling).  Timing is max over ranks.
+
+--impl reference times the fp64 CPU oracle on this host's cores on a bounded
+sample of the same workload (the baseline this library is compared with).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "causal varlen prefill attention TFLOP/s and tokens/s; % of GB300 BF16 peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# --------------------------------------------------------------------- utils --
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown", "clocks_event_reasons.sw_thermal_slowdown",
+              "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) != len(self.FIELDS):
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+                power.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[3:]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(x: float, ws: int, device=None) -> float:
+    """Max of a float over all ranks (identity when not distributed)."""
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_value(flops_per_step_per_rank: float, ms_total_max: float, steps: int, ws: int) -> float:
+    """Whole-job TFLOP/s: every rank processed its own copy of the step's units."""
+    return ws * flops_per_step_per_rank * steps / (ms_total_max * 1e-3) / 1e12
+
+
+def barrier(ws: int):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------ oracle timing --
+
+def oracle_sample_rows(wl, step, target_rows: int, seed: int):
+    """A bounded sample of query rows (t*H + h) spread uniformly over tokens and heads."""
+    rng = np.random.default_rng(seed)
+    T = step.total_q
+    n = min(target_rows, T * wl.n_heads)
+    return np.sort(rng.choice(T * wl.n_heads, size=n, replace=False)).astype(np.int64)
+
+
+def row_flops(wl, step, rows):
+    """Causal FLOPs of the selected rows (4 * d per visible key)."""
+    cu = np.array(step.cu_seqlens_q())
+    off = np.array(step.cache_offsets)
+    t = rows // wl.n_heads
+    b = np.searchsorted(cu, t, side="right") - 1
+    i = t - cu[b]
+    n_b = cu[b + 1] - cu[b]
+    vis = off[b] + (i + 1 if wl.causal else n_b)
+    return int(4 * wl.head_dim * vis.sum())
+
+
+def time_oracle(wl, inputs, rows, threads):
+    import oracle
+    from prefill_phase_attention_gb300 import workloads as W
+    cache_k, cache_v, steps = inputs
+    inp = steps[-1]
+    ck, cv = W.bf16_bits(cache_k), W.bf16_bits(cache_v)
+    t0 = time.perf_counter()
+    oracle.prefill_attention(W.bf16_bits(inp["q"]), W.bf16_bits(inp["k"]), W.bf16_bits(inp["v"]),
+                             inp["cu_seqlens_q"].numpy(), inp["cu_seqlens_k"].numpy(),
+                             inp["cache_offsets"].numpy(), ck, cv, n_heads=wl.n_heads,
+                             n_kv_heads=wl.n_kv_heads, head_dim=wl.head_dim, max_cache_len=wl.max_cache_len,
+                             scale=wl.scale, causal=wl.causal, rows=rows, want_cache=False, threads=threads)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(wl, inputs, budget_s: float = 15.0):
+    """The oracle on this host's cores over a sample sized to about `budget_s` seconds."""
+    import oracle
+    oracle.build()
+    cores = host_cores()
+    step = wl.steps[-1]
+    time_oracle(wl, inputs, oracle_sample_rows(wl, step, 64, seed=10), cores)  # threads, page faults
+    cal = oracle_sample_rows(wl, step, 512, seed=11)
+    dt = time_oracle(wl, inputs, cal, cores)
+    rate = row_flops(wl, step, cal) / max(dt, 1e-6)  # FLOP/s of the oracle on this host
+    per_row = row_flops(wl, step, cal) / cal.size
+    n = int(rate * budget_s / max(per_row, 1.0))
+    rows = oracle_sample_rows(wl, step, max(512, n), seed=12)
+    dt = time_oracle(wl, inputs, rows, cores)
+    fl = row_flops(wl, step, rows)
+    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"{rows.size} query rows (token, head) drawn uniformly from {wl.name} "
+                      f"(launch {len(wl.steps) - 1}), {fl / 1e9:.1f} GFLOP causal, {dt:.1f} s, fp64 C + OpenMP",
+            "seconds": round(dt, 2)}
+
+
+# ----------------------------------------------------------------- our arm --
+
+def run_ours(args, ws, rank, local):
+    import torch
+    from prefill_phase_attention_gb300 import binding, build
+    from prefill_phase_attention_gb300 import workloads as W
+
+    torch.cuda.set_device(local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    build.build()
+    binding.load()
+    wl = W.get(args.workload)
+    inputs = W.make_inputs(wl, sentinel=False)
+    cache_k, cache_v, steps = inputs
+    ck, cv = cache_k.cuda(), cache_v.cuda()
+    dev = [{k: v.cuda() for k, v in s.items()} for s in steps]
+    outs = [torch.empty_like(d["q"]) for d in dev]
+    lses = [torch.empty(d["q"].shape[0], wl.n_heads, device="cuda", dtype=torch.float32) for d in dev]
+    stream = torch.cuda.current_stream()
+
+    def call(d, o, l):
+        binding.prefill_attn_varlen(d["q"], d["k"], d["v"], d["cu_seqlens_q"], d["cu_seqlens_k"], ck, cv,
+                                    d["cache_offsets"], o, l, scale=wl.scale, causal=wl.causal)
+
+    def step():
+        for d, o, l in zip(dev, outs, lses):
+            call(d, o, l)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if binding.prefill_attn_device_status() != 0:
+        raise RuntimeError("device error word set during warm-up")
+
+    # timed region: K steps, per-launch events for the roofline
+    n_launch = len(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps * n_launch)]
+    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
+    sampler.start()
+    time.sleep(0.3)
+    launches = 0
+    barrier(ws)
+    torch.cuda.synchronize()
+    e_start.record(stream)
+    k = 0
+    for _ in range(args.steps):
+        for d, o, l in zip(dev, outs, lses):
+            ev[k][0].record(stream)
+            call(d, o, l)
+            ev[k][1].record(stream)
+            launches += binding.prefill_attn_last_launch_count()
+            k += 1
+    e_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    clocks = sampler.stop()
+    ms_total = e_start.elapsed_time(e_end)
+    ms_total = max_over_ranks(ms_total, ws, device=torch.device("cuda", local))
+    if binding.prefill_attn_device_status() != 0:
+        raise RuntimeError("device error word set during the timed region")
+    per_call_ms = [a.elapsed_time(b) for a, b in ev]
+    ms_step = ms_total / args.steps
+    flops_step = wl.flops()
+    value = weak_scaling_value(flops_step, ms_total, args.steps, ws)
+    tokens_s = ws * wl.tokens() / (ms_step * 1e-3)
+
+    peaks, peak_src = load_peaks()
+    peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    # roofline of the dominant kernel: algorithmic causal FLOPs per call / mean call time
+    per_launch = []
+    for li, s in enumerate(wl.steps):
+        fl = 4 * wl.head_dim * wl.n_heads * s.visible_pairs(wl.causal)
+        times = per_call_ms[li::n_launch]
+        per_launch.append((fl, statistics.mean(times)))
+    fl_tot = sum(f for f, _ in per_launch)
+    t_tot = sum(t for _, t in per_launch)
+    achieved = fl_tot / (t_tot * 1e-3) / 1e12
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", f"traffic_{wl.name}.json")
+    if os.path.exists(tpath):
+        traffic = json.load(open(tpath)).get("bytes_per_launch")
+
+    # end to end through the public API: pinned host inputs -> device -> call -> host result
+    h_in = [{kk: vv.pin_memory() for kk, vv in s.items()} for s in steps]
+    h_out = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
+    h_lse = [torch.empty(l.shape, dtype=l.dtype).pin_memory() for l in lses]
+    d_in = [{kk: torch.empty_like(vv, device="cuda") for kk, vv in s.items()} for s in steps]
+    h2d = sum(v.numel() * v.element_size() for s in steps for v in s.values())
+    d2h = sum(o.numel() * o.element_size() for o in outs) + sum(l.numel() * l.element_size() for l in lses)
+
+    def e2e_step():
+        for hi, di, o, l, ho, hl in zip(h_in, d_in, outs, lses, h_out, h_lse):
+            for kk in hi:
+                di[kk].copy_(hi[kk], non_blocking=True)
+            call(di, o, l)
+            ho.copy_(o, non_blocking=True)
+            hl.copy_(l, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 20))
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(ws)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks(time.perf_counter() - t0, ws, device=torch.device("cuda", local))
+    e2e_val = ws * flops_step * e2e_steps / e2e_s / 1e12
+
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "tokens_per_s": round(tokens_s, 1),
+        "pct_of_bf16_peak": round(100 * value / ws / peak, 2),
+        "config": {"workload": wl.name, "launches_per_step": n_launch, "num_seqs": wl.num_seqs,
+                   "tokens_per_step": wl.tokens(), "n_heads": wl.n_heads, "n_kv_heads": wl.n_kv_heads,
+                   "head_dim": wl.head_dim, "causal": wl.causal, "causal_flops_per_step": flops_step,
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+                   "l2": "inputs larger than L2 (no flush)" if wl.tokens() * (wl.n_heads + 2 * wl.n_kv_heads)
+                         * wl.head_dim * 2 > 129e6 else "inputs smaller than L2 (hot L2)"},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside back-to-back steps)",
+                     "timed": "per prefill_attn_varlen call (scheduler + attention kernel), CUDA events on "
+                              "the launching stream"},
+        "e2e": {"value": round(e2e_val, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h), "steps": e2e_steps,
+                "note": "pinned host q/k/v/metadata -> device, call, out+lse -> pinned host; KV cache stays "
+                        "device-resident"},
+        "gpu_launches": launches,
+        "clocks": clocks,
+    }
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(wl, inputs, budget_s=args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ----------------------------------------------------------- reference arm --
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return
+    from prefill_phase_attention_gb300 import workloads as W
+    import oracle
+    oracle.build()
+    wl = W.get(args.workload)
+    inputs = W.make_inputs(wl, sentinel=False)
+    step = wl.steps[-1]
+    cores = host_cores()
+    rows = oracle_sample_rows(wl, step, args.ref_rows, seed=13)
+    fl = row_flops(wl, step, rows)
+    for _ in range(args.warmup):
+        time_oracle(wl, inputs, rows, cores)
+    total = 0.0
+    for _ in range(args.steps):
+        total += time_oracle(wl, inputs, rows, cores)
+    value = fl * args.steps / total / 1e12
+    sample = (f"{rows.size} query rows (token, head) drawn uniformly from {wl.name} per step, "
+              f"{fl / 1e9:.2f} GFLOP causal per step")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "parallelism": "host cores"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="long32k")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--ref-rows", type=int, default=128, help="oracle rows per reference step")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps, reported as run
+    ws, rank, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+    else:
+        run_ours(args, ws, rank, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -18,7 +18,7 @@ struct SeqInfo {
     int q_start;  // first row of the sequence in the flattened q/k/v/out stream
     int n;        // new tokens (0 when the sequence is empty or its metadata was rejected)
     int P;        // cached prefix length = cache position of the first new token
-    int pad;
+    int pad;      // scheduler scratch: index of the sequence's first query block
 };
 
 // One work unit: query block [q0, q0 + 128/G) of sequence b against KV head kvh,

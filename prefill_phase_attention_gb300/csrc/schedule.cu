@@ -19,50 +19,16 @@ namespace pa {
 
 __device__ __forceinline__ int clamp_bin(int c) { return c < kCostBins - 1 ? c : kCostBins - 1; }
 
-__global__ void __launch_bounds__(1024) build_schedule_kernel(ScheduleArgs a) {
-    __shared__ int hist[kCostBins];
-    __shared__ int warp_sums[32];
-    const int tid = threadIdx.x;
-    const int nthr = blockDim.x;
-    const int tpu = kBlockM / a.group;  // query tokens per unit
-
-    for (int i = tid; i < kCostBins; i += nthr) hist[i] = 0;
-    __syncthreads();
-
-    // Pass 1: sanitise each sequence and histogram the unit costs.
-    for (int b = tid; b < a.num_seqs; b += nthr) {
-        const int q_start = a.cu_seqlens_q[b];
-        const int q_end = a.cu_seqlens_q[b + 1];
-        const int lk = a.cu_seqlens_k[b + 1] - a.cu_seqlens_k[b];
-        const int P = a.cache_offsets[b];
-        const long long n = (long long)q_end - q_start;
-        const bool ok = q_start >= 0 && n >= 0 && (long long)q_end <= a.total_q && P >= 0 &&
-                        (long long)lk == (long long)P + n && (long long)P + n <= a.max_cache_len &&
-                        (b > 0 || q_start == 0);
-        SeqInfo si;
-        si.q_start = ok ? q_start : 0;
-        si.n = ok ? (int)n : 0;
-        si.P = ok ? P : 0;
-        si.pad = 0;
-        if (!ok) atomicOr(&a.hdr->error, PA_DEVERR_METADATA);
-        a.seqs[b] = si;
-        for (int q0 = 0; q0 < si.n; q0 += tpu)
-            atomicAdd(&hist[clamp_bin(unit_tiles(si.n, si.P, q0, tpu, a.causal))], a.n_kv_heads);
-    }
-    __syncthreads();
-
-    // Exclusive scan in DESCENDING cost order: start[c] = sum of hist[c'] for c' > c.
-    // Each thread owns two adjacent bins of the reversed order.
-    static_assert(kCostBins == 2 * 1024, "scan assumes two bins per thread");
-    const int r0 = kCostBins - 1 - 2 * tid;  // bins r0 and r0 - 1, in that order
-    const int h0 = hist[r0], h1 = hist[r0 - 1];
-    int x = h0 + h1;
-    const int lane = tid & 31, warp = tid >> 5;
+// Block-wide exclusive scan of one int per thread (1024 threads); returns the
+// exclusive prefix and writes the block total to *total.
+__device__ __forceinline__ int block_exclusive_scan(int x, int* warp_sums, int* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int inc = x;
     for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
+        const int y = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += y;
     }
-    if (lane == 31) warp_sums[warp] = x;
+    if (lane == 31) warp_sums[warp] = inc;
     __syncthreads();
     if (warp == 0) {
         int w = warp_sums[lane];
@@ -70,12 +36,85 @@ __global__ void __launch_bounds__(1024) build_schedule_kernel(ScheduleArgs a) {
             const int y = __shfl_up_sync(0xffffffffu, w, o);
             if (lane >= o) w += y;
         }
-        warp_sums[lane] = w;  // inclusive
+        warp_sums[lane] = w;  // inclusive over warps
     }
     __syncthreads();
-    const int excl = x - (h0 + h1) + (warp > 0 ? warp_sums[warp - 1] : 0);
-    const int total = warp_sums[31];
+    const int excl = inc - x + (warp > 0 ? warp_sums[warp - 1] : 0);
+    *total = warp_sums[31];
     __syncthreads();
+    return excl;
+}
+
+// Sequence owning flattened query block i: the last b with seqs[b].pad <= i
+// among sequences that have blocks (pad holds the first block index of b).
+__device__ __forceinline__ int block_owner(const SeqInfo* seqs, int num_seqs, int i) {
+    int lo = 0, hi = num_seqs - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (seqs[mid].pad <= i)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    return lo;
+}
+
+__global__ void __launch_bounds__(1024) build_schedule_kernel(ScheduleArgs a) {
+    __shared__ int hist[kCostBins];
+    __shared__ int warp_sums[32];
+    __shared__ int s_total;
+    const int tid = threadIdx.x;
+    const int nthr = blockDim.x;
+    const int tpu = kBlockM / a.group;  // query tokens per unit
+
+    for (int i = tid; i < kCostBins; i += nthr) hist[i] = 0;
+
+    // Pass 1: sanitise each sequence; number its query blocks (first block
+    // index of b goes to SeqInfo::pad) with a block-wide scan per 1024 sequences.
+    int blocks_before = 0;
+    for (int b0 = 0; b0 < a.num_seqs; b0 += nthr) {
+        const int b = b0 + tid;
+        SeqInfo si{0, 0, 0, 0};
+        if (b < a.num_seqs) {
+            const int q_start = a.cu_seqlens_q[b];
+            const int q_end = a.cu_seqlens_q[b + 1];
+            const int lk = a.cu_seqlens_k[b + 1] - a.cu_seqlens_k[b];
+            const int P = a.cache_offsets[b];
+            const long long n = (long long)q_end - q_start;
+            const bool ok = q_start >= 0 && n >= 0 && (long long)q_end <= a.total_q && P >= 0 &&
+                            (long long)lk == (long long)P + n && (long long)P + n <= a.max_cache_len &&
+                            (b > 0 || q_start == 0);
+            if (!ok) atomicOr(&a.hdr->error, PA_DEVERR_METADATA);
+            si.q_start = ok ? q_start : 0;
+            si.n = ok ? (int)n : 0;
+            si.P = ok ? P : 0;
+        }
+        const int nblk = (si.n + tpu - 1) / tpu;
+        int chunk_total;
+        const int excl = block_exclusive_scan(nblk, warp_sums, &chunk_total);
+        si.pad = blocks_before + excl;
+        if (b < a.num_seqs) a.seqs[b] = si;
+        blocks_before += chunk_total;
+    }
+    const int total_blocks = blocks_before;
+    __threadfence_block();
+    __syncthreads();
+
+    // Pass 2: histogram of unit costs (each query block gives n_kv_heads units).
+    for (int i = tid; i < total_blocks; i += nthr) {
+        const int b = block_owner(a.seqs, a.num_seqs, i);
+        const SeqInfo si = a.seqs[b];
+        const int q0 = (i - si.pad) * tpu;
+        atomicAdd(&hist[clamp_bin(unit_tiles(si.n, si.P, q0, tpu, a.causal))], a.n_kv_heads);
+    }
+    __syncthreads();
+
+    // Exclusive scan in DESCENDING cost order: start[c] = sum of hist[c'] for c' > c.
+    static_assert(kCostBins == 2 * 1024, "scan assumes two bins per thread");
+    const int r0 = kCostBins - 1 - 2 * tid;  // this thread's bins: r0, then r0 - 1
+    const int h0 = hist[r0], h1 = hist[r0 - 1];
+    int total;
+    const int excl = block_exclusive_scan(h0 + h1, warp_sums, &total);
     hist[r0] = excl;
     hist[r0 - 1] = excl + h0;
     if (tid == 0) {
@@ -86,22 +125,23 @@ __global__ void __launch_bounds__(1024) build_schedule_kernel(ScheduleArgs a) {
     }
     __syncthreads();
 
-    // Pass 2: scatter the units to their sorted positions.
-    for (int b = tid; b < a.num_seqs; b += nthr) {
+    // Pass 3: scatter the units to their sorted positions (the KV heads of one
+    // query block stay adjacent).
+    for (int i = tid; i < total_blocks; i += nthr) {
+        const int b = block_owner(a.seqs, a.num_seqs, i);
         const SeqInfo si = a.seqs[b];
-        for (int q0 = 0; q0 < si.n; q0 += tpu) {
-            const int cost = unit_tiles(si.n, si.P, q0, tpu, a.causal);
-            const int base = atomicAdd(&hist[clamp_bin(cost)], a.n_kv_heads);
-            for (int kvh = 0; kvh < a.n_kv_heads; ++kvh) {
-                const int pos = base + kvh;
-                if (pos < a.max_units) {
-                    Unit u;
-                    u.b = b;
-                    u.kvh = kvh;
-                    u.q0 = q0;
-                    u.ntiles = cost;
-                    a.units[pos] = u;
-                }
+        const int q0 = (i - si.pad) * tpu;
+        const int cost = unit_tiles(si.n, si.P, q0, tpu, a.causal);
+        const int base = atomicAdd(&hist[clamp_bin(cost)], a.n_kv_heads);
+        for (int kvh = 0; kvh < a.n_kv_heads; ++kvh) {
+            const int pos = base + kvh;
+            if (pos < a.max_units) {
+                Unit u;
+                u.b = b;
+                u.kvh = kvh;
+                u.q0 = q0;
+                u.ntiles = cost;
+                a.units[pos] = u;
             }
         }
     }

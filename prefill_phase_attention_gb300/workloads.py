@@ -9,8 +9,10 @@ Shapes follow the flattened varlen layout of "大模型 Prompt Prefill 阶段的
 Batching 与算子排布" (nxmr.cn, §2: prompts packed head-to-tail into one
 [Total_Tokens, ...] stream indexed by cu_seqlens, e.g. lengths 5, 2, 3 give
 cu_seqlens [0, 5, 7, 10]) and the per-sequence cache layout
-(num_heads, seq_len, head_dim) of "Prefill 阶段" worked example (yfxerp.com,
-§2.1).  The five named workloads are the ones this library is measured on:
+(num_heads, seq_len, head_dim) of the worked example in "大语言模型推理核心：
+Prefill与Decode原理及工程优化" (yfxerp.com, §2.1).  The first five named
+workloads are the ones this library is measured on; long8k is the long32k
+shape at a quarter of the length, used for profiling:
 
 =================  ===========================================================
 tiny_packed        lengths [5, 2, 3], 4/4 heads, head_dim 32, empty cache
@@ -20,6 +22,7 @@ chunked_decode     8192-token prompt as 16 chunks of 512, each step packed with
                    64 one-token decode rows over cached contexts ~ U{256..4096};
                    GQA 32/8 heads, head_dim 128 (16 launches)
 long32k            one 32768-token prompt, 32/32 heads, head_dim 128
+long8k             one 8192-token prompt, 32/32 heads, head_dim 128
 =================  ===========================================================
 """
 from __future__ import annotations
@@ -126,12 +129,19 @@ def _long32k() -> Workload:
     return Workload("long32k", 32, 32, 128, 32768, [Step([32768], [0])], [0], seed=5)
 
 
+def _long8k() -> Workload:
+    # the long32k shape family at a quarter of the length (profiling case: q/k/v
+    # still exceed L2, device footprint under 1 GB)
+    return Workload("long8k", 32, 32, 128, 8192, [Step([8192], [0])], [0], seed=6)
+
+
 WORKLOADS = {
     "tiny_packed": _tiny_packed,
     "layer512": _layer512,
     "varlen16": _varlen16,
     "chunked_decode": _chunked_decode,
     "long32k": _long32k,
+    "long8k": _long8k,
 }
 
 
