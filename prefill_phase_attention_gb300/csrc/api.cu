@@ -164,7 +164,7 @@ pa_status prefill_attn_varlen(const void* q, const void* k, const void* v, const
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
 
     const int group = n_heads / n_kv_heads;
-    const int tpu = pa::kBlockM / group;
+    const int tpu = pa::kSlots * (pa::kBlockM / group);  // query tokens per work unit
     const long long max_units_ll = (long long)n_kv_heads * ((total_q + tpu - 1) / tpu + num_seqs);
     if (max_units_ll >= (1LL << 31)) return fail(PA_ERR_UNSUPPORTED, "too many work units");
     Workspace* ws = nullptr;

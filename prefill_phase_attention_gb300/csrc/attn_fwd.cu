@@ -1,9 +1,11 @@
 // attn_fwd.cu -- warp-specialised causal varlen prefill attention for sm_103a.
 //
-// Computes out = softmax(Q K^T * scale) V per work unit (128 query rows of one
-// sequence sharing one KV head; GQA heads packed into the rows) over the
-// unit's KV tiles -- the cached prefix read from the KV cache, then the
-// sequence's own new keys -- and writes the new K/V into the cache.
+// Computes out = softmax(Q K^T * scale) V per work unit -- two 128-row Q tiles
+// ("slots") of one sequence and one KV head, GQA query heads packed into the
+// rows -- over the unit's KV tiles (the cached prefix read from the KV cache,
+// then the sequence's own new keys), and writes the new K/V into the cache.
+// Both slots consume every K/V tile, so each tile loaded from L2 feeds 256
+// query rows.
 //
 // The method (pages, by title and section):
 //  - scaled dot-product attention, each row normalised over all visible keys:
@@ -18,22 +20,22 @@
 //    same page §3; prefill as the writer of every new token's K/V
 //    (mhpn.cn §1, §4; yfxerp.com §2.1).
 //
-// GB300 mapping (one persistent CTA per SM, 384 threads, all 512 TMEM columns):
-//   warp 0      TMA producer: fetches units from the longest-first list,
-//               loads Q once per unit and K tiles into a kStages ring;
-//   warp 2      TMA producer of the V tiles (a ring of its own, so K runs
-//               ahead of S while V waits for the PV products);
-//   warp 1      tcgen05 issuer: S = Q K^T (SS form, bf16 -> fp32 in TMEM,
-//               double-buffered, issued two tiles ahead of PV) and O += P V
-//               (P read from TMEM, V MN-major);
-//   warps 3,12  cache writers (K, V): copy the unit's own new K/V rows out of
-//               the staged tiles in shared memory into the cache (16-byte
-//               stores); second releaser of every ring stage;
-//   warps 4-11  softmax: two warps per TMEM sub-partition, each thread one
-//               query row (TMEM lane) and one half of the key columns; online
-//               max/sum in fp32 registers (partial maxima swapped through
-//               shared memory), exp2 on the MUFU, P packed to bf16 into TMEM,
-//               lazy O rescale, epilogue out = O / l (bf16) and LSE.
+// GB300 mapping (one persistent CTA per SM, 384 threads, all 512 TMEM columns:
+// slot s owns S_s at [256 s, 256 s + 128) and O_s at [256 s + 128, 256 s + 256);
+// P_s is written as bf16 over the first 64 columns of S_s):
+//   warp 0, lane 0  fetches units from the longest-first list, loads both Q
+//                   tiles once per unit and the K tiles into a ring;
+//   warp 0, lane 1  loads the V tiles into a ring of its own;
+//   warp 1          tcgen05 issuer, ping-pong over the slots:
+//                   PV_0(t), S_0(t+1), PV_1(t), S_1(t+1), ... (S in the SS
+//                   form, PV with P read from TMEM and V MN-major in SMEM);
+//   warps 2, 3      cache writers (V, K): copy the unit's own new rows out of
+//                   the staged tiles in shared memory into the cache; second
+//                   releaser of every ring stage;
+//   warps 4-7, 8-11 softmax of slot 0 and slot 1: one query row per thread
+//                   (its TMEM lane), fp32 running max/sum in registers, exp2
+//                   on the MUFU, lazy O rescale, epilogue out = O / l (bf16)
+//                   and LSE.
 // Every wait is bounded in time; on timeout the CTA records PA_DEVERR_TIMEOUT,
 // drains its in-flight copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
@@ -54,8 +56,9 @@ using namespace ptx;
 namespace {
 
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per wait
-constexpr int kThreads = 416;  // 5 control warps + 8 softmax warps
-constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256, kColP0 = 384, kColP1 = 448;
+constexpr int kThreads = 384;                   // 4 control warps + 8 softmax warps
+constexpr uint32_t kColSlot = 256;              // TMEM columns per slot: S then O
+constexpr uint32_t kColO = 128;                 // O offset within a slot
 
 template <int D>
 struct Cfg {
@@ -66,7 +69,8 @@ struct Cfg {
     static constexpr int kTileBytes = kChunks * kChunkBytes;  // 128 rows x D bf16
     static constexpr SmemSwizzle kSw = D >= 64 ? kSwizzle128B : kSwizzle64B;
     static constexpr int kSbo = 8 * kRowBytes;  // byte distance between 8-row groups
-    static constexpr int kStages = D == 128 ? 3 : 4;
+    static constexpr int kStagesK = D == 128 ? 3 : 4;
+    static constexpr int kStagesV = D == 128 ? 2 : 4;
     static constexpr uint32_t kIdescS = idesc_bf16_f32(kBlockM, kBlockN, 0, 0);
     static constexpr uint32_t kIdescO = idesc_bf16_f32(kBlockM, D, 0, 1);
 };
@@ -79,14 +83,12 @@ struct UnitSlot {
 struct __align__(8) Ctrl {
     uint64_t q_full, q_empty;
     uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
-    uint64_t s_full[2], s_empty[2], p_full[2], pv_done[2];
-    uint64_t o_empty, mma_drain;
+    uint64_t s_full[kSlots], p_full[kSlots], pv_done[kSlots], o_empty[kSlots];
+    uint64_t mma_drain;
     uint64_t unit_full[2], unit_empty[2];
-    uint64_t xchg[4];          // per sub-partition: the two softmax warps of the same rows
     UnitSlot slot[2];
     uint32_t tmem_base;
     int abort;
-    float xbuf[2][2][kBlockM];  // [exchange parity][column half][row]
 };
 
 // Tiles first (the dynamic shared window starts 1024-byte aligned, which the
@@ -94,8 +96,8 @@ struct __align__(8) Ctrl {
 // CTA never lands on an SM (each CTA holds all 512 TMEM columns).
 template <int D>
 constexpr int smem_bytes() {
-    return (Cfg<D>::kTileBytes * (1 + 2 * Cfg<D>::kStages) + (int)sizeof(Ctrl)) > 120 * 1024
-               ? Cfg<D>::kTileBytes * (1 + 2 * Cfg<D>::kStages) + (int)sizeof(Ctrl)
+    return (Cfg<D>::kTileBytes * (kSlots + Cfg<D>::kStagesK + Cfg<D>::kStagesV) + (int)sizeof(Ctrl)) > 120 * 1024
+               ? Cfg<D>::kTileBytes * (kSlots + Cfg<D>::kStagesK + Cfg<D>::kStagesV) + (int)sizeof(Ctrl)
                : 120 * 1024;
 }
 
@@ -148,6 +150,12 @@ __device__ __forceinline__ int tile_key_base(int j, int P, int np) {
     return j < np ? P - kBlockN * (np - j) : P + kBlockN * (j - np);
 }
 
+// KV tiles that slot `sl` of a unit visits (0 when the slot has no tokens).
+__device__ __forceinline__ int slot_tiles(const Unit& u, const SeqInfo& s, int sl, int tps, int causal) {
+    const int qs = u.q0 + sl * tps;
+    return qs < s.n ? unit_tiles(s.n, s.P, qs, tps, causal) : 0;
+}
+
 // Rows of new-key tile j (j >= np) that hold this unit's own tokens
 // [q0, q_end): tile rows [lo_row, lo_row + nrows).  The unit writes exactly
 // these tokens' K/V into the cache.
@@ -168,7 +176,7 @@ template <int D>
 __device__ __forceinline__ void copy_tile_rows(const uint8_t* tile, __nv_bfloat16* dst, int lo_row, int nrows,
                                                int lane) {
     using C = Cfg<D>;
-    constexpr int kGran = D / 8;               // 16-byte granules per row
+    constexpr int kGran = D / 8;  // 16-byte granules per row
     constexpr int kChunkGran = C::kChunkCols / 8;
     const int total = nrows * kGran;
 #pragma unroll 4
@@ -189,36 +197,38 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         if (threadIdx.x == 0) atomicOr(&p.hdr->error, PA_DEVERR_TIMEOUT);
         return;
     }
-    uint8_t* q_smem = smem_raw;
-    uint8_t* k_smem = q_smem + C::kTileBytes;
-    uint8_t* v_smem = k_smem + C::kStages * C::kTileBytes;
-    Ctrl* ctl = reinterpret_cast<Ctrl*>(v_smem + C::kStages * C::kTileBytes);
+    uint8_t* q_smem = smem_raw;                              // [kSlots] tiles
+    uint8_t* k_smem = q_smem + kSlots * C::kTileBytes;       // [kStagesK] tiles
+    uint8_t* v_smem = k_smem + C::kStagesK * C::kTileBytes;  // [kStagesV] tiles
+    Ctrl* ctl = reinterpret_cast<Ctrl*>(v_smem + C::kStagesV * C::kTileBytes);
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
     WorkspaceHeader* hdr = p.hdr;
     const int G = p.group;
-    const int tpu = kBlockM / G;
+    const int tps = kBlockM / G;  // query tokens per slot
 
     if (threadIdx.x == 0) {
         mbar_init(&ctl->q_full, 1);
         mbar_init(&ctl->q_empty, 1);
-        for (int s = 0; s < C::kStages; ++s) {
+        for (int s = 0; s < C::kStagesK; ++s) {
             mbar_init(&ctl->k_full[s], 1);
             mbar_init(&ctl->k_empty[s], 2);  // MMA commit + cache writer
+        }
+        for (int s = 0; s < C::kStagesV; ++s) {
             mbar_init(&ctl->v_full[s], 1);
             mbar_init(&ctl->v_empty[s], 2);
         }
+        for (int i = 0; i < kSlots; ++i) {
+            mbar_init(&ctl->s_full[i], 1);
+            mbar_init(&ctl->p_full[i], 4);  // the slot's 4 softmax warps
+            mbar_init(&ctl->pv_done[i], 1);
+            mbar_init(&ctl->o_empty[i], 4);
+        }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(&ctl->s_full[b], 1);
-            mbar_init(&ctl->s_empty[b], 8);
-            mbar_init(&ctl->p_full[b], 8);
-            mbar_init(&ctl->pv_done[b], 1);
             mbar_init(&ctl->unit_full[b], 1);
             mbar_init(&ctl->unit_empty[b], 12);  // MMA + V loader + 2 cache writers + 8 softmax warps
         }
-        for (int i = 0; i < 4; ++i) mbar_init(&ctl->xchg[i], 2);
-        mbar_init(&ctl->o_empty, 8);
         mbar_init(&ctl->mma_drain, 1);
         ctl->abort = 0;
         fence_mbar_init();
@@ -239,11 +249,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 
     // One KV ring (K or V): waits for the stage, then TMA-loads tile j of the
     // unit from the cache (prefix tiles) or from the new tokens' k/v.
-    auto load_kv_tile = [&](uint8_t* ring, uint64_t* full, uint64_t* empty, const CUtensorMap* tm_cache,
+    auto load_kv_tile = [&](uint8_t* ring, int stages, uint64_t* full, uint64_t* empty, const CUtensorMap* tm_cache,
                             const CUtensorMap* tm_new, int* last_parity, uint32_t t, int j, const Unit& u,
                             const SeqInfo& s, int np) -> bool {
-        const int st = t % C::kStages;
-        const uint32_t ph = (t / C::kStages) & 1;
+        const int st = t % stages;
+        const uint32_t ph = (t / stages) & 1;
         if (!wait_bar(&empty[st], ph ^ 1, ctl, hdr)) return false;
         const int kb = tile_key_base(j, s.P, np);
         mbar_arrive_expect_tx(&full[st], C::kTileBytes);
@@ -268,8 +278,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     };
 
     if (warp == 0) {
-        // --------------------------------------------- unit fetch, Q and K loads
         if (lane == 0) {
+            // ----------------------------------------- unit fetch, Q and K loads
             const int num_units = hdr->num_units;
             uint32_t t = 0;
             int last_q_parity[1] = {-1};
@@ -290,29 +300,29 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 if (us.u.b < 0) break;
                 const Unit u = us.u;
                 const SeqInfo s = us.s;
-                // Q tile: rows (token, head-in-group) of this unit
+                // both Q tiles: rows (token, head-in-group) of each slot
                 if (!wait_bar(&ctl->q_empty, (u_it & 1) ^ 1, ctl, hdr)) break;
-                mbar_arrive_expect_tx(&ctl->q_full, G * tpu * C::kRowBytes * C::kChunks);
-                for (int c = 0; c < C::kChunks; ++c)
-                    tma_load_3d(q_smem + c * C::kChunkBytes, &p.tm_q, &ctl->q_full, c * C::kChunkCols, u.kvh * G,
-                                s.q_start + u.q0);
+                const int nq = u.q0 + tps < s.n ? 2 : 1;
+                mbar_arrive_expect_tx(&ctl->q_full, nq * G * tps * C::kRowBytes * C::kChunks);
+                for (int i = 0; i < nq; ++i)
+                    for (int c = 0; c < C::kChunks; ++c)
+                        tma_load_3d(q_smem + i * C::kTileBytes + c * C::kChunkBytes, &p.tm_q, &ctl->q_full,
+                                    c * C::kChunkCols, u.kvh * G, s.q_start + u.q0 + i * tps);
                 last_q_parity[0] = u_it & 1;
                 const int np = (s.P + kBlockN - 1) / kBlockN;
                 bool ok = true;
                 for (int j = 0; j < u.ntiles && ok; ++j, ++t)
-                    ok = load_kv_tile(k_smem, ctl->k_full, ctl->k_empty, &p.tm_ck, &p.tm_k, last_k_parity, t, j, u,
-                                      s, np);
+                    ok = load_kv_tile(k_smem, C::kStagesK, ctl->k_full, ctl->k_empty, &p.tm_ck, &p.tm_k,
+                                      last_k_parity, t, j, u, s, np);
                 if (!ok) break;
             }
             if (aborted(ctl)) {
                 drain(&ctl->q_full, last_q_parity, 1);
-                drain(ctl->k_full, last_k_parity, C::kStages);
+                drain(ctl->k_full, last_k_parity, C::kStagesK);
             }
-        }
-    } else if (warp == 2) {
-        // ------------------------------------------------------------- V loads
-        // A ring of its own, so K tiles run ahead of S while V tiles wait for PV.
-        if (lane == 0) {
+        } else if (lane == 1) {
+            // ------------------------------------------------------- V loads
+            // A ring of its own, so K tiles run ahead of S while V tiles wait for PV.
             uint32_t t = 0;
             int last_v_parity[4] = {-1, -1, -1, -1};
             for (int u_it = 0;; ++u_it) {
@@ -324,11 +334,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 const int np = (us.s.P + kBlockN - 1) / kBlockN;
                 bool ok = true;
                 for (int j = 0; j < us.u.ntiles && ok; ++j, ++t)
-                    ok = load_kv_tile(v_smem, ctl->v_full, ctl->v_empty, &p.tm_cv, &p.tm_v, last_v_parity, t, j,
-                                      us.u, us.s, np);
+                    ok = load_kv_tile(v_smem, C::kStagesV, ctl->v_full, ctl->v_empty, &p.tm_cv, &p.tm_v,
+                                      last_v_parity, t, j, us.u, us.s, np);
                 if (!ok) break;
             }
-            if (aborted(ctl)) drain(ctl->v_full, last_v_parity, C::kStages);
+            if (aborted(ctl)) drain(ctl->v_full, last_v_parity, C::kStagesV);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------- MMA issuer
@@ -336,57 +346,92 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             const uint32_t q_addr = smem_u32(q_smem);
             const uint32_t k_addr = smem_u32(k_smem);
             const uint32_t v_addr = smem_u32(v_smem);
-            uint32_t t = 0;
+            uint32_t t = 0;                // KV tiles of this CTA so far
+            uint32_t ns[kSlots] = {0, 0};  // tiles processed per slot so far
+            uint32_t no[kSlots] = {0, 0};  // units with the slot active so far
             bool ok = true;
+            auto issue_s = [&](int i, uint32_t tt) {
+                const uint32_t kb = k_addr + (tt % C::kStagesK) * C::kTileBytes;
+                const uint32_t qa = q_addr + i * C::kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const int c = (kk * 16) / C::kChunkCols, w = (kk * 16) % C::kChunkCols;
+                    const uint64_t ad = smem_desc(qa + c * C::kChunkBytes + w * 2, 16, C::kSbo, C::kSw);
+                    const uint64_t bd = smem_desc(kb + c * C::kChunkBytes + w * 2, 16, C::kSbo, C::kSw);
+                    mma_ss(tmem + i * kColSlot, ad, bd, C::kIdescS, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(&ctl->s_full[i]);
+            };
+            auto issue_pv = [&](int i, uint32_t tt, bool first) {
+                const uint32_t vb = v_addr + (tt % C::kStagesV) * C::kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < kBlockN / 16; ++kk) {
+                    const uint64_t bd = smem_desc(vb + kk * 2 * C::kSbo, C::kChunkBytes, C::kSbo, C::kSw);
+                    mma_ts(tmem + i * kColSlot + kColO, tmem + i * kColSlot + kk * 8, bd, C::kIdescO,
+                           (!first || kk > 0) ? 1u : 0u);
+                }
+                mma_commit(&ctl->pv_done[i]);
+            };
             for (int u_it = 0; ok; ++u_it) {
                 const int sl = u_it & 1;
                 if (!wait_bar(&ctl->unit_full[sl], (u_it >> 1) & 1, ctl, hdr)) break;
                 const Unit u = ctl->slot[sl].u;
+                const SeqInfo s = ctl->slot[sl].s;
                 mbar_arrive(&ctl->unit_empty[sl]);
                 if (u.b < 0) break;
+                const int nt[kSlots] = {slot_tiles(u, s, 0, tps, p.causal), slot_tiles(u, s, 1, tps, p.causal)};
                 if (!wait_bar(&ctl->q_full, u_it & 1, ctl, hdr)) break;
-                auto issue_pv = [&](uint32_t tp, bool first) -> bool {
-                    const int stp = tp % C::kStages;
-                    const uint32_t bp = tp & 1;
-                    if (!wait_bar(&ctl->p_full[bp], (tp >> 1) & 1, ctl, hdr)) return false;
-                    if (!wait_bar(&ctl->v_full[stp], (tp / C::kStages) & 1, ctl, hdr)) return false;
-                    if (first && !wait_bar(&ctl->o_empty, (u_it & 1) ^ 1, ctl, hdr)) return false;
-                    tc_fence_after();
-                    const uint32_t vb = v_addr + stp * C::kTileBytes;
-                    const uint32_t pcol = bp ? kColP1 : kColP0;
-#pragma unroll
-                    for (int kk = 0; kk < kBlockN / 16; ++kk) {
-                        const uint64_t bd = smem_desc(vb + kk * 2 * C::kSbo, C::kChunkBytes, C::kSbo, C::kSw);
-                        mma_ts(tmem + kColO, tmem + pcol + kk * 8, bd, C::kIdescO, (!first || kk > 0) ? 1u : 0u);
+                // prologue: S of tile 0 for both slots
+                if (!wait_bar(&ctl->k_full[t % C::kStagesK], (t / C::kStagesK) & 1, ctl, hdr)) break;
+                tc_fence_after();
+                for (int i = 0; i < kSlots; ++i)
+                    if (nt[i] > 0) issue_s(i, t);
+                mma_commit(&ctl->k_empty[t % C::kStagesK]);
+                if (u.ntiles == 1) mma_commit(&ctl->q_empty);
+                for (int j = 0; j < u.ntiles && ok; ++j) {
+                    const uint32_t tj = t + j;
+                    bool v_ready = false, k_ready = false;
+                    for (int i = 0; i < kSlots; ++i) {
+                        if (j < nt[i]) {
+                            // PV_i(j): P_i(j) written and O_i free (first tile of the unit)
+                            if (!wait_bar(&ctl->p_full[i], (ns[i] + j) & 1, ctl, hdr)) { ok = false; break; }
+                            if (j == 0 && !wait_bar(&ctl->o_empty[i], (no[i] & 1) ^ 1, ctl, hdr)) { ok = false; break; }
+                            if (!v_ready) {
+                                if (!wait_bar(&ctl->v_full[tj % C::kStagesV], (tj / C::kStagesV) & 1, ctl, hdr)) {
+                                    ok = false;
+                                    break;
+                                }
+                                v_ready = true;
+                            }
+                            tc_fence_after();
+                            issue_pv(i, tj, j == 0);
+                        }
+                        if (j + 1 < nt[i]) {
+                            // S_i(j+1) overwrites P_i(j): issued after PV_i(j) on the in-order tensor pipe
+                            if (!k_ready) {
+                                const uint32_t tn = tj + 1;
+                                if (!wait_bar(&ctl->k_full[tn % C::kStagesK], (tn / C::kStagesK) & 1, ctl, hdr)) {
+                                    ok = false;
+                                    break;
+                                }
+                                k_ready = true;
+                                tc_fence_after();
+                            }
+                            issue_s(i, tj + 1);
+                        }
                     }
-                    mma_commit(&ctl->pv_done[bp]);
-                    mma_commit(&ctl->v_empty[stp]);
-                    return true;
-                };
-                for (int j = 0; j < u.ntiles; ++j, ++t) {
-                    const int st = t % C::kStages;
-                    const uint32_t b = t & 1;
-                    if (!wait_bar(&ctl->k_full[st], (t / C::kStages) & 1, ctl, hdr)) { ok = false; break; }
-                    if (!wait_bar(&ctl->s_empty[b], ((t >> 1) & 1) ^ 1, ctl, hdr)) { ok = false; break; }
-                    tc_fence_after();
-                    const uint32_t kb = k_addr + st * C::kTileBytes;
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const int c = (kk * 16) / C::kChunkCols, w = (kk * 16) % C::kChunkCols;
-                        const uint64_t ad = smem_desc(q_addr + c * C::kChunkBytes + w * 2, 16, C::kSbo, C::kSw);
-                        const uint64_t bd = smem_desc(kb + c * C::kChunkBytes + w * 2, 16, C::kSbo, C::kSw);
-                        mma_ss(tmem + (b ? kColS1 : kColS0), ad, bd, C::kIdescS, kk > 0 ? 1u : 0u);
+                    if (!ok) break;
+                    if (j + 1 < u.ntiles) {
+                        mma_commit(&ctl->k_empty[(tj + 1) % C::kStagesK]);
+                        if (j + 2 == u.ntiles) mma_commit(&ctl->q_empty);
                     }
-                    mma_commit(&ctl->s_full[b]);
-                    mma_commit(&ctl->k_empty[st]);
-                    if (j == u.ntiles - 1) mma_commit(&ctl->q_empty);
-                    // S runs two tiles ahead of PV: S(t+1) never waits behind
-                    // the softmax of tile t-1.
-                    if (j >= 2 && !issue_pv(t - 2, j == 2)) { ok = false; break; }
+                    mma_commit(&ctl->v_empty[tj % C::kStagesV]);
                 }
-                // the unit's last (up to two) PV products
-                if (ok && u.ntiles >= 2 && !issue_pv(t - 2, u.ntiles == 2)) ok = false;
-                if (ok && !issue_pv(t - 1, u.ntiles == 1)) ok = false;
+                for (int i = 0; i < kSlots; ++i) {
+                    ns[i] += nt[i];
+                    no[i] += nt[i] > 0 ? 1 : 0;
+                }
+                t += u.ntiles;
             }
             // every MMA this thread issued has finished before TMEM is released
             mma_commit(&ctl->mma_drain);
@@ -394,14 +439,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             while (!mbar_try_wait(&ctl->mma_drain, 0) && globaltimer_ns() - t0 < kTimeoutNs) {
             }
         }
-    } else if (warp == 3 || warp == 12) {
+    } else if (warp == 2 || warp == 3) {
         // -------------------------------------------------------- cache writers
-        // Warp 3 writes K, warp 12 writes V.  Each walks every tile of its ring
+        // Warp 3 writes K, warp 2 writes V.  Each walks every tile of its ring
         // in order and is the second releaser of every stage (with the MMA
         // commit), so it never waits on a barrier phase more than one ahead or
         // behind; on the tiles holding the unit's own tokens it first copies
         // those rows from shared memory into the cache.
         const bool is_k = warp == 3;
+        const int stages = is_k ? C::kStagesK : C::kStagesV;
         uint8_t* ring = is_k ? k_smem : v_smem;
         uint64_t* full = is_k ? ctl->k_full : ctl->v_full;
         uint64_t* empty = is_k ? ctl->k_empty : ctl->v_empty;
@@ -415,11 +461,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             if (lane == 0) mbar_arrive(&ctl->unit_empty[sl]);
             if (us.u.b < 0) break;
             const int np = (us.s.P + kBlockN - 1) / kBlockN;
-            const int q_end = min(us.u.q0 + tpu, us.s.n);
+            const int q_end = min(us.u.q0 + kSlots * tps, us.s.n);
             bool ok = true;
             for (int j = 0; j < us.u.ntiles; ++j, ++t) {
-                const int st = t % C::kStages;
-                if (!warp_wait(&full[st], (t / C::kStages) & 1, ctl, hdr)) { ok = false; break; }
+                const int st = t % stages;
+                if (!warp_wait(&full[st], (t / stages) & 1, ctl, hdr)) { ok = false; break; }
                 int lo_row, nrows;
                 if (own_rows(j, np, us.u.q0, q_end, lo_row, nrows)) {
                     const int first_tok = (j - np) * kBlockN + lo_row;  // token index within the sequence
@@ -434,29 +480,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         }
     } else {
         // ------------------------------------------------------------- softmax
-        // Warps 4-11.  Sub-partition sp = warp % 4 owns TMEM lanes (= query rows)
-        // [32 sp, 32 sp + 32); half hf takes S columns [64 hf, 64 hf + 64) and
-        // O columns [D/2 hf, D/2 hf + D/2).  The two warps of the same rows swap
-        // their partial row max (every tile) and row sum (epilogue) through
-        // shared memory.
-        constexpr int kHalfN = kBlockN / 2;
-        constexpr int kHalfD = D / 2;
+        // Warps 4-7 serve slot 0, warps 8-11 slot 1.  Sub-partition sp = warp % 4
+        // owns TMEM lanes (= query rows) [32 sp, 32 sp + 32).
+        const int slot = (warp - 4) >> 2;
         const int sp = warp & 3;
-        const int hf = (warp - 4) >> 2;
         const int r = sp * 32 + lane;  // query row of the tile == TMEM lane
         const uint32_t lane_off = (uint32_t)(sp * 32) << 16;
+        const uint32_t s_col = tmem + lane_off + slot * kColSlot;
+        const uint32_t o_col = s_col + kColO;
         const float sl2 = p.scale_log2;
-        uint32_t t = 0, xc = 0;
-        // swap one float with the partner warp; returns the partner's value
-        auto exchange = [&](float mine, float& theirs) -> bool {
-            ctl->xbuf[xc & 1][hf][r] = mine;
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&ctl->xchg[sp]);
-            if (!warp_wait(&ctl->xchg[sp], xc & 1, ctl, hdr)) return false;
-            theirs = ctl->xbuf[xc & 1][hf ^ 1][r];
-            ++xc;
-            return true;
-        };
+        uint32_t ns = 0;  // tiles this slot has processed
         for (int u_it = 0;; ++u_it) {
             const int sl = u_it & 1;
             if (!warp_wait(&ctl->unit_full[sl], (u_it >> 1) & 1, ctl, hdr)) break;
@@ -466,63 +499,66 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             if (us.u.b < 0) break;
             const Unit u = us.u;
             const SeqInfo s = us.s;
-            const int tok = u.q0 + r / G;
+            const int nt = slot_tiles(u, s, slot, tps, p.causal);
+            if (nt == 0) continue;
+            const int qs = u.q0 + slot * tps;
+            const int tok = qs + r / G;
             const int h = u.kvh * G + r % G;
-            const bool valid = r < tpu * G && tok < s.n;
+            const bool valid = r < tps * G && tok < s.n;
             const int Lk = s.P + s.n;
             const int row_hi = p.causal ? min(s.P + tok + 1, Lk) : Lk;  // keys [0, row_hi) visible
-            const int unit_hi = p.causal ? min(s.P + u.q0 + 1, Lk) : Lk;  // smallest row_hi of the unit
+            const int slot_hi = p.causal ? min(s.P + qs + 1, Lk) : Lk;  // smallest row_hi of the slot
             const int np = (s.P + kBlockN - 1) / kBlockN;
-            float m = -INFINITY, l = 0.f;  // l: this half's share of the row sum
+            float m = -INFINITY, l = 0.f;
             bool ok = true;
-            for (int j = 0; j < u.ntiles; ++j, ++t) {
-                const uint32_t b = t & 1;
-                if (!warp_wait(&ctl->s_full[b], (t >> 1) & 1, ctl, hdr)) { ok = false; break; }
+            for (int j = 0; j < nt; ++j) {
+                if (!warp_wait(&ctl->s_full[slot], (ns + j) & 1, ctl, hdr)) { ok = false; break; }
                 tc_fence_after();
-                float sv[kHalfN];
+                // S_slot(j) is complete, and with it every earlier MMA of this
+                // slot (the PV of tile j-1 included): O may be rescaled below.
+                float sv[kBlockN];
                 {
-                    uint32_t r0[32], r1[32];
-                    const uint32_t sa = tmem + lane_off + (b ? kColS1 : kColS0) + hf * kHalfN;
-                    tmem_ld32(sa, r0);
-                    tmem_ld32(sa + 32, r1);
+                    uint32_t r0[32], r1[32], r2[32], r3[32];
+                    tmem_ld32(s_col, r0);
+                    tmem_ld32(s_col + 32, r1);
+                    tmem_ld32(s_col + 64, r2);
+                    tmem_ld32(s_col + 96, r3);
                     tmem_wait_ld();
                     reg_fence(r0);
                     reg_fence(r1);
+                    reg_fence(r2);
+                    reg_fence(r3);
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
                         sv[i] = __uint_as_float(r0[i]);
                         sv[32 + i] = __uint_as_float(r1[i]);
+                        sv[64 + i] = __uint_as_float(r2[i]);
+                        sv[96 + i] = __uint_as_float(r3[i]);
                     }
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&ctl->s_empty[b]);
-
                 const int kb = tile_key_base(j, s.P, np);
-                if (kb < 0 || kb + kBlockN > unit_hi) {
-                    const int lo = -kb - hf * kHalfN, hi = row_hi - kb - hf * kHalfN;
+                if (kb < 0 || kb + kBlockN > slot_hi) {
+                    const int lo = -kb, hi = row_hi - kb;
 #pragma unroll
-                    for (int c = 0; c < kHalfN; ++c)
+                    for (int c = 0; c < kBlockN; ++c)
                         if (c < lo || c >= hi) sv[c] = -INFINITY;
                 }
                 float mx0 = sv[0], mx1 = sv[1], mx2 = sv[2], mx3 = sv[3];
 #pragma unroll
-                for (int c = 4; c < kHalfN; c += 4) {
+                for (int c = 4; c < kBlockN; c += 4) {
                     mx0 = fmaxf(mx0, sv[c]);
                     mx1 = fmaxf(mx1, sv[c + 1]);
                     mx2 = fmaxf(mx2, sv[c + 2]);
                     mx3 = fmaxf(mx3, sv[c + 3]);
                 }
-                float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)), mx_other;
-                if (!exchange(mx, mx_other)) { ok = false; break; }
-                const float m_tile = fmaxf(mx, mx_other) * sl2;
+                const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
                 const float m_new = fmaxf(m, m_tile);
                 float alpha = 1.f;
                 bool rescale = false;
                 if (j == 0) {
                     m = m_new;
                 } else {
-                    const bool need = m_new > m + 8.f;  // both halves of a row decide alike
+                    const bool need = m_new > m + 8.f;
                     rescale = __any_sync(0xffffffffu, need);
                     if (need) {
                         alpha = ex2(m - m_new);
@@ -530,98 +566,70 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                     }
                 }
                 const float m_use = m == -INFINITY ? 0.f : m;
-                uint32_t pk[kHalfN / 2];
+                // P as bf16 pairs over the first 64 columns of S: chunk c4 of 32
+                // scores goes to the 16 columns at 16 c4, all already read above.
                 float sum0 = 0.f, sum1 = 0.f;
 #pragma unroll
-                for (int c = 0; c < kHalfN; c += 2) {
-                    const float p0 = ex2(fmaf(sv[c], sl2, -m_use));
-                    const float p1 = ex2(fmaf(sv[c + 1], sl2, -m_use));
-                    sum0 += p0;
-                    sum1 += p1;
-                    pk[c / 2] = pack_bf16(p0, p1);
+                for (int c4 = 0; c4 < 4; ++c4) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float p0 = ex2(fmaf(sv[c4 * 32 + 2 * i], sl2, -m_use));
+                        const float p1 = ex2(fmaf(sv[c4 * 32 + 2 * i + 1], sl2, -m_use));
+                        sum0 += p0;
+                        sum1 += p1;
+                        pk[i] = pack_bf16(p0, p1);
+                    }
+                    tmem_st16(s_col + c4 * 16, pk);
                 }
                 l = l * alpha + (sum0 + sum1);
-                // P buffer b was last read by the PV MMA of tile t-2
-                if (j >= 2 && !warp_wait(&ctl->pv_done[b], ((t >> 1) & 1) ^ 1, ctl, hdr)) { ok = false; break; }
-                tmem_st32(tmem + lane_off + (b ? kColP1 : kColP0) + hf * (kHalfN / 2), pk);
-                tmem_wait_st();
                 if (rescale) {
-                    // O must hold the PV of tile t-1 before it is scaled
-                    if (!warp_wait(&ctl->pv_done[b ^ 1], ((t - 1) >> 1) & 1, ctl, hdr)) { ok = false; break; }
-                    tc_fence_after();
-                    const uint32_t oa = tmem + lane_off + kColO + hf * kHalfD;
-                    if constexpr (kHalfD >= 32) {
 #pragma unroll
-                        for (int c = 0; c < kHalfD; c += 32) {
-                            uint32_t o[32];
-                            tmem_ld32(oa + c, o);
-                            tmem_wait_ld();
-                            reg_fence(o);
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                            tmem_st32(oa + c, o);
-                        }
-                    } else {
-                        uint32_t o[16];
-                        tmem_ld16(oa, o);
+                    for (int c = 0; c < D; c += 32) {
+                        uint32_t o[32];
+                        tmem_ld32(o_col + c, o);
                         tmem_wait_ld();
                         reg_fence(o);
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                        tmem_st16(oa, o);
+                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                        tmem_st32(o_col + c, o);
                     }
-                    tmem_wait_st();
                 }
+                tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&ctl->p_full[b]);
+                if (lane == 0) mbar_arrive(&ctl->p_full[slot]);
             }
             if (!ok) break;
-            // epilogue: O of the unit is final once the PV of its last tile is done
-            float l_other;
-            if (!exchange(l, l_other)) break;
-            const float l_row = l + l_other;
-            const uint32_t tl = t - 1;
-            if (!warp_wait(&ctl->pv_done[tl & 1], (tl >> 1) & 1, ctl, hdr)) break;
+            // epilogue: O of the slot is final once the PV of its last tile is done
+            if (!warp_wait(&ctl->pv_done[slot], (ns + nt - 1) & 1, ctl, hdr)) break;
             tc_fence_after();
-            const float inv_l = 1.f / l_row;
+            const float inv_l = 1.f / l;
             const size_t row = (size_t)(s.q_start + tok) * p.n_heads + h;
-            uint4* dst = reinterpret_cast<uint4*>(p.out + row * D + hf * kHalfD);
-            const uint32_t oa = tmem + lane_off + kColO + hf * kHalfD;
-            auto store8 = [&](const uint32_t* o, int v) {
-                uint4 w;
-                w.x = pack_bf16(__uint_as_float(o[0]) * inv_l, __uint_as_float(o[1]) * inv_l);
-                w.y = pack_bf16(__uint_as_float(o[2]) * inv_l, __uint_as_float(o[3]) * inv_l);
-                w.z = pack_bf16(__uint_as_float(o[4]) * inv_l, __uint_as_float(o[5]) * inv_l);
-                w.w = pack_bf16(__uint_as_float(o[6]) * inv_l, __uint_as_float(o[7]) * inv_l);
-                dst[v] = w;
-            };
-            if constexpr (kHalfD >= 32) {
+            uint4* dst = reinterpret_cast<uint4*>(p.out + row * D);
 #pragma unroll
-                for (int c = 0; c < kHalfD; c += 32) {
-                    uint32_t o[32];
-                    tmem_ld32(oa + c, o);
-                    tmem_wait_ld();
-                    reg_fence(o);
-                    if (valid) {
-#pragma unroll
-                        for (int v4 = 0; v4 < 4; ++v4) store8(o + v4 * 8, c / 8 + v4);
-                    }
-                }
-            } else {
-                uint32_t o[16];
-                tmem_ld16(oa, o);
+            for (int c = 0; c < D; c += 32) {
+                uint32_t o[32];
+                tmem_ld32(o_col + c, o);
                 tmem_wait_ld();
                 reg_fence(o);
                 if (valid) {
-                    store8(o, 0);
-                    store8(o + 8, 1);
+#pragma unroll
+                    for (int v4 = 0; v4 < 4; ++v4) {
+                        uint4 w;
+                        w.x = pack_bf16(__uint_as_float(o[v4 * 8 + 0]) * inv_l, __uint_as_float(o[v4 * 8 + 1]) * inv_l);
+                        w.y = pack_bf16(__uint_as_float(o[v4 * 8 + 2]) * inv_l, __uint_as_float(o[v4 * 8 + 3]) * inv_l);
+                        w.z = pack_bf16(__uint_as_float(o[v4 * 8 + 4]) * inv_l, __uint_as_float(o[v4 * 8 + 5]) * inv_l);
+                        w.w = pack_bf16(__uint_as_float(o[v4 * 8 + 6]) * inv_l, __uint_as_float(o[v4 * 8 + 7]) * inv_l);
+                        dst[c / 8 + v4] = w;
+                    }
                 }
             }
-            if (valid && hf == 0 && p.lse) p.lse[row] = (m + lg2(l_row)) * 0.69314718055994530942f;
+            if (valid && p.lse) p.lse[row] = (m + lg2(l)) * 0.69314718055994530942f;
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&ctl->o_empty);
+            if (lane == 0) mbar_arrive(&ctl->o_empty[slot]);
+            ns += nt;
         }
     }
 

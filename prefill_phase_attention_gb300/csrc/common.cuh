@@ -6,8 +6,10 @@
 
 namespace pa {
 
-// Query rows per work unit (one tcgen05 MMA M) and keys per KV tile (MMA N of S = Q K^T).
+// Query rows per Q tile (one tcgen05 MMA M), Q tiles per work unit (they share
+// every K/V tile), and keys per KV tile (MMA N of S = Q K^T).
 constexpr int kBlockM = 128;
+constexpr int kSlots = 2;
 constexpr int kBlockN = 128;
 
 // Cost histogram of the longest-first scheduler (costs above the last bin share it).
@@ -21,14 +23,15 @@ struct SeqInfo {
     int pad;      // scheduler scratch: index of the sequence's first query block
 };
 
-// One work unit: query block [q0, q0 + 128/G) of sequence b against KV head kvh,
-// with all G query heads of that KV head packed into the 128 rows
-// (row r <-> token q0 + r / G, head kvh * G + r % G).
+// One work unit: query block [q0, q0 + 2 * (128/G)) of sequence b against KV
+// head kvh, split into two Q tiles ("slots") of 128/G tokens; in each tile the
+// G query heads of that KV head are packed into the 128 rows
+// (row r <-> token q0 + slot * 128/G + r / G, head kvh * G + r % G).
 struct Unit {
     int b;
     int kvh;
     int q0;
-    int ntiles;  // KV tiles the unit visits (its cost)
+    int ntiles;  // KV tiles the unit visits (its cost; the later slot visits all of them)
 };
 
 // Device workspace header; SeqInfo[num_seqs] and Unit[max_units] follow it.

@@ -65,7 +65,7 @@ __global__ void __launch_bounds__(1024) build_schedule_kernel(ScheduleArgs a) {
     __shared__ int s_total;
     const int tid = threadIdx.x;
     const int nthr = blockDim.x;
-    const int tpu = kBlockM / a.group;  // query tokens per unit
+    const int tpu = kSlots * (kBlockM / a.group);  // query tokens per unit
 
     for (int i = tid; i < kCostBins; i += nthr) hist[i] = 0;
 
