@@ -103,10 +103,9 @@ constexpr int smem_bytes() {
 
 __device__ __forceinline__ bool aborted(const Ctrl* c) { return *reinterpret_cast<const volatile int*>(&c->abort) != 0; }
 
-// Bounded wait; gives up when the CTA has aborted or after kTimeoutNs, in
-// which case it flags the CTA and the device error word.
-__device__ __noinline__ bool wait_bar(uint64_t* bar, uint32_t parity, Ctrl* c, WorkspaceHeader* hdr) {
-    if (mbar_try_wait(bar, parity)) return true;
+// Slow path of a bounded wait; gives up when the CTA has aborted or after
+// kTimeoutNs, in which case it flags the CTA and the device error word.
+__device__ __noinline__ bool wait_bar_slow(uint64_t* bar, uint32_t parity, Ctrl* c, WorkspaceHeader* hdr) {
     const uint64_t t0 = globaltimer_ns();
     for (;;) {
         for (int i = 0; i < 32; ++i)
@@ -118,6 +117,22 @@ __device__ __noinline__ bool wait_bar(uint64_t* bar, uint32_t parity, Ctrl* c, W
             return false;
         }
     }
+}
+
+// Bounded wait: one inline probe, then the out-of-line polling loop.
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, Ctrl* c, WorkspaceHeader* hdr) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return wait_bar_slow(bar, parity, c, hdr);
+}
+
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred = 0;
+    asm volatile(
+        "{\n\t.reg .pred P1;\n\t"
+        "elect.sync _|P1, 0xffffffff;\n\t"
+        "selp.b32 %0, 1, 0, P1;\n\t}"
+        : "+r"(pred));
+    return pred != 0;
 }
 
 // Warp-uniform bounded wait: every lane polls, then the warp agrees, so the
@@ -342,103 +357,120 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------- MMA issuer
-        if (lane == 0) {
-            const uint32_t q_addr = smem_u32(q_smem);
-            const uint32_t k_addr = smem_u32(k_smem);
-            const uint32_t v_addr = smem_u32(v_smem);
-            uint32_t t = 0;                // KV tiles of this CTA so far
-            uint32_t ns[kSlots] = {0, 0};  // tiles processed per slot so far
-            uint32_t no[kSlots] = {0, 0};  // units with the slot active so far
-            bool ok = true;
-            auto issue_s = [&](int i, uint32_t tt) {
-                const uint32_t kb = k_addr + (tt % C::kStagesK) * C::kTileBytes;
-                const uint32_t qa = q_addr + i * C::kTileBytes;
+        // The whole warp runs the loop (waits and descriptors stay warp-uniform);
+        // one elected lane issues the MMAs and commits.
+        const bool leader = elect_one();
+        const uint32_t q_addr = smem_u32(q_smem);
+        const uint32_t k_addr = smem_u32(k_smem);
+        const uint32_t v_addr = smem_u32(v_smem);
+        // descriptor templates; the start-address field (bits 0-13, 16-byte
+        // units) is advanced by adding (byte offset >> 4)
+        const uint64_t q_desc = smem_desc(q_addr, 16, C::kSbo, C::kSw);
+        const uint64_t k_desc = smem_desc(k_addr, 16, C::kSbo, C::kSw);
+        const uint64_t v_desc = smem_desc(v_addr, C::kChunkBytes, C::kSbo, C::kSw);
+        uint32_t t = 0;                // KV tiles of this CTA so far
+        uint32_t ns[kSlots] = {0, 0};  // tiles processed per slot so far
+        uint32_t no[kSlots] = {0, 0};  // units with the slot active so far
+        bool ok = true;
+        auto issue_s = [&](int i, uint32_t tt) {
+            if (leader) {
+                const uint32_t koff = (tt % C::kStagesK) * C::kTileBytes;
+                const uint32_t qoff = i * C::kTileBytes;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const int c = (kk * 16) / C::kChunkCols, w = (kk * 16) % C::kChunkCols;
-                    const uint64_t ad = smem_desc(qa + c * C::kChunkBytes + w * 2, 16, C::kSbo, C::kSw);
-                    const uint64_t bd = smem_desc(kb + c * C::kChunkBytes + w * 2, 16, C::kSbo, C::kSw);
-                    mma_ss(tmem + i * kColSlot, ad, bd, C::kIdescS, kk > 0 ? 1u : 0u);
+                    const uint32_t off = ((kk * 16) / C::kChunkCols) * C::kChunkBytes + ((kk * 16) % C::kChunkCols) * 2;
+                    mma_ss(tmem + i * kColSlot, q_desc + ((qoff + off) >> 4), k_desc + ((koff + off) >> 4),
+                           C::kIdescS, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(&ctl->s_full[i]);
-            };
-            auto issue_pv = [&](int i, uint32_t tt, bool first) {
-                const uint32_t vb = v_addr + (tt % C::kStagesV) * C::kTileBytes;
-#pragma unroll
-                for (int kk = 0; kk < kBlockN / 16; ++kk) {
-                    const uint64_t bd = smem_desc(vb + kk * 2 * C::kSbo, C::kChunkBytes, C::kSbo, C::kSw);
-                    mma_ts(tmem + i * kColSlot + kColO, tmem + i * kColSlot + kk * 8, bd, C::kIdescO,
-                           (!first || kk > 0) ? 1u : 0u);
-                }
-                mma_commit(&ctl->pv_done[i]);
-            };
-            for (int u_it = 0; ok; ++u_it) {
-                const int sl = u_it & 1;
-                if (!wait_bar(&ctl->unit_full[sl], (u_it >> 1) & 1, ctl, hdr)) break;
-                const Unit u = ctl->slot[sl].u;
-                const SeqInfo s = ctl->slot[sl].s;
-                mbar_arrive(&ctl->unit_empty[sl]);
-                if (u.b < 0) break;
-                const int nt[kSlots] = {slot_tiles(u, s, 0, tps, p.causal), slot_tiles(u, s, 1, tps, p.causal)};
-                if (!wait_bar(&ctl->q_full, u_it & 1, ctl, hdr)) break;
-                // prologue: S of tile 0 for both slots
-                if (!wait_bar(&ctl->k_full[t % C::kStagesK], (t / C::kStagesK) & 1, ctl, hdr)) break;
-                tc_fence_after();
-                for (int i = 0; i < kSlots; ++i)
-                    if (nt[i] > 0) issue_s(i, t);
-                mma_commit(&ctl->k_empty[t % C::kStagesK]);
-                if (u.ntiles == 1) mma_commit(&ctl->q_empty);
-                for (int j = 0; j < u.ntiles && ok; ++j) {
-                    const uint32_t tj = t + j;
-                    bool v_ready = false, k_ready = false;
-                    for (int i = 0; i < kSlots; ++i) {
-                        if (j < nt[i]) {
-                            // PV_i(j): P_i(j) written and O_i free (first tile of the unit)
-                            if (!wait_bar(&ctl->p_full[i], (ns[i] + j) & 1, ctl, hdr)) { ok = false; break; }
-                            if (j == 0 && !wait_bar(&ctl->o_empty[i], (no[i] & 1) ^ 1, ctl, hdr)) { ok = false; break; }
-                            if (!v_ready) {
-                                if (!wait_bar(&ctl->v_full[tj % C::kStagesV], (tj / C::kStagesV) & 1, ctl, hdr)) {
-                                    ok = false;
-                                    break;
-                                }
-                                v_ready = true;
-                            }
-                            tc_fence_after();
-                            issue_pv(i, tj, j == 0);
-                        }
-                        if (j + 1 < nt[i]) {
-                            // S_i(j+1) overwrites P_i(j): issued after PV_i(j) on the in-order tensor pipe
-                            if (!k_ready) {
-                                const uint32_t tn = tj + 1;
-                                if (!wait_bar(&ctl->k_full[tn % C::kStagesK], (tn / C::kStagesK) & 1, ctl, hdr)) {
-                                    ok = false;
-                                    break;
-                                }
-                                k_ready = true;
-                                tc_fence_after();
-                            }
-                            issue_s(i, tj + 1);
-                        }
-                    }
-                    if (!ok) break;
-                    if (j + 1 < u.ntiles) {
-                        mma_commit(&ctl->k_empty[(tj + 1) % C::kStagesK]);
-                        if (j + 2 == u.ntiles) mma_commit(&ctl->q_empty);
-                    }
-                    mma_commit(&ctl->v_empty[tj % C::kStagesV]);
-                }
-                for (int i = 0; i < kSlots; ++i) {
-                    ns[i] += nt[i];
-                    no[i] += nt[i] > 0 ? 1 : 0;
-                }
-                t += u.ntiles;
             }
-            // every MMA this thread issued has finished before TMEM is released
+            __syncwarp();
+        };
+        auto issue_pv = [&](int i, uint32_t tt, bool first) {
+            if (leader) {
+                const uint32_t voff = (tt % C::kStagesV) * C::kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < kBlockN / 16; ++kk)
+                    mma_ts(tmem + i * kColSlot + kColO, tmem + i * kColSlot + kk * 8,
+                           v_desc + ((voff + kk * 2 * C::kSbo) >> 4), C::kIdescO, (!first || kk > 0) ? 1u : 0u);
+                mma_commit(&ctl->pv_done[i]);
+            }
+            __syncwarp();
+        };
+        auto commit = [&](uint64_t* bar) {
+            if (leader) mma_commit(bar);
+            __syncwarp();
+        };
+        for (int u_it = 0; ok; ++u_it) {
+            const int sl = u_it & 1;
+            if (!warp_wait(&ctl->unit_full[sl], (u_it >> 1) & 1, ctl, hdr)) break;
+            const Unit u = ctl->slot[sl].u;
+            const SeqInfo s = ctl->slot[sl].s;
+            __syncwarp();
+            if (leader) mbar_arrive(&ctl->unit_empty[sl]);
+            if (u.b < 0) break;
+            const int nt[kSlots] = {slot_tiles(u, s, 0, tps, p.causal), slot_tiles(u, s, 1, tps, p.causal)};
+            if (!warp_wait(&ctl->q_full, u_it & 1, ctl, hdr)) break;
+            // prologue: S of tile 0 for both slots
+            if (!warp_wait(&ctl->k_full[t % C::kStagesK], (t / C::kStagesK) & 1, ctl, hdr)) break;
+            tc_fence_after();
+            for (int i = 0; i < kSlots; ++i)
+                if (nt[i] > 0) issue_s(i, t);
+            commit(&ctl->k_empty[t % C::kStagesK]);
+            if (u.ntiles == 1) commit(&ctl->q_empty);
+            for (int j = 0; j < u.ntiles && ok; ++j) {
+                const uint32_t tj = t + j;
+                bool v_ready = false, k_ready = false;
+                for (int i = 0; i < kSlots; ++i) {
+                    if (j < nt[i]) {
+                        // PV_i(j): P_i(j) written and O_i free (first tile of the unit)
+                        if (!warp_wait(&ctl->p_full[i], (ns[i] + j) & 1, ctl, hdr)) { ok = false; break; }
+                        if (j == 0 && !warp_wait(&ctl->o_empty[i], (no[i] & 1) ^ 1, ctl, hdr)) { ok = false; break; }
+                        if (!v_ready) {
+                            if (!warp_wait(&ctl->v_full[tj % C::kStagesV], (tj / C::kStagesV) & 1, ctl, hdr)) {
+                                ok = false;
+                                break;
+                            }
+                            v_ready = true;
+                        }
+                        tc_fence_after();
+                        issue_pv(i, tj, j == 0);
+                    }
+                    if (j + 1 < nt[i]) {
+                        // S_i(j+1) overwrites P_i(j): issued after PV_i(j) on the in-order tensor pipe
+                        if (!k_ready) {
+                            const uint32_t tn = tj + 1;
+                            if (!warp_wait(&ctl->k_full[tn % C::kStagesK], (tn / C::kStagesK) & 1, ctl, hdr)) {
+                                ok = false;
+                                break;
+                            }
+                            k_ready = true;
+                            tc_fence_after();
+                        }
+                        issue_s(i, tj + 1);
+                    }
+                }
+                if (!ok) break;
+                if (j + 1 < u.ntiles) {
+                    commit(&ctl->k_empty[(tj + 1) % C::kStagesK]);
+                    if (j + 2 == u.ntiles) commit(&ctl->q_empty);
+                }
+                commit(&ctl->v_empty[tj % C::kStagesV]);
+            }
+            for (int i = 0; i < kSlots; ++i) {
+                ns[i] += nt[i];
+                no[i] += nt[i] > 0 ? 1 : 0;
+            }
+            t += u.ntiles;
+        }
+        // every MMA this warp issued has finished before TMEM is released
+        if (leader) {
             mma_commit(&ctl->mma_drain);
             const uint64_t t0 = globaltimer_ns();
             while (!mbar_try_wait(&ctl->mma_drain, 0) && globaltimer_ns() - t0 < kTimeoutNs) {
             }
         }
+        __syncwarp();
     } else if (warp == 2 || warp == 3) {
         // -------------------------------------------------------- cache writers
         // Warp 3 writes K, warp 2 writes V.  Each walks every tile of its ring
