@@ -49,6 +49,16 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def kernel_sha256() -> str:
+    """Hash of the attention kernel's sources (ties stored ncu counters to a kernel version)."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("attn_fwd.cu", "ptx.cuh", "common.cuh"):
+        with open(os.path.join(ROOT, "prefill_phase_attention_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
 def host_cores() -> int:
     try:
         return len(os.sched_getaffinity(0))
@@ -287,7 +297,9 @@ def run_ours(args, ws, rank, local):
     traffic = None
     tpath = os.path.join(ROOT, "profiles", f"traffic_{wl.name}.json")
     if os.path.exists(tpath):
-        traffic = json.load(open(tpath)).get("bytes_per_launch")
+        rec = json.load(open(tpath))
+        if rec.get("kernel_sha256") == kernel_sha256():  # counters of this very kernel source only
+            traffic = rec.get("bytes_per_launch")
 
     # end to end through the public API: pinned host inputs -> device -> call -> host result
     h_in = [{kk: vv.pin_memory() for kk, vv in s.items()} for s in steps]
@@ -390,7 +402,7 @@ def main():
     ap.add_argument("--workload", default="long32k")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--cpu-budget", type=float, default=25.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--ref-rows", type=int, default=128, help="oracle rows per reference step")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps, reported as run
