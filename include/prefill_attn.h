@@ -117,6 +117,43 @@ pa_status prefill_attn_varlen(
     float scale, int causal, pa_stream_t stream);
 
 /*
+ * prefill_attn_varlen_noalloc -- prefill_attn_varlen that allocates nothing.
+ * The pages have no counterpart to this call; it exists for integration.
+ *
+ * Some callers cannot allocate device memory when they call in: serving
+ * engines that hand nearly all of HBM to their own KV-cache arena at start-up
+ * (a cudaMalloc would then fail, or carve into memory the arena counts on),
+ * and runtimes that forbid allocation on the request path because an
+ * allocation can synchronise the device and stall every stream.  This entry
+ * point takes the same arguments as prefill_attn_varlen and computes the same
+ * result, but the scheduler's scratch (the sanitised per-sequence metadata and
+ * the sorted work list) lives in one fixed array of about 1 MiB compiled into
+ * this library, instead of a workspace the library allocates.  That array is
+ * resident on every device that loads the library until the process exits.
+ *
+ * Limits: num_seqs <= 4096 and at most 61440 work units, where the host bounds
+ * the units as n_kv_heads * (ceil(total_q / (2 * (128 / G))) + num_seqs) with
+ * G = n_heads / n_kv_heads.  A larger call returns PA_ERR_UNSUPPORTED with the
+ * reason in prefill_attn_last_error() and launches nothing.
+ *
+ * The first call on each device looks up the array's device address on the
+ * host (cudaGetSymbolAddress); make that first call before any stream capture.
+ * Every call uses the same array: each call first clears its header (the work
+ * counter and the device error word), so calls whose work overlaps on the GPU
+ * -- on different streams, or on different host threads -- race on it and must
+ * be serialised by the caller.  The device error word of this variant is not
+ * reported by prefill_attn_device_status.
+ */
+pa_status prefill_attn_varlen_noalloc(
+    const void *q, const void *k, const void *v,
+    const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+    void *cache_k, void *cache_v, const int32_t *cache_offsets,
+    void *out, float *lse,
+    int num_seqs, int total_q, int max_cache_len,
+    int n_heads, int n_kv_heads, int head_dim,
+    float scale, int causal, pa_stream_t stream);
+
+/*
  * prefill_attn_varlen_validate -- strict host-side check of the same arguments.
  * Copies the three metadata arrays to the host (synchronises `stream`) and
  * checks every rule stated above: PA_OK or PA_ERR_INVALID_ARG with the reason

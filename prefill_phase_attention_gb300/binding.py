@@ -26,6 +26,7 @@ _VARLEN_ARGS = [_P] * 10 + [_I] * 6 + [_F, _I, _P]
 SIGNATURES = {
     "prefill_attn_varlen": (_I, _VARLEN_ARGS),
     "prefill_attn_varlen_validate": (_I, _VARLEN_ARGS),
+    "prefill_attn_varlen_noalloc": (_I, _VARLEN_ARGS),
     "prefill_attn_device_status": (_I, [_P, ctypes.POINTER(ctypes.c_int32)]),
     "prefill_attn_release": (None, []),
     "prefill_attn_status_string": (ctypes.c_char_p, [_I]),
@@ -110,6 +111,16 @@ def prefill_attn_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_k, cache_v, c
     args = _varlen_args(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_k, cache_v, cache_offsets, out, lse,
                         scale, causal, stream)
     _check(load().prefill_attn_varlen(*args))
+
+
+def prefill_attn_varlen_noalloc(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_k, cache_v, cache_offsets, out,
+                                lse=None, *, scale: Optional[float] = None, causal: bool = True,
+                                stream=None) -> None:
+    """Same as prefill_attn_varlen, with the scheduler scratch in the library's fixed
+    device array instead of an allocated workspace (see include/prefill_attn.h)."""
+    args = _varlen_args(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_k, cache_v, cache_offsets, out, lse,
+                        scale, causal, stream)
+    _check(load().prefill_attn_varlen_noalloc(*args))
 
 
 def prefill_attn_varlen_validate(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_k, cache_v, cache_offsets,

@@ -289,4 +289,117 @@ void prefill_attn_release(void) {
     g_ws.clear();
 }
 
+
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant: the scheduler scratch lives in a fixed device array.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr int kNoAllocMaxSeqs = 4096;
+constexpr int kNoAllocMaxUnits = 61440;
+constexpr size_t kNoAllocHeaderBytes = 16;
+constexpr size_t kNoAllocBytes = kNoAllocHeaderBytes + (size_t)kNoAllocMaxSeqs * sizeof(pa::SeqInfo) +
+                                 (size_t)kNoAllocMaxUnits * sizeof(pa::Unit);
+static_assert(sizeof(pa::WorkspaceHeader) <= kNoAllocHeaderBytes, "header size");
+
+// In host code this name is only a stand-in for the array; its device address
+// comes from cudaGetSymbolAddress, once per device.
+__device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
+
+std::mutex g_noalloc_mu;
+std::map<int, void*> g_noalloc_addr;
+
+pa_status noalloc_scratch(int dev, void** out) {
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    auto it = g_noalloc_addr.find(dev);
+    if (it != g_noalloc_addr.end()) {
+        *out = it->second;
+        return PA_OK;
+    }
+    void* ptr = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);  // the current device is `dev`
+    if (e != cudaSuccess || !ptr) return cuda_fail(e, "cudaGetSymbolAddress(scratch)");
+    g_noalloc_addr[dev] = ptr;
+    *out = ptr;
+    return PA_OK;
+}
+
+}  // namespace
+
+extern "C" pa_status prefill_attn_varlen_noalloc(const void* q, const void* k, const void* v,
+                                                 const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                                                 void* cache_k, void* cache_v, const int32_t* cache_offsets,
+                                                 void* out, float* lse, int num_seqs, int total_q,
+                                                 int max_cache_len, int n_heads, int n_kv_heads, int head_dim,
+                                                 float scale, int causal, pa_stream_t stream_) {
+    g_last_error.clear();
+    g_last_launches = 0;
+    pa_status s = check_args(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_k, cache_v, cache_offsets, out, lse,
+                             num_seqs, total_q, max_cache_len, n_heads, n_kv_heads, head_dim, scale, causal);
+    if (s != PA_OK) return s;
+    if (num_seqs == 0 || total_q == 0) return PA_OK;
+    const int group = n_heads / n_kv_heads;
+    const int tpu = pa::kSlots * (pa::kBlockM / group);
+    const long long units = (long long)n_kv_heads * ((total_q + tpu - 1) / tpu + num_seqs);
+    if (num_seqs > kNoAllocMaxSeqs)
+        return fail(PA_ERR_UNSUPPORTED, "num_seqs %d exceeds the allocation-free limit %d", num_seqs, kNoAllocMaxSeqs);
+    if (units > kNoAllocMaxUnits)
+        return fail(PA_ERR_UNSUPPORTED, "up to %lld work units exceed the allocation-free limit %d", units,
+                    kNoAllocMaxUnits);
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    void* scratch = nullptr;
+    s = noalloc_scratch(dev, &scratch);
+    if (s != PA_OK) return s;
+    // the array keeps the previous call's contents: clear the header (error word, counters)
+    e = cudaMemsetAsync(scratch, 0, kNoAllocHeaderBytes, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the scratch header");
+
+    pa::ScheduleArgs sa;
+    sa.cu_seqlens_q = cu_seqlens_q;
+    sa.cu_seqlens_k = cu_seqlens_k;
+    sa.cache_offsets = cache_offsets;
+    sa.hdr = static_cast<pa::WorkspaceHeader*>(scratch);
+    sa.seqs = reinterpret_cast<pa::SeqInfo*>(static_cast<unsigned char*>(scratch) + kNoAllocHeaderBytes);
+    sa.units = reinterpret_cast<pa::Unit*>(sa.seqs + kNoAllocMaxSeqs);
+    sa.num_seqs = num_seqs;
+    sa.total_q = total_q;
+    sa.max_cache_len = max_cache_len;
+    sa.n_kv_heads = n_kv_heads;
+    sa.group = group;
+    sa.causal = causal;
+    sa.max_units = kNoAllocMaxUnits;
+    e = pa::launch_build_schedule(sa, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "schedule launch");
+
+    pa::FwdParams p;
+    p.k = static_cast<const __nv_bfloat16*>(k);
+    p.v = static_cast<const __nv_bfloat16*>(v);
+    p.cache_k = static_cast<__nv_bfloat16*>(cache_k);
+    p.cache_v = static_cast<__nv_bfloat16*>(cache_v);
+    p.out = static_cast<__nv_bfloat16*>(out);
+    p.lse = lse;
+    p.hdr = sa.hdr;
+    p.seqs = sa.seqs;
+    p.units = sa.units;
+    p.n_heads = n_heads;
+    p.n_kv_heads = n_kv_heads;
+    p.group = group;
+    p.max_cache_len = max_cache_len;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.causal = causal;
+    e = pa::encode_fwd_maps(p, q, total_q, num_seqs, head_dim);
+    if (e != cudaSuccess) return cuda_fail(e, "tensor map encoding");
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    const int grid = (int)std::min<long long>(sms, units);
+    e = pa::launch_attn_fwd(p, head_dim, grid, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "attention launch");
+    g_last_launches = 2;
+    return PA_OK;
+}
