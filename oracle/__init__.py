@@ -32,6 +32,7 @@ ERRORS = {
     -4: "a sequence does not fit its cache slot",
     -5: "selected row out of range",
     -6: "out of memory",
+    -7: "a window needs the causal mask",
 }
 
 
@@ -54,7 +55,7 @@ def load_library(path: str):
     P = ctypes.c_void_p
     I = ctypes.c_int
     f.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, I,
-                  ctypes.c_double, I, P, ctypes.c_int64, I]
+                  ctypes.c_double, I, I, P, ctypes.c_int64, I]
     f.restype = I
     return lib
 
@@ -72,13 +73,14 @@ def _ptr(a: Optional[np.ndarray]):
 
 def prefill_attention(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_offsets, cache_k, cache_v, *,
                       n_heads: int, n_kv_heads: int, head_dim: int, max_cache_len: int,
-                      scale: float, causal: bool = True, rows: Optional[np.ndarray] = None,
+                      scale: float, causal: bool = True, window: int = 0, rows: Optional[np.ndarray] = None,
                       want_cache: bool = True, threads: int = 0, lib=None):
     """Run the oracle.
 
     q [T,H,d], k/v [T,Hk,d], cache_k/v [B,Hk,cap,d]: uint16 bf16 bit patterns.
     cu_seqlens_q/k [B+1], cache_offsets [B]: int32.
     rows: optional int64 array of flattened (token * n_heads + head) rows.
+    window: 0, or W > 0 (causal only): each query sees its W most recent keys.
 
     Returns (out float64 [T,H,d], lse float64 [T,H], cache_k', cache_v') where
     unselected rows of out/lse are NaN and the cache images are None when
@@ -102,7 +104,7 @@ def prefill_attention(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_offsets, cache_
     rc = lib.oracle_prefill_attention(
         _ptr(q), _ptr(k), _ptr(v), _ptr(cu_q), _ptr(cu_k), _ptr(off), _ptr(cache_k), _ptr(cache_v),
         _ptr(ck), _ptr(cv), _ptr(out), _ptr(lse),
-        num_seqs, max_cache_len, n_heads, n_kv_heads, head_dim, float(scale), int(bool(causal)),
+        num_seqs, max_cache_len, n_heads, n_kv_heads, head_dim, float(scale), int(bool(causal)), int(window),
         _ptr(sel), 0 if sel is None else sel.shape[0], int(threads))
     if rc != 0:
         raise ValueError(f"oracle: {ERRORS.get(rc, rc)}")

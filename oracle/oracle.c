@@ -34,6 +34,10 @@
  *    positions after its K/V are appended).
  *  - GQA: query head h reads KV head h / (n_heads / n_kv_heads)
  *    ([zwxr] §2.4: 32 query heads over 8 KV heads; contiguous groups).
+ *  - Sliding window (optional, causal only): with a window of W tokens the
+ *    query at absolute position p sees only keys p - W + 1 .. p, the W most
+ *    recent positions including itself ([yfxerp] §4.3: attend over the last
+ *    4096 tokens).
  *  - KV-cache production: cache[b][kvh][P + i][:] = k[cu_q[b] + i][kvh][:] (and
  *    the same for v), a bit copy into the (kv_heads, seq, head_dim) layout of
  *    [yfxerp] §2.1 / §3.2; every other cache entry is left as it was.
@@ -71,6 +75,7 @@ typedef struct {
     int num_seqs, cap, n_heads, n_kv_heads, d;
     double scale;
     int causal;
+    int window; /* 0: none */
 } problem;
 
 /* Key j of sequence b, KV head kvh: the cached prefix, then the new tokens. */
@@ -93,11 +98,12 @@ static void attend_row(const problem *pb, int b, int i, int h, double *s)
     const int kvh = h / (pb->n_heads / pb->n_kv_heads);
     const size_t t = (size_t)pb->cu_q[b] + (size_t)i;
     const uint16_t *qrow = pb->q + (t * pb->n_heads + h) * d;
-    /* visible keys: 0 .. last (inclusive) */
+    /* visible keys: first .. last (inclusive) */
     const int last = pb->causal ? P + i : Lk - 1;
+    const int first = (pb->causal && pb->window > 0 && P + i - pb->window + 1 > 0) ? P + i - pb->window + 1 : 0;
 
     double m = -INFINITY;
-    for (int j = 0; j <= last; ++j) {
+    for (int j = first; j <= last; ++j) {
         const uint16_t *kr = key_row(pb, pb->cache_k, pb->k, b, kvh, j);
         double dot = 0.0;
         for (int e = 0; e < d; ++e)
@@ -107,13 +113,13 @@ static void attend_row(const problem *pb, int b, int i, int h, double *s)
             m = s[j];
     }
     double Z = 0.0;
-    for (int j = 0; j <= last; ++j)
+    for (int j = first; j <= last; ++j)
         Z += exp(s[j] - m);
 
     double *orow = pb->out + (t * pb->n_heads + h) * d;
     for (int e = 0; e < d; ++e)
         orow[e] = 0.0;
-    for (int j = 0; j <= last; ++j) {
+    for (int j = first; j <= last; ++j) {
         const double w = exp(s[j] - m) / Z;
         const uint16_t *vr = key_row(pb, pb->cache_v, pb->v, b, kvh, j);
         for (int e = 0; e < d; ++e)
@@ -142,7 +148,7 @@ static int owner(const int32_t *cu_q, int num_seqs, int64_t t)
  *  -1 bad sizes, -2 cu_seqlens_q not starting at 0 or decreasing,
  *  -3 cu_seqlens_k inconsistent with cache_offsets + seqlen_q,
  *  -4 a sequence does not fit its cache slot, -5 a selected row out of range,
- *  -6 out of memory.
+ *  -6 out of memory, -7 a window without the causal mask.
  *
  * rows: optional list of (t * n_heads + h) query rows to compute; NULL = all.
  * Only the selected rows of out/lse are written.  The cache image
@@ -156,9 +162,11 @@ int oracle_prefill_attention(
     uint16_t *cache_k_out, uint16_t *cache_v_out,
     double *out, double *lse,
     int num_seqs, int max_cache_len, int n_heads, int n_kv_heads, int head_dim,
-    double scale, int causal,
+    double scale, int causal, int window,
     const int64_t *rows, int64_t n_rows, int n_threads)
 {
+    if (window < 0 || (window > 0 && !causal))
+        return -7;
     if (num_seqs < 0 || max_cache_len < 0 || n_heads <= 0 || n_kv_heads <= 0 || head_dim <= 0 ||
         n_heads % n_kv_heads != 0)
         return -1;
@@ -176,7 +184,7 @@ int oracle_prefill_attention(
     const int64_t total_q = num_seqs > 0 ? cu_seqlens_q[num_seqs] : 0;
 
     problem pb = {q, k, v, cache_k, cache_v, cu_seqlens_q, cache_offsets, out, lse,
-                  num_seqs, max_cache_len, n_heads, n_kv_heads, head_dim, scale, causal};
+                  num_seqs, max_cache_len, n_heads, n_kv_heads, head_dim, scale, causal, window};
 
     const int64_t n_all = total_q * n_heads;
     const int64_t n_work = rows ? n_rows : n_all;

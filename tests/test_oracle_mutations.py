@@ -22,8 +22,12 @@ MUTATIONS = {
                               "const int kvh = h % pb->n_kv_heads;"),
     "scale_dropped": ("s[j] = pb->scale * dot;", "s[j] = dot;"),
     "scale_divides": ("s[j] = pb->scale * dot;", "s[j] = dot / pb->scale;"),
-    "first_key_dropped_from_sum": ("for (int j = 0; j <= last; ++j)\n        Z += exp(s[j] - m);",
-                                   "for (int j = (last > 0); j <= last; ++j)\n        Z += exp(s[j] - m);"),
+    "first_key_dropped_from_sum": ("for (int j = first; j <= last; ++j)\n        Z += exp(s[j] - m);",
+                                   "for (int j = first + (last > first); j <= last; ++j)\n        Z += exp(s[j] - m);"),
+    "window_one_key_short": ("P + i - pb->window + 1 > 0) ? P + i - pb->window + 1 : 0;",
+                             "P + i - pb->window + 2 > 0) ? P + i - pb->window + 2 : 0;"),
+    "window_ignores_prefix": ("P + i - pb->window + 1 > 0) ? P + i - pb->window + 1 : 0;",
+                              "i - pb->window + 1 > 0) ? P + i - pb->window + 1 : P;"),
     "value_read_from_keys": ("key_row(pb, pb->cache_v, pb->v, b, kvh, j)",
                              "key_row(pb, pb->cache_k, pb->k, b, kvh, j)"),
     "lse_without_max": ("pb->lse[t * pb->n_heads + h] = m + log(Z);",
@@ -45,6 +49,8 @@ PIN_TESTS = [
     pins.test_cache_write_closed_form,
     pins.test_toy_shapes_and_decode_append,
     functools.partial(pins.test_matches_torch_sdpa_float64, case="r3", causal=True),
+    pins.test_window_closed_forms,
+    functools.partial(pins.test_window_matches_torch_sdpa_float64, window=37),
 ]
 
 

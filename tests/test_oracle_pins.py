@@ -21,14 +21,14 @@ from prefill_phase_attention_gb300 import workloads as W
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
 
-def run_oracle(oracle_mod, wl, cache_k, cache_v, inp, rows=None, causal=None):
+def run_oracle(oracle_mod, wl, cache_k, cache_v, inp, rows=None, causal=None, window=0):
     return oracle_mod.prefill_attention(
         W.bf16_bits(inp["q"]), W.bf16_bits(inp["k"]), W.bf16_bits(inp["v"]),
         inp["cu_seqlens_q"].numpy(), inp["cu_seqlens_k"].numpy(), inp["cache_offsets"].numpy(),
         W.bf16_bits(cache_k), W.bf16_bits(cache_v),
         n_heads=wl.n_heads, n_kv_heads=wl.n_kv_heads, head_dim=wl.head_dim,
         max_cache_len=wl.max_cache_len, scale=wl.scale,
-        causal=wl.causal if causal is None else causal, rows=rows)
+        causal=wl.causal if causal is None else causal, window=window, rows=rows)
 
 
 def f64(t):
@@ -291,7 +291,7 @@ def test_flop_and_kv_accounting_matches_pages():
 
 # ------------------------------------------- independent library routine ---
 
-def _sdpa_reference(wl, ck, cv, inp, causal):
+def _sdpa_reference(wl, ck, cv, inp, causal, window=0):
     """PyTorch float64 SDPA per (sequence, head) with an explicit bottom-right mask."""
     import torch.nn.functional as F
     T = inp["q"].shape[0]
@@ -308,7 +308,10 @@ def _sdpa_reference(wl, ck, cv, inp, causal):
         Q = inp["q"][cu[b]:cu[b + 1]].double()
         mask = torch.ones(n, P + n, dtype=torch.bool)
         if causal:
-            mask = torch.arange(P + n)[None, :] <= (P + torch.arange(n))[:, None]
+            key, qpos = torch.arange(P + n)[None, :], (P + torch.arange(n))[:, None]
+            mask = key <= qpos
+            if window > 0:
+                mask &= key > qpos - window
         for h in range(wl.n_heads):
             o = F.scaled_dot_product_attention(Q[None, :, h], K[None, :, h // G], V[None, :, h // G],
                                                attn_mask=mask[None], scale=wl.scale)
@@ -330,5 +333,64 @@ def test_matches_torch_sdpa_float64(oracle_mod, case, causal):
     cv = cv.nan_to_num(0.0)
     out, _, _, _ = run_oracle(oracle_mod, wl, ck, cv, inp, causal=causal)
     ref = _sdpa_reference(wl, ck, cv, inp, causal)
+    assert np.nanmax(np.abs(out - ref)) < 1e-12
+    assert np.array_equal(np.isnan(out), np.isnan(ref))
+
+
+# ------------------------------------------------------------ sliding window ---
+# [yfxerp] §4.3: with sliding_window = W the model attends over the last W
+# tokens; read as: the query at absolute position p sees keys p - W + 1 .. p.
+
+def test_window_closed_forms(oracle_mod):
+    wl = _custom("win", 4, 2, 32, [9, 6], [7, 0], cap=20)
+    ck, cv, (inp,) = W.make_inputs(wl)
+    # a window longer than every sequence changes nothing (bitwise)
+    full, lfull, _, _ = run_oracle(oracle_mod, wl, ck, cv, inp)
+    big, lbig, _, _ = run_oracle(oracle_mod, wl, ck, cv, inp, window=100)
+    assert np.array_equal(full, big) and np.array_equal(lfull, lbig)
+    # window 1: every row sees only itself -> out = v, lse = scale * q.k
+    one, lone, _, _ = run_oracle(oracle_mod, wl, ck, cv, inp, window=1)
+    G = wl.n_heads // wl.n_kv_heads
+    for t in range(inp["q"].shape[0]):
+        for h in range(wl.n_heads):
+            assert np.array_equal(one[t, h], f64(inp["v"][t, h // G]))
+            s_ = wl.scale * float(f64(inp["q"][t, h]) @ f64(inp["k"][t, h // G]))
+            assert lone[t, h] == pytest.approx(s_, abs=1e-13)
+    # equal keys, window 4: uniform weights over the last min(4, P+i+1) positions
+    key = inp["k"][0, 0].clone()
+    inp_eq = dict(inp, k=key.expand_as(inp["k"]).contiguous())
+    ck_eq = key.expand_as(ck).contiguous()
+    out, lse, _, _ = run_oracle(oracle_mod, wl, ck_eq, cv, inp_eq, window=4)
+    cu = inp["cu_seqlens_q"].tolist()
+    for b, P in enumerate([7, 0]):
+        for i in range(cu[b + 1] - cu[b]):
+            t = cu[b] + i
+            lo = max(0, P + i - 3)
+            for h in range(wl.n_heads):
+                kvh = h // G
+                allv = np.concatenate([f64(cv[b, kvh, :P]), f64(inp["v"][cu[b]:cu[b + 1], kvh])])
+                vals = allv[lo:P + i + 1]
+                assert np.allclose(out[t, h], vals.mean(axis=0), rtol=0, atol=1e-14)
+                s_ = wl.scale * float(f64(inp["q"][t, h]) @ f64(key))
+                assert lse[t, h] == pytest.approx(s_ + math.log(P + i + 1 - lo), abs=1e-13)
+    # rows of the windowed softmax sum to one
+    ones, _, _, _ = run_oracle(oracle_mod, wl, ck, torch.ones_like(cv), dict(inp, v=torch.ones_like(inp["v"])), window=5)
+    assert np.all(np.abs(ones - 1.0) <= 1e-15)
+
+
+def test_window_needs_causal(oracle_mod):
+    wl = _custom("winnc", 2, 2, 32, [3], [0], cap=4)
+    ck, cv, (inp,) = W.make_inputs(wl)
+    with pytest.raises(ValueError, match="causal"):
+        run_oracle(oracle_mod, wl, ck, cv, inp, causal=False, window=2)
+
+
+@pytest.mark.parametrize("window", [1, 37, 200])
+def test_window_matches_torch_sdpa_float64(oracle_mod, window):
+    wl = W.random_workload(77, head_dim=64, group=2, max_len=120, max_prefix=150)
+    ck, cv, (inp,) = W.make_inputs(wl)
+    ck, cv = ck.nan_to_num(0.0), cv.nan_to_num(0.0)
+    out, _, _, _ = run_oracle(oracle_mod, wl, ck, cv, inp, window=window)
+    ref = _sdpa_reference(wl, ck, cv, inp, True, window=window)
     assert np.nanmax(np.abs(out - ref)) < 1e-12
     assert np.array_equal(np.isnan(out), np.isnan(ref))
