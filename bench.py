@@ -165,7 +165,7 @@ def oracle_sample_rows(wl, step, target_rows: int, seed: int):
     return np.sort(rng.choice(T * wl.n_heads, size=n, replace=False)).astype(np.int64)
 
 
-def row_flops(wl, step, rows):
+def row_flops(wl, step, rows, window=0):
     """Causal FLOPs of the selected rows (4 * d per visible key)."""
     cu = np.array(step.cu_seqlens_q())
     off = np.array(step.cache_offsets)
@@ -174,10 +174,12 @@ def row_flops(wl, step, rows):
     i = t - cu[b]
     n_b = cu[b + 1] - cu[b]
     vis = off[b] + (i + 1 if wl.causal else n_b)
+    if window > 0:
+        vis = np.minimum(vis, window)
     return int(4 * wl.head_dim * vis.sum())
 
 
-def time_oracle(wl, inputs, rows, threads):
+def time_oracle(wl, inputs, rows, threads, window=0):
     import oracle
     from prefill_phase_attention_gb300 import workloads as W
     cache_k, cache_v, steps = inputs
@@ -188,25 +190,26 @@ def time_oracle(wl, inputs, rows, threads):
                              inp["cu_seqlens_q"].numpy(), inp["cu_seqlens_k"].numpy(),
                              inp["cache_offsets"].numpy(), ck, cv, n_heads=wl.n_heads,
                              n_kv_heads=wl.n_kv_heads, head_dim=wl.head_dim, max_cache_len=wl.max_cache_len,
-                             scale=wl.scale, causal=wl.causal, rows=rows, want_cache=False, threads=threads)
+                             scale=wl.scale, causal=wl.causal, window=window, rows=rows, want_cache=False,
+                             threads=threads)
     return time.perf_counter() - t0
 
 
-def cpu_baseline(wl, inputs, budget_s: float = 15.0):
+def cpu_baseline(wl, inputs, budget_s: float = 15.0, window: int = 0):
     """The oracle on this host's cores over a sample sized to about `budget_s` seconds."""
     import oracle
     oracle.build()
     cores = host_cores()
     step = wl.steps[-1]
-    time_oracle(wl, inputs, oracle_sample_rows(wl, step, 64, seed=10), cores)  # threads, page faults
+    time_oracle(wl, inputs, oracle_sample_rows(wl, step, 64, seed=10), cores, window)  # threads, page faults
     cal = oracle_sample_rows(wl, step, 512, seed=11)
-    dt = time_oracle(wl, inputs, cal, cores)
-    rate = row_flops(wl, step, cal) / max(dt, 1e-6)  # FLOP/s of the oracle on this host
-    per_row = row_flops(wl, step, cal) / cal.size
+    dt = time_oracle(wl, inputs, cal, cores, window)
+    rate = row_flops(wl, step, cal, window) / max(dt, 1e-6)  # FLOP/s of the oracle on this host
+    per_row = row_flops(wl, step, cal, window) / cal.size
     n = int(rate * budget_s / max(per_row, 1.0))
     rows = oracle_sample_rows(wl, step, max(512, n), seed=12)
-    dt = time_oracle(wl, inputs, rows, cores)
-    fl = row_flops(wl, step, rows)
+    dt = time_oracle(wl, inputs, rows, cores, window)
+    fl = row_flops(wl, step, rows, window)
     return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
             "sample": f"{rows.size} query rows (token, head) drawn uniformly from {wl.name} "
                       f"(launch {len(wl.steps) - 1}), {fl / 1e9:.1f} GFLOP causal, {dt:.1f} s, fp64 C + OpenMP",
@@ -236,8 +239,13 @@ def run_ours(args, ws, rank, local):
     stream = torch.cuda.current_stream()
 
     def call(d, o, l):
-        binding.prefill_attn_varlen(d["q"], d["k"], d["v"], d["cu_seqlens_q"], d["cu_seqlens_k"], ck, cv,
-                                    d["cache_offsets"], o, l, scale=wl.scale, causal=wl.causal)
+        if args.window:
+            binding.prefill_attn_varlen_ex(d["q"], d["k"], d["v"], d["cu_seqlens_q"], d["cu_seqlens_k"], ck, cv,
+                                           d["cache_offsets"], o, l, scale=wl.scale, causal=wl.causal,
+                                           window=args.window)
+        else:
+            binding.prefill_attn_varlen(d["q"], d["k"], d["v"], d["cu_seqlens_q"], d["cu_seqlens_k"], ck, cv,
+                                        d["cache_offsets"], o, l, scale=wl.scale, causal=wl.causal)
 
     def step():
         for d, o, l in zip(dev, outs, lses):
@@ -279,7 +287,7 @@ def run_ours(args, ws, rank, local):
         raise RuntimeError("device error word set during the timed region")
     per_call_ms = [a.elapsed_time(b) for a, b in ev]
     ms_step = ms_total / args.steps
-    flops_step = wl.flops()
+    flops_step = wl.flops(args.window)
     value = weak_scaling_value(flops_step, ms_total, args.steps, ws)
     tokens_s = ws * wl.tokens() / (ms_step * 1e-3)
 
@@ -288,7 +296,7 @@ def run_ours(args, ws, rank, local):
     # roofline of the dominant kernel: algorithmic causal FLOPs per call / mean call time
     per_launch = []
     for li, s in enumerate(wl.steps):
-        fl = 4 * wl.head_dim * wl.n_heads * s.visible_pairs(wl.causal)
+        fl = 4 * wl.head_dim * wl.n_heads * s.visible_pairs(wl.causal, args.window)
         times = per_call_ms[li::n_launch]
         per_launch.append((fl, statistics.mean(times)))
     fl_tot = sum(f for f, _ in per_launch)
@@ -335,7 +343,8 @@ def run_ours(args, ws, rank, local):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "tokens_per_s": round(tokens_s, 1),
         "pct_of_bf16_peak": round(100 * value / ws / peak, 2),
-        "config": {"workload": wl.name, "launches_per_step": n_launch, "num_seqs": wl.num_seqs,
+        "config": {"workload": wl.name + (f"+window{args.window}" if args.window else ""),
+                   "launches_per_step": n_launch, "window": args.window, "num_seqs": wl.num_seqs,
                    "tokens_per_step": wl.tokens(), "n_heads": wl.n_heads, "n_kv_heads": wl.n_kv_heads,
                    "head_dim": wl.head_dim, "causal": wl.causal, "causal_flops_per_step": flops_step,
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
@@ -354,7 +363,7 @@ def run_ours(args, ws, rank, local):
         "clocks": clocks,
     }
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(wl, inputs, budget_s=args.cpu_budget)
+        result["cpu_baseline"] = cpu_baseline(wl, inputs, budget_s=args.cpu_budget, window=args.window)
     if rank == 0:
         print(json.dumps(result), flush=True)
     if ws > 1:
@@ -375,12 +384,12 @@ def run_reference(args, ws, rank):
     step = wl.steps[-1]
     cores = host_cores()
     rows = oracle_sample_rows(wl, step, args.ref_rows, seed=13)
-    fl = row_flops(wl, step, rows)
+    fl = row_flops(wl, step, rows, args.window)
     for _ in range(args.warmup):
-        time_oracle(wl, inputs, rows, cores)
+        time_oracle(wl, inputs, rows, cores, args.window)
     total = 0.0
     for _ in range(args.steps):
-        total += time_oracle(wl, inputs, rows, cores)
+        total += time_oracle(wl, inputs, rows, cores, args.window)
     value = fl * args.steps / total / 1e12
     sample = (f"{rows.size} query rows (token, head) drawn uniformly from {wl.name} per step, "
               f"{fl / 1e9:.2f} GFLOP causal per step")
@@ -401,6 +410,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="long32k")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--window", type=int, default=0, help="sliding window (0: none; the bench line counts only "
+                                                             "the visible pairs)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=25.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--ref-rows", type=int, default=128, help="oracle rows per reference step")

@@ -117,6 +117,35 @@ pa_status prefill_attn_varlen(
     float scale, int causal, pa_stream_t stream);
 
 /*
+ * Options of prefill_attn_varlen_ex.  Zero-initialise the struct and set
+ * struct_size = sizeof(pa_options); a field past the struct_size the caller
+ * passes is taken as zero, so older callers keep working as fields are added.
+ */
+typedef struct pa_options {
+    uint32_t struct_size;
+    /* Sliding window ("attend over the last W tokens", sliding_window = 4096 in
+     * "大语言模型推理核心：Prefill与Decode原理及工程优化" (yfxerp.com), §4.3):
+     * 0 = none; W > 0 (requires causal = 1): the query at absolute position p
+     * sees keys p - W + 1 .. p only.  KV tiles wholly outside every window of a
+     * work unit are not read.  The cache still receives every new token. */
+    int32_t window;
+} pa_options;
+
+/*
+ * prefill_attn_varlen_ex -- prefill_attn_varlen with options (NULL = none).
+ * Same arguments, layouts, ownership and errors as prefill_attn_varlen, plus
+ * PA_ERR_INVALID_ARG for a bad option (reason in prefill_attn_last_error()).
+ */
+pa_status prefill_attn_varlen_ex(
+    const void *q, const void *k, const void *v,
+    const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+    void *cache_k, void *cache_v, const int32_t *cache_offsets,
+    void *out, float *lse,
+    int num_seqs, int total_q, int max_cache_len,
+    int n_heads, int n_kv_heads, int head_dim,
+    float scale, int causal, const pa_options *opts, pa_stream_t stream);
+
+/*
  * prefill_attn_varlen_noalloc -- prefill_attn_varlen that allocates nothing.
  * The pages have no counterpart to this call; it exists for integration.
  *

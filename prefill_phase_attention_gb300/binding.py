@@ -20,13 +20,20 @@ STATUS = {0: "PA_OK", 1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED", 3: "PA_E
           4: "PA_ERR_DEVICE_TIMEOUT", 5: "PA_ERR_DEVICE_METADATA"}
 DEVERR_METADATA, DEVERR_TIMEOUT, DEVERR_OVERFLOW = 0x1, 0x2, 0x4
 
+class PaOptions(ctypes.Structure):
+    """pa_options of include/prefill_attn.h."""
+    _fields_ = [("struct_size", ctypes.c_uint32), ("window", ctypes.c_int32)]
+
+
 # Entry points declared in include/prefill_attn.h: name -> (restype, argtypes)
 _P, _I, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
 _VARLEN_ARGS = [_P] * 10 + [_I] * 6 + [_F, _I, _P]
+_VARLEN_EX_ARGS = [_P] * 10 + [_I] * 6 + [_F, _I, ctypes.POINTER(PaOptions), _P]
 SIGNATURES = {
     "prefill_attn_varlen": (_I, _VARLEN_ARGS),
     "prefill_attn_varlen_validate": (_I, _VARLEN_ARGS),
     "prefill_attn_varlen_noalloc": (_I, _VARLEN_ARGS),
+    "prefill_attn_varlen_ex": (_I, _VARLEN_EX_ARGS),
     "prefill_attn_device_status": (_I, [_P, ctypes.POINTER(ctypes.c_int32)]),
     "prefill_attn_release": (None, []),
     "prefill_attn_status_string": (ctypes.c_char_p, [_I]),
@@ -111,6 +118,21 @@ def prefill_attn_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_k, cache_v, c
     args = _varlen_args(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_k, cache_v, cache_offsets, out, lse,
                         scale, causal, stream)
     _check(load().prefill_attn_varlen(*args))
+
+
+def make_options(window: int = 0) -> PaOptions:
+    return PaOptions(ctypes.sizeof(PaOptions), int(window))
+
+
+def prefill_attn_varlen_ex(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_k, cache_v, cache_offsets, out, lse=None, *,
+                           scale: Optional[float] = None, causal: bool = True, window: int = 0,
+                           stream=None) -> None:
+    """prefill_attn_varlen with options: `window` > 0 restricts each query to its
+    `window` most recent keys (causal only)."""
+    args = _varlen_args(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_k, cache_v, cache_offsets, out, lse,
+                        scale, causal, stream)
+    opts = make_options(window)
+    _check(load().prefill_attn_varlen_ex(*args[:-1], ctypes.byref(opts), args[-1]))
 
 
 def prefill_attn_varlen_noalloc(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_k, cache_v, cache_offsets, out,

@@ -127,9 +127,94 @@ pa_status check_args(const void* q, const void* k, const void* v, const int32_t*
     return PA_OK;
 }
 
+struct Options {
+    int window = 0;
+};
+
+// Reads the caller's options; fields past the caller's struct_size count as zero.
+pa_status read_options(const pa_options* opts, int causal, Options* o) {
+    *o = Options();
+    if (!opts) return PA_OK;
+    if (opts->struct_size < offsetof(pa_options, window) + sizeof(int32_t))
+        return fail(PA_ERR_INVALID_ARG, "pa_options.struct_size %u is too small", (unsigned)opts->struct_size);
+    o->window = opts->window;
+    if (o->window < 0) return fail(PA_ERR_INVALID_ARG, "window must be >= 0 (got %d)", o->window);
+    if (o->window > 0 && causal != 1) return fail(PA_ERR_INVALID_ARG, "a sliding window needs causal = 1");
+    return PA_OK;
+}
+
+// Upper bound on the work units of a call (host-side; device metadata unread).
+long long unit_bound(int total_q, int num_seqs, int n_heads, int n_kv_heads) {
+    const int group = n_heads / n_kv_heads;
+    const int tpu = pa::kSlots * (pa::kBlockM / group);  // query tokens per work unit
+    return (long long)n_kv_heads * ((total_q + tpu - 1) / tpu + num_seqs);
+}
+
+struct Scratch {
+    pa::WorkspaceHeader* hdr;
+    pa::SeqInfo* seqs;
+    pa::Unit* units;
+    int max_units;
+};
+
+// Enqueues the scheduler and the attention kernel (arguments already checked).
+pa_status enqueue(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q,
+                  const int32_t* cu_seqlens_k, void* cache_k, void* cache_v, const int32_t* cache_offsets, void* out,
+                  float* lse, int num_seqs, int total_q, int max_cache_len, int n_heads, int n_kv_heads,
+                  int head_dim, float scale, int causal, const Options& o, const Scratch& scr, long long units_bound,
+                  int dev, cudaStream_t stream) {
+    const int group = n_heads / n_kv_heads;
+    pa::ScheduleArgs sa;
+    sa.cu_seqlens_q = cu_seqlens_q;
+    sa.cu_seqlens_k = cu_seqlens_k;
+    sa.cache_offsets = cache_offsets;
+    sa.hdr = scr.hdr;
+    sa.seqs = scr.seqs;
+    sa.units = scr.units;
+    sa.num_seqs = num_seqs;
+    sa.total_q = total_q;
+    sa.max_cache_len = max_cache_len;
+    sa.n_kv_heads = n_kv_heads;
+    sa.group = group;
+    sa.causal = causal;
+    sa.window = o.window;
+    sa.max_units = scr.max_units;
+    cudaError_t e = pa::launch_build_schedule(sa, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "schedule launch");
+
+    pa::FwdParams p;
+    p.k = static_cast<const __nv_bfloat16*>(k);
+    p.v = static_cast<const __nv_bfloat16*>(v);
+    p.cache_k = static_cast<__nv_bfloat16*>(cache_k);
+    p.cache_v = static_cast<__nv_bfloat16*>(cache_v);
+    p.out = static_cast<__nv_bfloat16*>(out);
+    p.lse = lse;
+    p.hdr = scr.hdr;
+    p.seqs = scr.seqs;
+    p.units = scr.units;
+    p.n_heads = n_heads;
+    p.n_kv_heads = n_kv_heads;
+    p.group = group;
+    p.max_cache_len = max_cache_len;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.causal = causal;
+    p.window = o.window;
+    e = pa::encode_fwd_maps(p, q, total_q, num_seqs, head_dim);
+    if (e != cudaSuccess) return cuda_fail(e, "tensor map encoding");
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    const int grid = (int)std::min<long long>(sms, units_bound);
+    e = pa::launch_attn_fwd(p, head_dim, grid, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "attention launch");
+    g_last_launches = 2;
+    return PA_OK;
+}
+
 }  // namespace
 
 extern "C" {
+
 
 const char* prefill_attn_status_string(pa_status s) {
     switch (s) {
@@ -152,68 +237,37 @@ pa_status prefill_attn_varlen(const void* q, const void* k, const void* v, const
                               const int32_t* cache_offsets, void* out, float* lse, int num_seqs, int total_q,
                               int max_cache_len, int n_heads, int n_kv_heads, int head_dim, float scale,
                               int causal, pa_stream_t stream_) {
+    return prefill_attn_varlen_ex(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_k, cache_v, cache_offsets, out, lse,
+                                  num_seqs, total_q, max_cache_len, n_heads, n_kv_heads, head_dim, scale, causal,
+                                  nullptr, stream_);
+}
+
+pa_status prefill_attn_varlen_ex(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q,
+                                 const int32_t* cu_seqlens_k, void* cache_k, void* cache_v,
+                                 const int32_t* cache_offsets, void* out, float* lse, int num_seqs, int total_q,
+                                 int max_cache_len, int n_heads, int n_kv_heads, int head_dim, float scale,
+                                 int causal, const pa_options* opts, pa_stream_t stream_) {
     g_last_error.clear();
     g_last_launches = 0;
-    pa_status s = check_args(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_k, cache_v, cache_offsets, out, lse,
-                             num_seqs, total_q, max_cache_len, n_heads, n_kv_heads, head_dim, scale, causal);
+    Options o;
+    pa_status s = read_options(opts, causal, &o);
+    if (s != PA_OK) return s;
+    s = check_args(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_k, cache_v, cache_offsets, out, lse, num_seqs,
+                   total_q, max_cache_len, n_heads, n_kv_heads, head_dim, scale, causal);
     if (s != PA_OK) return s;
     if (num_seqs == 0 || total_q == 0) return PA_OK;
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-
-    const int group = n_heads / n_kv_heads;
-    const int tpu = pa::kSlots * (pa::kBlockM / group);  // query tokens per work unit
-    const long long max_units_ll = (long long)n_kv_heads * ((total_q + tpu - 1) / tpu + num_seqs);
+    const long long max_units_ll = unit_bound(total_q, num_seqs, n_heads, n_kv_heads);
     if (max_units_ll >= (1LL << 31)) return fail(PA_ERR_UNSUPPORTED, "too many work units");
     Workspace* ws = nullptr;
     s = get_workspace(dev, stream, num_seqs, (int)max_units_ll, &ws);
     if (s != PA_OK) return s;
-
-    pa::ScheduleArgs sa;
-    sa.cu_seqlens_q = cu_seqlens_q;
-    sa.cu_seqlens_k = cu_seqlens_k;
-    sa.cache_offsets = cache_offsets;
-    sa.hdr = static_cast<pa::WorkspaceHeader*>(ws->ptr);
-    sa.seqs = ws_seqs(*ws);
-    sa.units = ws_units(*ws);
-    sa.num_seqs = num_seqs;
-    sa.total_q = total_q;
-    sa.max_cache_len = max_cache_len;
-    sa.n_kv_heads = n_kv_heads;
-    sa.group = group;
-    sa.causal = causal;
-    sa.max_units = ws->max_units;
-    e = pa::launch_build_schedule(sa, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "schedule launch");
-
-    pa::FwdParams p;
-    p.k = static_cast<const __nv_bfloat16*>(k);
-    p.v = static_cast<const __nv_bfloat16*>(v);
-    p.cache_k = static_cast<__nv_bfloat16*>(cache_k);
-    p.cache_v = static_cast<__nv_bfloat16*>(cache_v);
-    p.out = static_cast<__nv_bfloat16*>(out);
-    p.lse = lse;
-    p.hdr = sa.hdr;
-    p.seqs = sa.seqs;
-    p.units = sa.units;
-    p.n_heads = n_heads;
-    p.n_kv_heads = n_kv_heads;
-    p.group = group;
-    p.max_cache_len = max_cache_len;
-    p.scale_log2 = scale * 1.4426950408889634f;
-    p.causal = causal;
-    e = pa::encode_fwd_maps(p, q, total_q, num_seqs, head_dim);
-    if (e != cudaSuccess) return cuda_fail(e, "tensor map encoding");
-    int sms = 0;
-    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
-    const int grid = (int)std::min<long long>(sms, max_units_ll);
-    e = pa::launch_attn_fwd(p, head_dim, grid, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "attention launch");
-    g_last_launches = 2;
-    return PA_OK;
+    Scratch scr{static_cast<pa::WorkspaceHeader*>(ws->ptr), ws_seqs(*ws), ws_units(*ws), ws->max_units};
+    return enqueue(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_k, cache_v, cache_offsets, out, lse, num_seqs, total_q,
+                   max_cache_len, n_heads, n_kv_heads, head_dim, scale, causal, o, scr, max_units_ll, dev, stream);
 }
 
 pa_status prefill_attn_varlen_validate(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q,
@@ -340,9 +394,7 @@ extern "C" pa_status prefill_attn_varlen_noalloc(const void* q, const void* k, c
                              num_seqs, total_q, max_cache_len, n_heads, n_kv_heads, head_dim, scale, causal);
     if (s != PA_OK) return s;
     if (num_seqs == 0 || total_q == 0) return PA_OK;
-    const int group = n_heads / n_kv_heads;
-    const int tpu = pa::kSlots * (pa::kBlockM / group);
-    const long long units = (long long)n_kv_heads * ((total_q + tpu - 1) / tpu + num_seqs);
+    const long long units = unit_bound(total_q, num_seqs, n_heads, n_kv_heads);
     if (num_seqs > kNoAllocMaxSeqs)
         return fail(PA_ERR_UNSUPPORTED, "num_seqs %d exceeds the allocation-free limit %d", num_seqs, kNoAllocMaxSeqs);
     if (units > kNoAllocMaxUnits)
@@ -358,48 +410,9 @@ extern "C" pa_status prefill_attn_varlen_noalloc(const void* q, const void* k, c
     // the array keeps the previous call's contents: clear the header (error word, counters)
     e = cudaMemsetAsync(scratch, 0, kNoAllocHeaderBytes, stream);
     if (e != cudaSuccess) return cuda_fail(e, "clearing the scratch header");
-
-    pa::ScheduleArgs sa;
-    sa.cu_seqlens_q = cu_seqlens_q;
-    sa.cu_seqlens_k = cu_seqlens_k;
-    sa.cache_offsets = cache_offsets;
-    sa.hdr = static_cast<pa::WorkspaceHeader*>(scratch);
-    sa.seqs = reinterpret_cast<pa::SeqInfo*>(static_cast<unsigned char*>(scratch) + kNoAllocHeaderBytes);
-    sa.units = reinterpret_cast<pa::Unit*>(sa.seqs + kNoAllocMaxSeqs);
-    sa.num_seqs = num_seqs;
-    sa.total_q = total_q;
-    sa.max_cache_len = max_cache_len;
-    sa.n_kv_heads = n_kv_heads;
-    sa.group = group;
-    sa.causal = causal;
-    sa.max_units = kNoAllocMaxUnits;
-    e = pa::launch_build_schedule(sa, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "schedule launch");
-
-    pa::FwdParams p;
-    p.k = static_cast<const __nv_bfloat16*>(k);
-    p.v = static_cast<const __nv_bfloat16*>(v);
-    p.cache_k = static_cast<__nv_bfloat16*>(cache_k);
-    p.cache_v = static_cast<__nv_bfloat16*>(cache_v);
-    p.out = static_cast<__nv_bfloat16*>(out);
-    p.lse = lse;
-    p.hdr = sa.hdr;
-    p.seqs = sa.seqs;
-    p.units = sa.units;
-    p.n_heads = n_heads;
-    p.n_kv_heads = n_kv_heads;
-    p.group = group;
-    p.max_cache_len = max_cache_len;
-    p.scale_log2 = scale * 1.4426950408889634f;
-    p.causal = causal;
-    e = pa::encode_fwd_maps(p, q, total_q, num_seqs, head_dim);
-    if (e != cudaSuccess) return cuda_fail(e, "tensor map encoding");
-    int sms = 0;
-    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
-    const int grid = (int)std::min<long long>(sms, units);
-    e = pa::launch_attn_fwd(p, head_dim, grid, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "attention launch");
-    g_last_launches = 2;
-    return PA_OK;
+    pa::SeqInfo* seqs = reinterpret_cast<pa::SeqInfo*>(static_cast<unsigned char*>(scratch) + kNoAllocHeaderBytes);
+    Scratch scr{static_cast<pa::WorkspaceHeader*>(scratch), seqs, reinterpret_cast<pa::Unit*>(seqs + kNoAllocMaxSeqs),
+                kNoAllocMaxUnits};
+    return enqueue(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_k, cache_v, cache_offsets, out, lse, num_seqs, total_q,
+                   max_cache_len, n_heads, n_kv_heads, head_dim, scale, causal, Options(), scr, units, dev, stream);
 }

@@ -42,6 +42,7 @@
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 
+#include <climits>
 #include <cstdint>
 #include <mutex>
 
@@ -165,10 +166,32 @@ __device__ __forceinline__ int tile_key_base(int j, int P, int np) {
     return j < np ? P - kBlockN * (np - j) : P + kBlockN * (j - np);
 }
 
-// KV tiles that slot `sl` of a unit visits (0 when the slot has no tokens).
-__device__ __forceinline__ int slot_tiles(const Unit& u, const SeqInfo& s, int sl, int tps, int causal) {
-    const int qs = u.q0 + sl * tps;
-    return qs < s.n ? unit_tiles(s.n, s.P, qs, tps, causal) : 0;
+// The KV tiles a unit streams, [lo, lo + ntiles) in the sequence's tile
+// numbering, and the sub-range [a[s], b[s]) of that stream each slot visits
+// (a = b = 0 when the slot has no tokens).  With a sliding window the later
+// slot may start after the earlier one; the two ranges always touch.
+struct UnitGeo {
+    int lo, ntiles, np;
+    int a[kSlots], b[kSlots];
+};
+
+__device__ __forceinline__ UnitGeo unit_geo(const Unit& u, const SeqInfo& s, int tps, int causal, int window) {
+    UnitGeo g;
+    g.np = prefix_tiles(s.P);
+    const TileSpan all = query_tiles(s.n, s.P, u.q0, min(u.q0 + kSlots * tps, s.n), causal, window);
+    g.lo = all.lo;
+    g.ntiles = all.hi - all.lo;
+#pragma unroll
+    for (int i = 0; i < kSlots; ++i) {
+        const int qs = u.q0 + i * tps;
+        g.a[i] = g.b[i] = 0;
+        if (qs < s.n) {
+            const TileSpan t = query_tiles(s.n, s.P, qs, min(qs + tps, s.n), causal, window);
+            g.a[i] = t.lo - g.lo;
+            g.b[i] = t.hi - g.lo;
+        }
+    }
+    return g;
 }
 
 // Rows of new-key tile j (j >= np) that hold this unit's own tokens
@@ -266,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     // unit from the cache (prefix tiles) or from the new tokens' k/v.
     auto load_kv_tile = [&](uint8_t* ring, int stages, uint64_t* full, uint64_t* empty, const CUtensorMap* tm_cache,
                             const CUtensorMap* tm_new, int* last_parity, uint32_t t, int j, const Unit& u,
-                            const SeqInfo& s, int np) -> bool {
+                            const SeqInfo& s, int np) -> bool {  // j: tile index in the sequence
         const int st = t % stages;
         const uint32_t ph = (t / stages) & 1;
         if (!wait_bar(&empty[st], ph ^ 1, ctl, hdr)) return false;
@@ -324,11 +347,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                         tma_load_3d(q_smem + i * C::kTileBytes + c * C::kChunkBytes, &p.tm_q, &ctl->q_full,
                                     c * C::kChunkCols, u.kvh * G, s.q_start + u.q0 + i * tps);
                 last_q_parity[0] = u_it & 1;
-                const int np = (s.P + kBlockN - 1) / kBlockN;
+                const UnitGeo ug = unit_geo(u, s, tps, p.causal, p.window);
                 bool ok = true;
-                for (int j = 0; j < u.ntiles && ok; ++j, ++t)
+                for (int j = 0; j < ug.ntiles && ok; ++j, ++t)
                     ok = load_kv_tile(k_smem, C::kStagesK, ctl->k_full, ctl->k_empty, &p.tm_ck, &p.tm_k,
-                                      last_k_parity, t, j, u, s, np);
+                                      last_k_parity, t, ug.lo + j, u, s, ug.np);
                 if (!ok) break;
             }
             if (aborted(ctl)) {
@@ -346,11 +369,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 const UnitSlot us = ctl->slot[sl];
                 mbar_arrive(&ctl->unit_empty[sl]);
                 if (us.u.b < 0) break;
-                const int np = (us.s.P + kBlockN - 1) / kBlockN;
+                const UnitGeo ug = unit_geo(us.u, us.s, tps, p.causal, p.window);
                 bool ok = true;
-                for (int j = 0; j < us.u.ntiles && ok; ++j, ++t)
+                for (int j = 0; j < ug.ntiles && ok; ++j, ++t)
                     ok = load_kv_tile(v_smem, C::kStagesV, ctl->v_full, ctl->v_empty, &p.tm_cv, &p.tm_v,
-                                      last_v_parity, t, j, us.u, us.s, np);
+                                      last_v_parity, t, ug.lo + j, us.u, us.s, ug.np);
                 if (!ok) break;
             }
             if (aborted(ctl)) drain(ctl->v_full, last_v_parity, C::kStagesV);
@@ -409,23 +432,24 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             __syncwarp();
             if (leader) mbar_arrive(&ctl->unit_empty[sl]);
             if (u.b < 0) break;
-            const int nt[kSlots] = {slot_tiles(u, s, 0, tps, p.causal), slot_tiles(u, s, 1, tps, p.causal)};
+            const UnitGeo ug = unit_geo(u, s, tps, p.causal, p.window);
+            const int ntiles = ug.ntiles;
             if (!warp_wait(&ctl->q_full, u_it & 1, ctl, hdr)) break;
-            // prologue: S of tile 0 for both slots
+            // prologue: S of tile 0 for the slots that start there
             if (!warp_wait(&ctl->k_full[t % C::kStagesK], (t / C::kStagesK) & 1, ctl, hdr)) break;
             tc_fence_after();
             for (int i = 0; i < kSlots; ++i)
-                if (nt[i] > 0) issue_s(i, t);
+                if (ug.a[i] == 0 && ug.b[i] > 0) issue_s(i, t);
             commit(&ctl->k_empty[t % C::kStagesK]);
-            if (u.ntiles == 1) commit(&ctl->q_empty);
-            for (int j = 0; j < u.ntiles && ok; ++j) {
+            if (ntiles == 1) commit(&ctl->q_empty);
+            for (int j = 0; j < ntiles && ok; ++j) {
                 const uint32_t tj = t + j;
                 bool v_ready = false, k_ready = false;
                 for (int i = 0; i < kSlots; ++i) {
-                    if (j < nt[i]) {
-                        // PV_i(j): P_i(j) written and O_i free (first tile of the unit)
-                        if (!warp_wait(&ctl->p_full[i], (ns[i] + j) & 1, ctl, hdr)) { ok = false; break; }
-                        if (j == 0 && !warp_wait(&ctl->o_empty[i], (no[i] & 1) ^ 1, ctl, hdr)) { ok = false; break; }
+                    if (j >= ug.a[i] && j < ug.b[i]) {
+                        // PV_i(j): P_i(j) written and O_i free (first tile of the slot)
+                        if (!warp_wait(&ctl->p_full[i], (ns[i] + j - ug.a[i]) & 1, ctl, hdr)) { ok = false; break; }
+                        if (j == ug.a[i] && !warp_wait(&ctl->o_empty[i], (no[i] & 1) ^ 1, ctl, hdr)) { ok = false; break; }
                         if (!v_ready) {
                             if (!warp_wait(&ctl->v_full[tj % C::kStagesV], (tj / C::kStagesV) & 1, ctl, hdr)) {
                                 ok = false;
@@ -434,9 +458,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                             v_ready = true;
                         }
                         tc_fence_after();
-                        issue_pv(i, tj, j == 0);
+                        issue_pv(i, tj, j == ug.a[i]);
                     }
-                    if (j + 1 < nt[i]) {
+                    if (j + 1 >= ug.a[i] && j + 1 < ug.b[i]) {
                         // S_i(j+1) overwrites P_i(j): issued after PV_i(j) on the in-order tensor pipe
                         if (!k_ready) {
                             const uint32_t tn = tj + 1;
@@ -451,17 +475,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                     }
                 }
                 if (!ok) break;
-                if (j + 1 < u.ntiles) {
+                if (j + 1 < ntiles) {
                     commit(&ctl->k_empty[(tj + 1) % C::kStagesK]);
-                    if (j + 2 == u.ntiles) commit(&ctl->q_empty);
+                    if (j + 2 == ntiles) commit(&ctl->q_empty);
                 }
                 commit(&ctl->v_empty[tj % C::kStagesV]);
             }
             for (int i = 0; i < kSlots; ++i) {
-                ns[i] += nt[i];
-                no[i] += nt[i] > 0 ? 1 : 0;
+                ns[i] += ug.b[i] - ug.a[i];
+                no[i] += ug.b[i] > ug.a[i] ? 1 : 0;
             }
-            t += u.ntiles;
+            t += ntiles;
         }
         // every MMA this warp issued has finished before TMEM is released
         if (leader) {
@@ -492,10 +516,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             __syncwarp();
             if (lane == 0) mbar_arrive(&ctl->unit_empty[sl]);
             if (us.u.b < 0) break;
-            const int np = (us.s.P + kBlockN - 1) / kBlockN;
+            const UnitGeo ug = unit_geo(us.u, us.s, tps, p.causal, p.window);
+            const int np = ug.np;
             const int q_end = min(us.u.q0 + kSlots * tps, us.s.n);
             bool ok = true;
-            for (int j = 0; j < us.u.ntiles; ++j, ++t) {
+            for (int jr = 0; jr < ug.ntiles; ++jr, ++t) {
+                const int j = ug.lo + jr;  // tile index in the sequence
                 const int st = t % stages;
                 if (!warp_wait(&full[st], (t / stages) & 1, ctl, hdr)) { ok = false; break; }
                 int lo_row, nrows;
@@ -531,16 +557,21 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             if (us.u.b < 0) break;
             const Unit u = us.u;
             const SeqInfo s = us.s;
-            const int nt = slot_tiles(u, s, slot, tps, p.causal);
+            const UnitGeo ug = unit_geo(u, s, tps, p.causal, p.window);
+            const int nt = ug.b[slot] - ug.a[slot];
             if (nt == 0) continue;
             const int qs = u.q0 + slot * tps;
+            const int qe = min(qs + tps, s.n);
             const int tok = qs + r / G;
             const int h = u.kvh * G + r % G;
             const bool valid = r < tps * G && tok < s.n;
             const int Lk = s.P + s.n;
             const int row_hi = p.causal ? min(s.P + tok + 1, Lk) : Lk;  // keys [0, row_hi) visible
             const int slot_hi = p.causal ? min(s.P + qs + 1, Lk) : Lk;  // smallest row_hi of the slot
-            const int np = (s.P + kBlockN - 1) / kBlockN;
+            // sliding window: keys [row_lo, row_hi) visible; slot_lo = largest row_lo of the slot
+            const int row_lo = (p.causal && p.window > 0) ? s.P + tok - p.window + 1 : INT_MIN / 2;
+            const int slot_lo = (p.causal && p.window > 0) ? s.P + qe - p.window : INT_MIN / 2;
+            const int np = ug.np;
             float m = -INFINITY, l = 0.f;
             bool ok = true;
             for (int j = 0; j < nt; ++j) {
@@ -568,9 +599,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                         sv[96 + i] = __uint_as_float(r3[i]);
                     }
                 }
-                const int kb = tile_key_base(j, s.P, np);
-                if (kb < 0 || kb + kBlockN > slot_hi) {
-                    const int lo = -kb, hi = row_hi - kb;
+                const int kb = tile_key_base(ug.lo + ug.a[slot] + j, s.P, np);
+                if (kb < 0 || kb + kBlockN > slot_hi || kb < slot_lo) {
+                    const int lo = max(-kb, row_lo - kb), hi = row_hi - kb;
 #pragma unroll
                     for (int c = 0; c < kBlockN; ++c)
                         if (c < lo || c >= hi) sv[c] = -INFINITY;

@@ -55,18 +55,44 @@ struct ScheduleArgs {
     int n_kv_heads;
     int group;      // n_heads / n_kv_heads
     int causal;
+    int window;     // sliding window (0: none)
     int max_units;  // capacity of the unit list
 };
 
-// Number of KV tiles of a unit.  The prefix [0, P) is cut into tiles that END
-// at P (the first one may start below 0 and is masked there), and the new keys
-// [P, P + n) into tiles that START at P, so no tile ever reads cache entries at
-// or past P.  Causal units stop at the tile holding their last query token.
-__host__ __device__ inline int unit_tiles(int n, int P, int q0, int tokens_per_unit, int causal) {
-    const int prefix_tiles = (P + kBlockN - 1) / kBlockN;
-    const int q_end = (q0 + tokens_per_unit < n) ? q0 + tokens_per_unit : n;
-    const int new_tiles = causal ? (q_end - 1) / kBlockN + 1 : (n + kBlockN - 1) / kBlockN;
-    return prefix_tiles + new_tiles;
+// KV tiles of a sequence with P cached tokens: the prefix [0, P) is cut into
+// tiles that END at P (the first one may start below 0 and is masked there),
+// and the new keys [P, P + n) into tiles that START at P, so no tile ever
+// reads cache entries at or past P.  Tile j < np = ceil(P / 128) covers keys
+// [P - 128 (np - j), ...), tile j >= np covers [P + 128 (j - np), ...).
+__host__ __device__ inline int prefix_tiles(int P) { return (P + kBlockN - 1) / kBlockN; }
+
+// Tile holding key position `key` (0 <= key < P + n).
+__host__ __device__ inline int key_tile(int key, int P) {
+    const int np = prefix_tiles(P);
+    return key < P ? np - (P - key + kBlockN - 1) / kBlockN : np + (key - P) / kBlockN;
+}
+
+struct TileSpan {
+    int lo, hi;  // tile indices [lo, hi)
+};
+
+// Tiles holding the keys that query tokens [qs, qe) (0 <= qs < qe <= n) see:
+// causal -> keys up to P + qe - 1, from P + qs - window + 1 when window > 0;
+// not causal -> all P + n keys.
+__host__ __device__ inline TileSpan query_tiles(int n, int P, int qs, int qe, int causal, int window) {
+    int klo = 0;
+    if (causal && window > 0 && P + qs - window + 1 > 0) klo = P + qs - window + 1;
+    const int khi = causal ? P + qe : P + n;  // exclusive
+    TileSpan t;
+    t.lo = key_tile(klo, P);
+    t.hi = key_tile(khi - 1, P) + 1;
+    return t;
+}
+
+// KV tiles a work unit streams (its cost): tokens [q0, min(q0 + tokens, n)).
+__host__ __device__ inline int unit_tiles(int n, int P, int q0, int tokens_per_unit, int causal, int window) {
+    const TileSpan t = query_tiles(n, P, q0, (q0 + tokens_per_unit < n) ? q0 + tokens_per_unit : n, causal, window);
+    return t.hi - t.lo;
 }
 
 }  // namespace pa

@@ -38,6 +38,7 @@ struct FwdParams {
     int n_heads, n_kv_heads, group, max_cache_len;
     float scale_log2;        // scale * log2(e)
     int causal;
+    int window;              // sliding window (0: none)
 };
 
 // Encodes the tensor maps of `p` (the pointer fields and sizes must be set).

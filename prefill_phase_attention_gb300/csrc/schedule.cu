@@ -105,7 +105,7 @@ __global__ void __launch_bounds__(1024) build_schedule_kernel(ScheduleArgs a) {
         const int b = block_owner(a.seqs, a.num_seqs, i);
         const SeqInfo si = a.seqs[b];
         const int q0 = (i - si.pad) * tpu;
-        atomicAdd(&hist[clamp_bin(unit_tiles(si.n, si.P, q0, tpu, a.causal))], a.n_kv_heads);
+        atomicAdd(&hist[clamp_bin(unit_tiles(si.n, si.P, q0, tpu, a.causal, a.window))], a.n_kv_heads);
     }
     __syncthreads();
 
@@ -131,7 +131,7 @@ __global__ void __launch_bounds__(1024) build_schedule_kernel(ScheduleArgs a) {
         const int b = block_owner(a.seqs, a.num_seqs, i);
         const SeqInfo si = a.seqs[b];
         const int q0 = (i - si.pad) * tpu;
-        const int cost = unit_tiles(si.n, si.P, q0, tpu, a.causal);
+        const int cost = unit_tiles(si.n, si.P, q0, tpu, a.causal, a.window);
         const int base = atomicAdd(&hist[clamp_bin(cost)], a.n_kv_heads);
         for (int kvh = 0; kvh < a.n_kv_heads; ++kvh) {
             const int pos = base + kvh;

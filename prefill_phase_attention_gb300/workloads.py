@@ -61,11 +61,17 @@ class Step:
         lk = [p + n for p, n in zip(self.cache_offsets, self.seqlens_q)]
         return [0] + list(np.cumsum(lk, dtype=np.int64).tolist())
 
-    def visible_pairs(self, causal: bool = True) -> int:
-        """Number of (query, key) pairs that the causal mask leaves visible."""
+    def visible_pairs(self, causal: bool = True, window: int = 0) -> int:
+        """Number of (query, key) pairs the mask leaves visible (window: causal
+        sliding window of that many most recent keys, 0 = none)."""
         tot = 0
         for n, p in zip(self.seqlens_q, self.cache_offsets):
-            tot += n * p + (n * (n + 1) // 2 if causal else n * n)
+            if causal and window > 0:
+                # query i sees min(p + i + 1, window) keys
+                full = max(0, min(n, window - p))          # rows with p + i + 1 <= window
+                tot += full * p + full * (full + 1) // 2 + (n - full) * window
+            else:
+                tot += n * p + (n * (n + 1) // 2 if causal else n * n)
         return tot
 
 
@@ -91,9 +97,9 @@ class Workload:
     def num_seqs(self) -> int:
         return self.steps[0].num_seqs
 
-    def flops(self) -> int:
+    def flops(self, window: int = 0) -> int:
         """Causal attention FLOPs: 4 * head_dim * n_heads per visible pair."""
-        return 4 * self.head_dim * self.n_heads * sum(s.visible_pairs(self.causal) for s in self.steps)
+        return 4 * self.head_dim * self.n_heads * sum(s.visible_pairs(self.causal, window) for s in self.steps)
 
     def tokens(self) -> int:
         return sum(s.total_q for s in self.steps)

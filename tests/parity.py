@@ -43,15 +43,20 @@ class Guarded:
         return bool((g == GUARD_F32).all())
 
 
-def run_step_gpu(wl, inp, cache_k_dev, cache_v_dev, guarded=True):
+def run_step_gpu(wl, inp, cache_k_dev, cache_v_dev, guarded=True, window=0):
     """One launch on the GPU; returns (out, lse) CUDA tensors (and checks guards)."""
     dev = {k: v.cuda() for k, v in inp.items()}
     T = inp["q"].shape[0]
     out = Guarded((T, wl.n_heads, wl.head_dim), torch.bfloat16)
     lse = Guarded((T, wl.n_heads), torch.float32)
-    binding.prefill_attn_varlen(dev["q"], dev["k"], dev["v"], dev["cu_seqlens_q"], dev["cu_seqlens_k"],
-                                cache_k_dev, cache_v_dev, dev["cache_offsets"], out.t, lse.t,
-                                scale=wl.scale, causal=wl.causal)
+    if window:
+        binding.prefill_attn_varlen_ex(dev["q"], dev["k"], dev["v"], dev["cu_seqlens_q"], dev["cu_seqlens_k"],
+                                       cache_k_dev, cache_v_dev, dev["cache_offsets"], out.t, lse.t,
+                                       scale=wl.scale, causal=wl.causal, window=window)
+    else:
+        binding.prefill_attn_varlen(dev["q"], dev["k"], dev["v"], dev["cu_seqlens_q"], dev["cu_seqlens_k"],
+                                    cache_k_dev, cache_v_dev, dev["cache_offsets"], out.t, lse.t,
+                                    scale=wl.scale, causal=wl.causal)
     torch.cuda.synchronize()
     assert out.guards_intact(), "write outside out"
     assert lse.guards_intact(), "write outside lse"
@@ -59,12 +64,13 @@ def run_step_gpu(wl, inp, cache_k_dev, cache_v_dev, guarded=True):
     return out.t, lse.t
 
 
-def oracle_step(wl, inp, cache_k_bits, cache_v_bits, rows=None, want_cache=True):
+def oracle_step(wl, inp, cache_k_bits, cache_v_bits, rows=None, want_cache=True, window=0):
     return oracle.prefill_attention(
         W.bf16_bits(inp["q"]), W.bf16_bits(inp["k"]), W.bf16_bits(inp["v"]),
         inp["cu_seqlens_q"].numpy(), inp["cu_seqlens_k"].numpy(), inp["cache_offsets"].numpy(),
         cache_k_bits, cache_v_bits, n_heads=wl.n_heads, n_kv_heads=wl.n_kv_heads, head_dim=wl.head_dim,
-        max_cache_len=wl.max_cache_len, scale=wl.scale, causal=wl.causal, rows=rows, want_cache=want_cache)
+        max_cache_len=wl.max_cache_len, scale=wl.scale, causal=wl.causal, window=window, rows=rows,
+        want_cache=want_cache)
 
 
 def compare(out_gpu, lse_gpu, out_ref, lse_ref, rows=None, label=""):

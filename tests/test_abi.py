@@ -80,3 +80,16 @@ def test_python_binding_refuses_cpu_tensors(lib):
     i = torch.zeros(2, dtype=torch.int32)
     with pytest.raises(ValueError):
         binding.prefill_attn_varlen(t, t, t, i, i, t[None], t[None], i[:1], t)
+
+
+def _call_ex(lib, window=0, causal=1, struct_size=None):
+    opts = binding.PaOptions(ctypes.sizeof(binding.PaOptions) if struct_size is None else struct_size, window)
+    return lib.prefill_attn_varlen_ex(16, 32, 48, 64, 80, 96, 112, 128, 144, None, 1, 4, 8, 4, 2, 64,
+                                      0.125, causal, ctypes.byref(opts), None)
+
+
+@pytest.mark.parametrize("kw,msg", [(dict(window=-1), "window"), (dict(window=8, causal=0), "causal"),
+                                    (dict(struct_size=2), "struct_size")])
+def test_options_are_checked_before_launch(lib, kw, msg):
+    assert _call_ex(lib, **kw) == 1
+    assert msg in lib.prefill_attn_last_error().decode()

@@ -394,3 +394,14 @@ def test_window_matches_torch_sdpa_float64(oracle_mod, window):
     ref = _sdpa_reference(wl, ck, cv, inp, True, window=window)
     assert np.nanmax(np.abs(out - ref)) < 1e-12
     assert np.array_equal(np.isnan(out), np.isnan(ref))
+
+
+def test_window_pair_count_matches_brute_force():
+    """The bench's FLOP accounting under a window equals a direct count."""
+    for lens, pref, win in (([9, 1, 30], [0, 5, 40], 7), ([300], [0], 64), ([5, 2, 3], [0, 0, 0], 0)):
+        step = W.Step(lens, pref)
+        brute = 0
+        for n, P in zip(lens, pref):
+            for i in range(n):
+                brute += (P + i + 1) if win == 0 else min(P + i + 1, win)
+        assert step.visible_pairs(True, win) == brute

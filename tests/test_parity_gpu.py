@@ -21,13 +21,14 @@ def _lib(oracle_mod):
         pytest.fail("GPU tests need CUDA")
 
 
-def _run_single_step(wl, rows=None):
+def _run_single_step(wl, rows=None, window=0):
     ck, cv, (inp,) = W.make_inputs(wl)
     ck_d = PT.Guarded(ck.shape, torch.bfloat16, fill=ck)
     cv_d = PT.Guarded(cv.shape, torch.bfloat16, fill=cv)
-    out, lse = PT.run_step_gpu(wl, inp, ck_d.t, cv_d.t)
+    out, lse = PT.run_step_gpu(wl, inp, ck_d.t, cv_d.t, window=window)
     assert ck_d.guards_intact() and cv_d.guards_intact(), "write outside the cache"
-    ref_out, ref_lse, ref_ck, ref_cv = PT.oracle_step(wl, inp, W.bf16_bits(ck), W.bf16_bits(cv), rows=rows)
+    ref_out, ref_lse, ref_ck, ref_cv = PT.oracle_step(wl, inp, W.bf16_bits(ck), W.bf16_bits(cv), rows=rows,
+                                                      window=window)
     stats = PT.compare(out, lse, ref_out, ref_lse, rows=rows, label=wl.name)
     assert np.array_equal(W.bf16_bits(ck_d.t.cpu()), ref_ck), "cache_k differs"
     assert np.array_equal(W.bf16_bits(cv_d.t.cpu()), ref_cv), "cache_v differs"
@@ -122,3 +123,26 @@ def test_inconsistent_device_metadata_is_flagged_and_skipped():
     with pytest.raises(binding.PrefillAttnError, match="cu_seqlens_k"):
         binding.prefill_attn_varlen_validate(dev["q"], dev["k"], dev["v"], dev["cu_seqlens_q"], bad_k, ck_d,
                                              cv_d, dev["cache_offsets"], out, None, scale=wl.scale)
+
+
+@pytest.mark.parametrize("seed", range(6))
+@pytest.mark.parametrize("d,group", [(32, 1), (64, 2), (128, 4), (128, 8)])
+@pytest.mark.parametrize("window", [1, 17, 128, 200, 1000])
+def test_sliding_window_random_shapes(seed, d, group, window):
+    wl = W.random_workload(seed * 7 + d + group + window, head_dim=d, group=group, n_kv_heads=2)
+    _run_single_step(wl, window=window)
+
+
+def test_sliding_window_long_prompt_sampled():
+    """8192-token prompt with the page's window of 4096 tokens (sampled rows)."""
+    wl = W.get("long8k")
+    rows = PT.sample_rows(wl.steps[0], wl.n_heads, 96, seed=8)
+    _run_single_step(wl, rows=rows, window=4096)
+
+
+def test_sliding_window_chunk_over_cached_prefix():
+    """Chunks over a long cached prefix with a window shorter than the prefix."""
+    wl = W.Workload("winchunk", 16, 4, 128, 3000, [W.Step([300, 1, 700], [2000, 1500, 600])], [2000, 1500, 600],
+                    seed=31)
+    for window in (64, 333, 1024):
+        _run_single_step(wl, window=window)
