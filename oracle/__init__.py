@@ -33,6 +33,7 @@ ERRORS = {
     -5: "selected row out of range",
     -6: "out of memory",
     -7: "a window needs the causal mask",
+    -8: "bad block table",
 }
 
 
@@ -55,7 +56,7 @@ def load_library(path: str):
     P = ctypes.c_void_p
     I = ctypes.c_int
     f.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, I,
-                  ctypes.c_double, I, I, P, ctypes.c_int64, I]
+                  ctypes.c_double, I, I, P, I, I, I, P, ctypes.c_int64, I]
     f.restype = I
     return lib
 
@@ -73,7 +74,8 @@ def _ptr(a: Optional[np.ndarray]):
 
 def prefill_attention(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_offsets, cache_k, cache_v, *,
                       n_heads: int, n_kv_heads: int, head_dim: int, max_cache_len: int,
-                      scale: float, causal: bool = True, window: int = 0, rows: Optional[np.ndarray] = None,
+                      scale: float, causal: bool = True, window: int = 0, block_table=None, block_size: int = 0,
+                      rows: Optional[np.ndarray] = None,
                       want_cache: bool = True, threads: int = 0, lib=None):
     """Run the oracle.
 
@@ -81,6 +83,8 @@ def prefill_attention(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_offsets, cache_
     cu_seqlens_q/k [B+1], cache_offsets [B]: int32.
     rows: optional int64 array of flattened (token * n_heads + head) rows.
     window: 0, or W > 0 (causal only): each query sees its W most recent keys.
+    block_table: optional int32 [B, max_blocks]; then cache_k/v are block pools
+    [num_blocks, Hk, block_size, d] and max_cache_len = max_blocks * block_size.
 
     Returns (out float64 [T,H,d], lse float64 [T,H], cache_k', cache_v') where
     unselected rows of out/lse are NaN and the cache images are None when
@@ -95,7 +99,14 @@ def prefill_attention(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_offsets, cache_
     total_q = int(cu_q[-1]) if num_seqs else 0
     assert q.size == total_q * n_heads * head_dim, "q size disagrees with cu_seqlens_q"
     assert k.size == total_q * n_kv_heads * head_dim and v.size == k.size
-    assert cache_k.size == num_seqs * n_kv_heads * max_cache_len * head_dim == cache_v.size
+    if block_table is None:
+        assert cache_k.size == num_seqs * n_kv_heads * max_cache_len * head_dim == cache_v.size
+        bt, max_blocks, num_blocks = None, 0, 0
+    else:
+        bt = np.ascontiguousarray(block_table, dtype=np.int32)
+        max_blocks = bt.shape[1]
+        num_blocks = cache_k.shape[0]
+        assert cache_k.shape == (num_blocks, n_kv_heads, block_size, head_dim) == cache_v.shape
     out = np.full((total_q, n_heads, head_dim), np.nan, dtype=np.float64)
     lse = np.full((total_q, n_heads), np.nan, dtype=np.float64)
     ck = np.empty_like(cache_k) if want_cache else None
@@ -105,7 +116,7 @@ def prefill_attention(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_offsets, cache_
         _ptr(q), _ptr(k), _ptr(v), _ptr(cu_q), _ptr(cu_k), _ptr(off), _ptr(cache_k), _ptr(cache_v),
         _ptr(ck), _ptr(cv), _ptr(out), _ptr(lse),
         num_seqs, max_cache_len, n_heads, n_kv_heads, head_dim, float(scale), int(bool(causal)), int(window),
-        _ptr(sel), 0 if sel is None else sel.shape[0], int(threads))
+        _ptr(bt), int(block_size), int(max_blocks), int(num_blocks), _ptr(sel), 0 if sel is None else sel.shape[0], int(threads))
     if rc != 0:
         raise ValueError(f"oracle: {ERRORS.get(rc, rc)}")
     if want_cache:

@@ -41,6 +41,11 @@
  *  - KV-cache production: cache[b][kvh][P + i][:] = k[cu_q[b] + i][kvh][:] (and
  *    the same for v), a bit copy into the (kv_heads, seq, head_dim) layout of
  *    [yfxerp] §2.1 / §3.2; every other cache entry is left as it was.
+ *  - Paged cache (optional; [zskr] §4.2, [yfxerp] §4.1, [zwxr] §3.4): the cache
+ *    is a pool of fixed-size blocks, [num_blocks][kv_heads][block_size][head_dim],
+ *    and position p of sequence b lives in row p % block_size of block
+ *    block_table[b][p / block_size].  Reads of the prefix and writes of the new
+ *    tokens both go through the table; blocks may be shared between sequences.
  *
  * Inputs q, k, v and the caches are bf16 bit patterns (uint16); each value is
  * widened exactly to fp64 before any arithmetic.  Outputs are fp64:
@@ -76,7 +81,19 @@ typedef struct {
     double scale;
     int causal;
     int window; /* 0: none */
+    const int32_t *block_table; /* paged cache: [num_seqs][max_blocks]; NULL: contiguous slots */
+    int block_size, max_blocks, num_blocks;
 } problem;
+
+/* Row of the cache holding position `pos` of sequence b, KV head kvh. */
+static size_t cache_row(const problem *pb, int b, int kvh, int pos)
+{
+    if (pb->block_table) {
+        const int blk = pb->block_table[(size_t)b * pb->max_blocks + pos / pb->block_size];
+        return ((size_t)blk * pb->n_kv_heads + kvh) * pb->block_size + (size_t)(pos % pb->block_size);
+    }
+    return ((size_t)b * pb->n_kv_heads + kvh) * pb->cap + (size_t)pos;
+}
 
 /* Key j of sequence b, KV head kvh: the cached prefix, then the new tokens. */
 static const uint16_t *key_row(const problem *pb, const uint16_t *cache, const uint16_t *fresh,
@@ -84,7 +101,7 @@ static const uint16_t *key_row(const problem *pb, const uint16_t *cache, const u
 {
     int P = pb->off[b];
     if (j < P)
-        return cache + (((size_t)b * pb->n_kv_heads + kvh) * pb->cap + (size_t)j) * pb->d;
+        return cache + cache_row(pb, b, kvh, j) * pb->d;
     return fresh + ((size_t)(pb->cu_q[b] + (j - P)) * pb->n_kv_heads + kvh) * pb->d;
 }
 
@@ -148,7 +165,10 @@ static int owner(const int32_t *cu_q, int num_seqs, int64_t t)
  *  -1 bad sizes, -2 cu_seqlens_q not starting at 0 or decreasing,
  *  -3 cu_seqlens_k inconsistent with cache_offsets + seqlen_q,
  *  -4 a sequence does not fit its cache slot, -5 a selected row out of range,
- *  -6 out of memory, -7 a window without the causal mask.
+ *  -6 out of memory, -7 a window without the causal mask, -8 a bad block table.
+ *
+ * Paged cache: block_table != NULL, the caches are [num_blocks][Hk][block_size]
+ * [head_dim] pools and max_cache_len must be max_blocks * block_size.
  *
  * rows: optional list of (t * n_heads + h) query rows to compute; NULL = all.
  * Only the selected rows of out/lse are written.  The cache image
@@ -163,6 +183,7 @@ int oracle_prefill_attention(
     double *out, double *lse,
     int num_seqs, int max_cache_len, int n_heads, int n_kv_heads, int head_dim,
     double scale, int causal, int window,
+    const int32_t *block_table, int block_size, int max_blocks, int num_blocks,
     const int64_t *rows, int64_t n_rows, int n_threads)
 {
     if (window < 0 || (window > 0 && !causal))
@@ -180,11 +201,20 @@ int oracle_prefill_attention(
             return -3;
         if (cache_offsets[b] < 0 || cache_offsets[b] + n > max_cache_len)
             return -4;
+        if (block_table) {
+            if (block_size <= 0 || max_blocks * block_size != max_cache_len)
+                return -8;
+            const int used = (cache_offsets[b] + n + block_size - 1) / block_size;
+            for (int L = 0; L < used; ++L)
+                if (block_table[(size_t)b * max_blocks + L] < 0 || block_table[(size_t)b * max_blocks + L] >= num_blocks)
+                    return -8;
+        }
     }
     const int64_t total_q = num_seqs > 0 ? cu_seqlens_q[num_seqs] : 0;
 
     problem pb = {q, k, v, cache_k, cache_v, cu_seqlens_q, cache_offsets, out, lse,
-                  num_seqs, max_cache_len, n_heads, n_kv_heads, head_dim, scale, causal, window};
+                  num_seqs, max_cache_len, n_heads, n_kv_heads, head_dim, scale, causal, window,
+                  block_table, block_size, max_blocks, num_blocks};
 
     const int64_t n_all = total_q * n_heads;
     const int64_t n_work = rows ? n_rows : n_all;
@@ -223,8 +253,8 @@ int oracle_prefill_attention(
         return -6;
 
     /* The cache image: everything as it was, plus the new tokens at P + i. */
-    const size_t slot = (size_t)max_cache_len * head_dim;
-    const size_t cache_elems = (size_t)num_seqs * n_kv_heads * slot;
+    const size_t cache_elems = block_table ? (size_t)num_blocks * n_kv_heads * block_size * head_dim
+                                           : (size_t)num_seqs * n_kv_heads * max_cache_len * head_dim;
     for (int c = 0; c < 2; ++c) {
         uint16_t *dst = c == 0 ? cache_k_out : cache_v_out;
         const uint16_t *src = c == 0 ? cache_k : cache_v;
@@ -238,7 +268,7 @@ int oracle_prefill_attention(
             const int n = cu_seqlens_q[b + 1] - cu_seqlens_q[b];
             for (int kvh = 0; kvh < n_kv_heads; ++kvh)
                 for (int i = 0; i < n; ++i)
-                    memcpy(dst + (((size_t)b * n_kv_heads + kvh) * max_cache_len + (size_t)(P + i)) * head_dim,
+                    memcpy(dst + cache_row(&pb, b, kvh, P + i) * head_dim,
                            fresh + ((size_t)(cu_seqlens_q[b] + i) * n_kv_heads + kvh) * head_dim,
                            (size_t)head_dim * sizeof(uint16_t));
         }

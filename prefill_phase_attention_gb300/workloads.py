@@ -199,6 +199,40 @@ def make_cache(wl: Workload, g: torch.Generator, sentinel: bool = True):
     return caches[0], caches[1]
 
 
+def make_paged_cache(wl: Workload, block_size: int, g: torch.Generator, extra_blocks: int = 3,
+                     sentinel: bool = True):
+    """A paged cache: (block_table [num_seqs, max_blocks] int32, pool_k, pool_v).
+
+    The pools are [num_blocks, n_kv_heads, block_size, head_dim] bf16 (CPU)
+    with num_blocks = num_seqs * max_blocks + extra_blocks, max_blocks =
+    ceil(max_cache_len / block_size); each sequence gets max_blocks distinct
+    physical blocks drawn by a seeded permutation.  Position p of sequence b
+    is row p % block_size of block table[b][p // block_size]; the first
+    ``wl.prefilled[b]`` positions hold seeded N(0,1) tokens, every other row
+    the NaN sentinel (or zero).
+    """
+    B, Hk, d = wl.num_seqs, wl.n_kv_heads, wl.head_dim
+    max_blocks = -(-wl.max_cache_len // block_size)
+    num_blocks = B * max_blocks + extra_blocks
+    perm = torch.randperm(num_blocks, generator=g)[: B * max_blocks]
+    table = perm.to(torch.int32).reshape(B, max_blocks)
+    pools = []
+    for _ in range(2):
+        c = torch.empty((num_blocks, Hk, block_size, d), dtype=torch.bfloat16)
+        if sentinel:
+            c.view(torch.int16).fill_(CACHE_SENTINEL_BITS)
+        else:
+            c.zero_()
+        for b, p in enumerate(wl.prefilled):
+            if p:
+                vals = _randn_bf16(g, (Hk, p, d))
+                for L in range(-(-p // block_size)):
+                    rows = min(block_size, p - L * block_size)
+                    c[int(table[b, L]), :, :rows] = vals[:, L * block_size: L * block_size + rows]
+        pools.append(c)
+    return table, pools[0], pools[1]
+
+
 def make_step_inputs(wl: Workload, step: Step, g: torch.Generator):
     """q [T,H,d], k/v [T,Hk,d] bf16 and the int32 metadata of one launch (CPU)."""
     t = step.total_q

@@ -32,10 +32,16 @@ MUTATIONS = {
                              "key_row(pb, pb->cache_k, pb->k, b, kvh, j)"),
     "lse_without_max": ("pb->lse[t * pb->n_heads + h] = m + log(Z);",
                         "pb->lse[t * pb->n_heads + h] = log(Z);"),
-    "cache_written_at_zero": ("* max_cache_len + (size_t)(P + i)) * head_dim",
-                              "* max_cache_len + (size_t)(i)) * head_dim"),
-    "prefix_keys_shifted": ("return cache + (((size_t)b * pb->n_kv_heads + kvh) * pb->cap + (size_t)j) * pb->d;",
-                            "return cache + (((size_t)b * pb->n_kv_heads + kvh) * pb->cap + (size_t)(j > 0 ? j - 1 : 0)) * pb->d;"),
+    "cache_written_at_zero": ("memcpy(dst + cache_row(&pb, b, kvh, P + i) * head_dim,",
+                              "memcpy(dst + cache_row(&pb, b, kvh, i) * head_dim,"),
+    "prefix_keys_shifted": ("return cache + cache_row(pb, b, kvh, j) * pb->d;",
+                            "return cache + cache_row(pb, b, kvh, j > 0 ? j - 1 : 0) * pb->d;"),
+    # paged cache (every mutant stays inside the pool: the pin tables fill every entry)
+    "paged_row_off_by_one": ("(size_t)(pos % pb->block_size);", "(size_t)((pos + 1) % pb->block_size);"),
+    "paged_pool_heads_outer": ("((size_t)blk * pb->n_kv_heads + kvh) * pb->block_size",
+                               "((size_t)kvh * pb->num_blocks + blk) * pb->block_size"),
+    "paged_table_of_first_seq": ("pb->block_table[(size_t)b * pb->max_blocks + pos / pb->block_size]",
+                                 "pb->block_table[pos / pb->block_size]"),
 }
 
 PIN_TESTS = [
@@ -51,6 +57,8 @@ PIN_TESTS = [
     functools.partial(pins.test_matches_torch_sdpa_float64, case="r3", causal=True),
     pins.test_window_closed_forms,
     functools.partial(pins.test_window_matches_torch_sdpa_float64, window=37),
+    functools.partial(pins.test_paged_equals_contiguous, bs=16, seed=1),
+    functools.partial(pins.test_paged_equals_contiguous, bs=5, seed=2),
 ]
 
 

@@ -21,14 +21,17 @@ from prefill_phase_attention_gb300 import workloads as W
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
 
-def run_oracle(oracle_mod, wl, cache_k, cache_v, inp, rows=None, causal=None, window=0):
+def run_oracle(oracle_mod, wl, cache_k, cache_v, inp, rows=None, causal=None, window=0,
+               block_table=None, block_size=0):
+    cap = wl.max_cache_len if block_table is None else block_table.shape[1] * block_size
     return oracle_mod.prefill_attention(
         W.bf16_bits(inp["q"]), W.bf16_bits(inp["k"]), W.bf16_bits(inp["v"]),
         inp["cu_seqlens_q"].numpy(), inp["cu_seqlens_k"].numpy(), inp["cache_offsets"].numpy(),
         W.bf16_bits(cache_k), W.bf16_bits(cache_v),
         n_heads=wl.n_heads, n_kv_heads=wl.n_kv_heads, head_dim=wl.head_dim,
-        max_cache_len=wl.max_cache_len, scale=wl.scale,
-        causal=wl.causal if causal is None else causal, window=window, rows=rows)
+        max_cache_len=cap, scale=wl.scale,
+        causal=wl.causal if causal is None else causal, window=window, rows=rows,
+        block_table=None if block_table is None else np.asarray(block_table, np.int32), block_size=block_size)
 
 
 def f64(t):
@@ -405,3 +408,127 @@ def test_window_pair_count_matches_brute_force():
             for i in range(n):
                 brute += (P + i + 1) if win == 0 else min(P + i + 1, win)
         assert step.visible_pairs(True, win) == brute
+
+
+# ---------------------------------------------------------------- paged cache ---
+# [zskr] §4.2, [yfxerp] §4.1, [zwxr] §3.4: the cache is a pool of fixed-size
+# blocks and a per-sequence block table maps logical block L (positions
+# [L bs, (L + 1) bs)) to a physical block; the layout of one block is
+# [kv_heads][block_size][head_dim] (the page's 16 x 16 x 128 block).
+
+def _scatter_to_pool(cache_bits, table, bs, num_blocks):
+    """Logical cache [B, Hk, cap, d] (uint16) -> pool [num_blocks, Hk, bs, d] by the table."""
+    B, Hk, cap, d = cache_bits.shape
+    pool = np.full((num_blocks, Hk, bs, d), W.CACHE_SENTINEL_BITS, np.uint16)
+    for b in range(B):
+        for pos in range(cap):
+            pool[table[b][pos // bs], :, pos % bs] = cache_bits[b, :, pos]
+    return pool
+
+
+def _gather_from_pool(pool, table, bs, cap):
+    B = len(table)
+    out = np.empty((B, pool.shape[1], cap, pool.shape[3]), np.uint16)
+    for b in range(B):
+        for pos in range(cap):
+            out[b, :, pos] = pool[table[b][pos // bs], :, pos % bs]
+    return out
+
+
+def _paged_case(oracle_mod, wl, bs, seed, extra=4):
+    """Runs wl contiguous and paged (random physical blocks); returns both results."""
+    ck, cv, (inp,) = W.make_inputs(wl)
+    rng = np.random.default_rng(seed)
+    maxb = -(-wl.max_cache_len // bs)
+    cap = maxb * bs
+    # pad the logical cache to whole blocks with the sentinel
+    pad = lambda c: np.concatenate([W.bf16_bits(c), np.full(c.shape[:2] + (cap - c.shape[2], c.shape[3]),
+                                                            W.CACHE_SENTINEL_BITS, np.uint16)], axis=2)
+    ckb, cvb = pad(ck), pad(cv)
+    nb = wl.num_seqs * maxb + extra
+    table = rng.permutation(nb)[: wl.num_seqs * maxb].reshape(wl.num_seqs, maxb).astype(np.int32)
+    pk, pv = _scatter_to_pool(ckb, table, bs, nb), _scatter_to_pool(cvb, table, bs, nb)
+    as_bf16 = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+    cont = oracle_mod.prefill_attention(
+        W.bf16_bits(inp["q"]), W.bf16_bits(inp["k"]), W.bf16_bits(inp["v"]),
+        inp["cu_seqlens_q"].numpy(), inp["cu_seqlens_k"].numpy(), inp["cache_offsets"].numpy(), ckb, cvb,
+        n_heads=wl.n_heads, n_kv_heads=wl.n_kv_heads, head_dim=wl.head_dim, max_cache_len=cap,
+        scale=wl.scale, causal=wl.causal)
+    paged = run_oracle(oracle_mod, wl, as_bf16(pk), as_bf16(pv), inp, block_table=table, block_size=bs)
+    return cont, paged, table, (pk, pv), cap
+
+
+@pytest.mark.parametrize("bs,seed", [(16, 1), (5, 2), (1, 3), (64, 4)])
+def test_paged_equals_contiguous(oracle_mod, bs, seed):
+    """Any placement of the blocks gives the contiguous result bit for bit, and
+    the new tokens land in the rows the table names (and nowhere else)."""
+    wl = W.random_workload(60 + seed, head_dim=32, group=2, max_len=70, max_prefix=90)
+    (o1, l1, ck1, cv1), (o2, l2, pk2, pv2), table, (pk, pv), cap = _paged_case(oracle_mod, wl, bs, seed)
+    assert np.array_equal(o1, o2, equal_nan=True) and np.array_equal(l1, l2, equal_nan=True)
+    assert np.array_equal(_gather_from_pool(pk2, table, bs, cap), ck1)
+    assert np.array_equal(_gather_from_pool(pv2, table, bs, cap), cv1)
+    unused = np.setdiff1d(np.arange(pk.shape[0]), table.ravel())
+    assert np.array_equal(pk2[unused], pk[unused]) and np.array_equal(pv2[unused], pv[unused])
+
+
+def test_paged_matches_torch_sdpa_float64(oracle_mod):
+    """Paged read path against the library routine on the gathered logical cache."""
+    wl = W.random_workload(71, head_dim=64, group=4, max_len=60, max_prefix=100)
+    ck, cv, (inp,) = W.make_inputs(wl, sentinel=False)
+    bs = 8
+    g = torch.Generator().manual_seed(5)
+    table, pk, pv = W.make_paged_cache(wl, bs, g, sentinel=False)
+    out, _, _, _ = run_oracle(oracle_mod, wl, pk, pv, inp, block_table=table.numpy(), block_size=bs)
+    cap = table.shape[1] * bs
+    tb = table.numpy()
+    lk = torch.from_numpy(_gather_from_pool(W.bf16_bits(pk), tb, bs, cap).view(np.int16)).view(torch.bfloat16)
+    lv = torch.from_numpy(_gather_from_pool(W.bf16_bits(pv), tb, bs, cap).view(np.int16)).view(torch.bfloat16)
+    ref = _sdpa_reference(wl, lk, lv, inp, True)
+    assert np.nanmax(np.abs(out - ref)) < 1e-12
+
+
+def test_paged_shared_prefix_blocks(oracle_mod):
+    """Two requests with the same 2-block prefix may map it to the same physical
+    blocks (prefix caching, [zwxr] §3.4): same result as private copies."""
+    bs, H, Hk, d = 16, 4, 2, 32
+    wl = _custom("shared", H, Hk, d, [20, 9], [32, 32], cap=64)
+    ck, cv, (inp,) = W.make_inputs(wl)
+    ck[1, :, :32] = ck[0, :, :32]
+    cv[1, :, :32] = cv[0, :, :32]
+    private = np.array([[0, 1, 2, 3], [4, 5, 6, 7]], np.int32)
+    shared = np.array([[0, 1, 2, 3], [0, 1, 6, 7]], np.int32)
+    nb = 8
+    pk = _scatter_to_pool(W.bf16_bits(ck), private, bs, nb)
+    pv = _scatter_to_pool(W.bf16_bits(cv), private, bs, nb)
+    as_bf16 = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+    o1, l1, pk1, _ = run_oracle(oracle_mod, wl, as_bf16(pk), as_bf16(pv), inp, block_table=private, block_size=bs)
+    pk_s, pv_s = pk.copy(), pv.copy()
+    pk_s[4:6] = W.CACHE_SENTINEL_BITS  # the private copies are not read any more
+    pv_s[4:6] = W.CACHE_SENTINEL_BITS
+    o2, l2, pk2, _ = run_oracle(oracle_mod, wl, as_bf16(pk_s), as_bf16(pv_s), inp, block_table=shared, block_size=bs)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+    assert np.array_equal(pk2[[0, 1, 2, 3, 6, 7]], pk1[[0, 1, 2, 3, 6, 7]])
+
+
+def test_paged_bad_block_table_is_rejected(oracle_mod):
+    bs = 4
+    wl = _custom("badpaged", 2, 2, 32, [3, 2], [5, 0], cap=8)
+    ck, cv, (inp,) = W.make_inputs(wl)
+    g = torch.Generator().manual_seed(0)
+    table, pk, pv = W.make_paged_cache(wl, bs, g)
+    for bad in (-1, pk.shape[0]):
+        t = table.numpy().copy()
+        t[0, 1] = bad
+        with pytest.raises(ValueError, match="block table"):
+            run_oracle(oracle_mod, wl, pk, pv, inp, block_table=t, block_size=bs)
+    # entries past the blocks a sequence uses are not looked at
+    t = table.numpy().copy()
+    t[1, 1] = -1
+    run_oracle(oracle_mod, wl, pk, pv, inp, block_table=t, block_size=bs)
+    # max_cache_len must be max_blocks * block_size
+    with pytest.raises(ValueError, match="block table"):
+        oracle_mod.prefill_attention(
+            W.bf16_bits(inp["q"]), W.bf16_bits(inp["k"]), W.bf16_bits(inp["v"]),
+            inp["cu_seqlens_q"].numpy(), inp["cu_seqlens_k"].numpy(), inp["cache_offsets"].numpy(),
+            W.bf16_bits(pk), W.bf16_bits(pv), n_heads=2, n_kv_heads=2, head_dim=32, max_cache_len=9,
+            scale=wl.scale, block_table=table.numpy(), block_size=bs)
