@@ -232,17 +232,25 @@ def run_ours(args, ws, rank, local):
     wl = W.get(args.workload)
     inputs = W.make_inputs(wl, sentinel=False)
     cache_k, cache_v, steps = inputs
-    ck, cv = cache_k.cuda(), cache_v.cuda()
+    table_d = None
+    if args.paged:
+        # the same workload over a paged cache: a block pool + per-sequence block table
+        table, pool_k, pool_v = W.make_paged_cache(wl, args.paged, torch.Generator().manual_seed(wl.seed),
+                                                   sentinel=False)
+        ck, cv, table_d = pool_k.cuda(), pool_v.cuda(), table.cuda()
+        del pool_k, pool_v
+    else:
+        ck, cv = cache_k.cuda(), cache_v.cuda()
     dev = [{k: v.cuda() for k, v in s.items()} for s in steps]
     outs = [torch.empty_like(d["q"]) for d in dev]
     lses = [torch.empty(d["q"].shape[0], wl.n_heads, device="cuda", dtype=torch.float32) for d in dev]
     stream = torch.cuda.current_stream()
 
     def call(d, o, l):
-        if args.window:
+        if args.window or args.paged:
             binding.prefill_attn_varlen_ex(d["q"], d["k"], d["v"], d["cu_seqlens_q"], d["cu_seqlens_k"], ck, cv,
                                            d["cache_offsets"], o, l, scale=wl.scale, causal=wl.causal,
-                                           window=args.window)
+                                           window=args.window, block_table=table_d)
         else:
             binding.prefill_attn_varlen(d["q"], d["k"], d["v"], d["cu_seqlens_q"], d["cu_seqlens_k"], ck, cv,
                                         d["cache_offsets"], o, l, scale=wl.scale, causal=wl.causal)
@@ -303,7 +311,8 @@ def run_ours(args, ws, rank, local):
     t_tot = sum(t for _, t in per_launch)
     achieved = fl_tot / (t_tot * 1e-3) / 1e12
     traffic = None
-    tpath = os.path.join(ROOT, "profiles", f"traffic_{wl.name}.json")
+    variant = (f"_window{args.window}" if args.window else "") + (f"_paged{args.paged}" if args.paged else "")
+    tpath = os.path.join(ROOT, "profiles", f"traffic_{wl.name}{variant}.json")
     if os.path.exists(tpath):
         rec = json.load(open(tpath))
         if rec.get("kernel_sha256") == kernel_sha256():  # counters of this very kernel source only
@@ -343,8 +352,10 @@ def run_ours(args, ws, rank, local):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "tokens_per_s": round(tokens_s, 1),
         "pct_of_bf16_peak": round(100 * value / ws / peak, 2),
-        "config": {"workload": wl.name + (f"+window{args.window}" if args.window else ""),
+        "config": {"workload": wl.name + (f"+window{args.window}" if args.window else "")
+                   + (f"+paged{args.paged}" if args.paged else ""),
                    "launches_per_step": n_launch, "window": args.window, "num_seqs": wl.num_seqs,
+                   "kv_cache": f"paged, {args.paged}-token blocks" if args.paged else "contiguous per sequence",
                    "tokens_per_step": wl.tokens(), "n_heads": wl.n_heads, "n_kv_heads": wl.n_kv_heads,
                    "head_dim": wl.head_dim, "causal": wl.causal, "causal_flops_per_step": flops_step,
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
@@ -412,6 +423,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--window", type=int, default=0, help="sliding window (0: none; the bench line counts only "
                                                              "the visible pairs)")
+    ap.add_argument("--paged", type=int, default=0, help="block size of a paged KV cache (0: contiguous cache)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=25.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--ref-rows", type=int, default=128, help="oracle rows per reference step")

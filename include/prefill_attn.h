@@ -129,6 +129,32 @@ typedef struct pa_options {
      * sees keys p - W + 1 .. p only.  KV tiles wholly outside every window of a
      * work unit are not read.  The cache still receives every new token. */
     int32_t window;
+    /* Paged KV cache (PagedAttention's block pool and per-request block table:
+     * "大模型推理优化：Prefill、Decode与KV Cache的工程实践" (zskr.cn) §4.2,
+     * "大语言模型推理核心：Prefill与Decode原理及工程优化" (yfxerp.com) §4.1, and
+     * the untitled compute-accounting page (zwxr.cn) §3.4).  block_table = NULL: the
+     * contiguous per-sequence cache described under prefill_attn_varlen.
+     * Otherwise cache_k and cache_v are pools of num_blocks blocks, each
+     * [n_kv_heads][block_size][head_dim] bf16 (the pool is [num_blocks,
+     * n_kv_heads, block_size, head_dim], row-major, 16-byte aligned), and
+     * block_table is a device array of int32 [num_seqs][max_blocks_per_seq]:
+     * position p of sequence b (prefix or new token) lives in row
+     * p % block_size of block block_table[b * max_blocks_per_seq + p / block_size].
+     * block_size is a power of two, 8 .. 4096; max_cache_len must equal
+     * max_blocks_per_seq * block_size; num_blocks * n_kv_heads < 2^31.  Blocks
+     * may be shared between sequences (a common prefix) as long as no two
+     * sequences of a call write the same row.  Only the entries for positions
+     * [0, cache_offsets[b] + seqlen_q[b]) are read; a sequence whose entry
+     * there is outside [0, num_blocks) is rejected on the device like other
+     * inconsistent metadata (PA_DEVERR_METADATA, nothing of it read or
+     * written).  The call may read the rows of a sequence's last prefix block
+     * past its prefix (their values never reach the result: any bit pattern,
+     * NaN included, is fine there). */
+    const int32_t *block_table;
+    int32_t block_size;
+    int32_t max_blocks_per_seq;
+    int32_t num_blocks;
+    int32_t reserved;  /* must be 0 */
 } pa_options;
 
 /*

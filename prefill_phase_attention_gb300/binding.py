@@ -22,7 +22,10 @@ DEVERR_METADATA, DEVERR_TIMEOUT, DEVERR_OVERFLOW = 0x1, 0x2, 0x4
 
 class PaOptions(ctypes.Structure):
     """pa_options of include/prefill_attn.h."""
-    _fields_ = [("struct_size", ctypes.c_uint32), ("window", ctypes.c_int32)]
+    _fields_ = [("struct_size", ctypes.c_uint32), ("window", ctypes.c_int32),
+                ("block_table", ctypes.c_void_p), ("block_size", ctypes.c_int32),
+                ("max_blocks_per_seq", ctypes.c_int32), ("num_blocks", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
 
 # Entry points declared in include/prefill_attn.h: name -> (restype, argtypes)
@@ -84,7 +87,7 @@ def _stream_handle(stream) -> int:
 
 
 def _varlen_args(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_k, cache_v, cache_offsets, out, lse,
-                 scale, causal, stream):
+                 scale, causal, stream, max_cache_len=None):
     for name, t, dt in (("q", q, torch.bfloat16), ("k", k, torch.bfloat16), ("v", v, torch.bfloat16),
                         ("cache_k", cache_k, torch.bfloat16), ("cache_v", cache_v, torch.bfloat16),
                         ("out", out, torch.bfloat16), ("cu_seqlens_q", cu_seqlens_q, torch.int32),
@@ -103,7 +106,8 @@ def _varlen_args(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_k, cache_v, cache_of
     return (q.data_ptr(), k.data_ptr(), v.data_ptr(), cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr(),
             cache_k.data_ptr(), cache_v.data_ptr(), cache_offsets.data_ptr(), out.data_ptr(),
             None if lse is None else lse.data_ptr(),
-            num_seqs, total_q, cache_k.shape[2], n_heads, n_kv_heads, head_dim,
+            num_seqs, total_q, cache_k.shape[2] if max_cache_len is None else max_cache_len,
+            n_heads, n_kv_heads, head_dim,
             float(scale), int(bool(causal)), _stream_handle(stream))
 
 
@@ -120,18 +124,38 @@ def prefill_attn_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_k, cache_v, c
     _check(load().prefill_attn_varlen(*args))
 
 
-def make_options(window: int = 0) -> PaOptions:
-    return PaOptions(ctypes.sizeof(PaOptions), int(window))
+def make_options(window: int = 0, block_table=None, block_size: int = 0, num_blocks: int = 0) -> PaOptions:
+    o = PaOptions()
+    o.struct_size = ctypes.sizeof(PaOptions)
+    o.window = int(window)
+    if block_table is not None:
+        o.block_table = block_table.data_ptr()
+        o.block_size = int(block_size)
+        o.max_blocks_per_seq = int(block_table.shape[1])
+        o.num_blocks = int(num_blocks)
+    return o
 
 
 def prefill_attn_varlen_ex(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_k, cache_v, cache_offsets, out, lse=None, *,
                            scale: Optional[float] = None, causal: bool = True, window: int = 0,
-                           stream=None) -> None:
-    """prefill_attn_varlen with options: `window` > 0 restricts each query to its
-    `window` most recent keys (causal only)."""
+                           block_table=None, stream=None) -> None:
+    """prefill_attn_varlen with options.
+
+    window > 0 restricts each query to its `window` most recent keys (causal only).
+    block_table (int32 CUDA [num_seqs, max_blocks_per_seq]) selects the paged cache:
+    cache_k/v are then block pools [num_blocks, n_kv_heads, block_size, head_dim]
+    and position p of sequence b lives in row p % block_size of block
+    block_table[b, p // block_size].
+    """
+    cap = None
+    if block_table is not None:
+        if block_table.dtype != torch.int32 or not block_table.is_cuda or not block_table.is_contiguous() \
+                or block_table.dim() != 2:
+            raise ValueError("block_table must be a contiguous 2-D CUDA int32 tensor")
+        cap = block_table.shape[1] * cache_k.shape[2]
     args = _varlen_args(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_k, cache_v, cache_offsets, out, lse,
-                        scale, causal, stream)
-    opts = make_options(window)
+                        scale, causal, stream, max_cache_len=cap)
+    opts = make_options(window, block_table, cache_k.shape[2], cache_k.shape[0])
     _check(load().prefill_attn_varlen_ex(*args[:-1], ctypes.byref(opts), args[-1]))
 
 

@@ -91,7 +91,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 pa_status check_args(const void* q, const void* k, const void* v, const int32_t* cu_q, const int32_t* cu_k,
                      const void* cache_k, const void* cache_v, const int32_t* off, const void* out,
                      const float* lse, int num_seqs, int total_q, int max_cache_len, int n_heads,
-                     int n_kv_heads, int head_dim, float scale, int causal) {
+                     int n_kv_heads, int head_dim, float scale, int causal, bool paged = false) {
     if (num_seqs < 0) return fail(PA_ERR_INVALID_ARG, "num_seqs must be >= 0 (got %d)", num_seqs);
     if (total_q < 0) return fail(PA_ERR_INVALID_ARG, "total_q must be >= 0 (got %d)", total_q);
     if (max_cache_len < 1) return fail(PA_ERR_INVALID_ARG, "max_cache_len must be >= 1 (got %d)", max_cache_len);
@@ -122,24 +122,58 @@ pa_status check_args(const void* q, const void* k, const void* v, const int32_t*
     // Row counts used by 32-bit kernel index arithmetic.
     if ((long long)total_q * n_heads >= (1LL << 31))
         return fail(PA_ERR_UNSUPPORTED, "total_q * n_heads must be < 2^31");
-    if ((long long)num_seqs * n_kv_heads * max_cache_len >= (1LL << 31))
+    if (!paged && (long long)num_seqs * n_kv_heads * max_cache_len >= (1LL << 31))
         return fail(PA_ERR_UNSUPPORTED, "num_seqs * n_kv_heads * max_cache_len must be < 2^31");
     return PA_OK;
 }
 
 struct Options {
     int window = 0;
+    const int32_t* block_table = nullptr;  // paged cache when set
+    int block_size = 0, max_blocks = 0, num_blocks = 0;
 };
 
 // Reads the caller's options; fields past the caller's struct_size count as zero.
 pa_status read_options(const pa_options* opts, int causal, Options* o) {
     *o = Options();
     if (!opts) return PA_OK;
-    if (opts->struct_size < offsetof(pa_options, window) + sizeof(int32_t))
+    const size_t have = opts->struct_size;
+    if (have < offsetof(pa_options, window) + sizeof(int32_t))
         return fail(PA_ERR_INVALID_ARG, "pa_options.struct_size %u is too small", (unsigned)opts->struct_size);
     o->window = opts->window;
     if (o->window < 0) return fail(PA_ERR_INVALID_ARG, "window must be >= 0 (got %d)", o->window);
     if (o->window > 0 && causal != 1) return fail(PA_ERR_INVALID_ARG, "a sliding window needs causal = 1");
+    if (have >= offsetof(pa_options, reserved) + sizeof(int32_t)) {
+        if (opts->reserved != 0) return fail(PA_ERR_INVALID_ARG, "pa_options.reserved must be 0");
+    }
+    if (have >= offsetof(pa_options, num_blocks) + sizeof(int32_t) && opts->block_table) {
+        o->block_table = opts->block_table;
+        o->block_size = opts->block_size;
+        o->max_blocks = opts->max_blocks_per_seq;
+        o->num_blocks = opts->num_blocks;
+        const int bs = o->block_size;
+        if (bs < 8 || bs > 4096 || (bs & (bs - 1)) != 0)
+            return fail(PA_ERR_UNSUPPORTED, "block_size must be a power of two in [8, 4096] (got %d)", bs);
+        if (o->max_blocks < 1 || o->num_blocks < 1)
+            return fail(PA_ERR_INVALID_ARG, "max_blocks_per_seq (%d) and num_blocks (%d) must be >= 1", o->max_blocks,
+                        o->num_blocks);
+        if (reinterpret_cast<uintptr_t>(o->block_table) & 3u)
+            return fail(PA_ERR_INVALID_ARG, "block_table must be 4-byte aligned");
+    } else if (have >= offsetof(pa_options, block_table) + sizeof(void*) && opts->block_table) {
+        return fail(PA_ERR_INVALID_ARG, "pa_options.struct_size %u does not cover the paged-cache fields",
+                    (unsigned)opts->struct_size);
+    }
+    return PA_OK;
+}
+
+// Checks that need both the options and the call's sizes.
+pa_status check_paged(const Options& o, int max_cache_len, int n_kv_heads) {
+    if (!o.block_table) return PA_OK;
+    if ((long long)o.max_blocks * o.block_size != max_cache_len)
+        return fail(PA_ERR_INVALID_ARG, "max_cache_len (%d) must equal max_blocks_per_seq (%d) * block_size (%d)",
+                    max_cache_len, o.max_blocks, o.block_size);
+    if ((long long)o.num_blocks * n_kv_heads >= (1LL << 31))
+        return fail(PA_ERR_UNSUPPORTED, "num_blocks * n_kv_heads must be < 2^31");
     return PA_OK;
 }
 
@@ -179,6 +213,10 @@ pa_status enqueue(const void* q, const void* k, const void* v, const int32_t* cu
     sa.causal = causal;
     sa.window = o.window;
     sa.max_units = scr.max_units;
+    sa.block_table = o.block_table;
+    sa.block_size = o.block_size;
+    sa.max_blocks = o.max_blocks;
+    sa.num_blocks = o.num_blocks;
     cudaError_t e = pa::launch_build_schedule(sa, stream);
     if (e != cudaSuccess) return cuda_fail(e, "schedule launch");
 
@@ -199,7 +237,13 @@ pa_status enqueue(const void* q, const void* k, const void* v, const int32_t* cu
     p.scale_log2 = scale * 1.4426950408889634f;
     p.causal = causal;
     p.window = o.window;
-    e = pa::encode_fwd_maps(p, q, total_q, num_seqs, head_dim);
+    p.block_table = o.block_table;
+    p.block_log2 = 0;
+    while (o.block_table && (1 << p.block_log2) < o.block_size) ++p.block_log2;
+    p.box_rows = std::min(o.block_size, pa::kBlockN);
+    p.max_blocks = o.max_blocks;
+    p.num_blocks = o.num_blocks;
+    e = pa::encode_fwd_maps(p, q, total_q, num_seqs, head_dim, o.num_blocks);
     if (e != cudaSuccess) return cuda_fail(e, "tensor map encoding");
     int sms = 0;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -253,7 +297,9 @@ pa_status prefill_attn_varlen_ex(const void* q, const void* k, const void* v, co
     pa_status s = read_options(opts, causal, &o);
     if (s != PA_OK) return s;
     s = check_args(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_k, cache_v, cache_offsets, out, lse, num_seqs,
-                   total_q, max_cache_len, n_heads, n_kv_heads, head_dim, scale, causal);
+                   total_q, max_cache_len, n_heads, n_kv_heads, head_dim, scale, causal, o.block_table != nullptr);
+    if (s != PA_OK) return s;
+    s = check_paged(o, max_cache_len, n_kv_heads);
     if (s != PA_OK) return s;
     if (num_seqs == 0 || total_q == 0) return PA_OK;
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);

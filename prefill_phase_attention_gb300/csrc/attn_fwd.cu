@@ -84,6 +84,7 @@ struct UnitSlot {
 struct __align__(8) Ctrl {
     uint64_t q_full, q_empty;
     uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
+    uint64_t v_fix[4];  // paged cache: last prefix V tile with the rows past P zeroed
     uint64_t s_full[kSlots], p_full[kSlots], pv_done[kSlots], o_empty[kSlots];
     uint64_t mma_drain;
     uint64_t unit_full[2], unit_empty[2];
@@ -161,9 +162,18 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 }
 
 // First key (absolute position in the sequence) of KV tile j of a unit whose
-// sequence has P cached tokens split into np = ceil(P / 128) prefix tiles.
+// sequence has P cached tokens split into np = ceil(P / 128) prefix tiles
+// (ending at P, or starting at 0 for a paged cache).
+template <bool kPaged>
 __device__ __forceinline__ int tile_key_base(int j, int P, int np) {
-    return j < np ? P - kBlockN * (np - j) : P + kBlockN * (j - np);
+    if (j >= np) return P + kBlockN * (j - np);
+    return kPaged ? kBlockN * j : P - kBlockN * (np - j);
+}
+
+// Paged cache: the last prefix tile when P is not a multiple of 128 -- its
+// rows from P on hold no prefix key (other tokens' entries, or stale data).
+__device__ __forceinline__ bool paged_tail_tile(int j, int P, int np) {
+    return j == np - 1 && (P & (kBlockN - 1)) != 0;
 }
 
 // The KV tiles a unit streams, [lo, lo + ntiles) in the sequence's tile
@@ -175,10 +185,11 @@ struct UnitGeo {
     int a[kSlots], b[kSlots];
 };
 
+template <bool kPaged>
 __device__ __forceinline__ UnitGeo unit_geo(const Unit& u, const SeqInfo& s, int tps, int causal, int window) {
     UnitGeo g;
     g.np = prefix_tiles(s.P);
-    const TileSpan all = query_tiles(s.n, s.P, u.q0, min(u.q0 + kSlots * tps, s.n), causal, window);
+    const TileSpan all = query_tiles(s.n, s.P, u.q0, min(u.q0 + kSlots * tps, s.n), causal, window, kPaged);
     g.lo = all.lo;
     g.ntiles = all.hi - all.lo;
 #pragma unroll
@@ -186,7 +197,7 @@ __device__ __forceinline__ UnitGeo unit_geo(const Unit& u, const SeqInfo& s, int
         const int qs = u.q0 + i * tps;
         g.a[i] = g.b[i] = 0;
         if (qs < s.n) {
-            const TileSpan t = query_tiles(s.n, s.P, qs, min(qs + tps, s.n), causal, window);
+            const TileSpan t = query_tiles(s.n, s.P, qs, min(qs + tps, s.n), causal, window, kPaged);
             g.a[i] = t.lo - g.lo;
             g.b[i] = t.hi - g.lo;
         }
@@ -211,7 +222,7 @@ __device__ __forceinline__ bool own_rows(int j, int np, int q0, int q_end, int& 
 // memory to consecutive cache rows starting at `dst` (one warp; 16-byte
 // granules, the warp's stores cover contiguous cache rows).
 template <int D>
-__device__ __forceinline__ void copy_tile_rows(const uint8_t* tile, __nv_bfloat16* dst, int lo_row, int nrows,
+__device__ __noinline__ void copy_tile_rows(const uint8_t* tile, __nv_bfloat16* dst, int lo_row, int nrows,
                                                int lane) {
     using C = Cfg<D>;
     constexpr int kGran = D / 8;  // 16-byte granules per row
@@ -227,7 +238,77 @@ __device__ __forceinline__ void copy_tile_rows(const uint8_t* tile, __nv_bfloat1
     }
 }
 
+// Paged cache: copies rows [lo_row, lo_row + nrows) of a staged tile to the
+// cache rows of positions pos0, pos0 + 1, ... of one sequence, each through the
+// sequence's block table (pool [num_blocks][Hk][block_size][D]).  The
+// scheduler has already rejected sequences naming a block outside the pool;
+// the range check here only keeps a stray id from turning into a stray store.
 template <int D>
+__device__ __noinline__ void copy_tile_rows_paged(const uint8_t* tile, __nv_bfloat16* pool, const int32_t* table,
+                                                     int block_log2, int num_blocks, int n_kv_heads, int kvh,
+                                                     int pos0, int lo_row, int nrows, int lane) {
+    using C = Cfg<D>;
+    constexpr int kGran = D / 8;
+    constexpr int kChunkGran = C::kChunkCols / 8;
+    const int total = nrows * kGran;
+    const int bmask = (1 << block_log2) - 1;
+#pragma unroll 4
+    for (int idx = lane; idx < total; idx += 32) {
+        const int ri = idx / kGran, g = idx % kGran;
+        const int r = lo_row + ri, pos = pos0 + ri;
+        const int c = g / kChunkGran, gg = g % kChunkGran;
+        const int phys = D >= 64 ? (gg ^ (r & 7)) : (gg ^ ((r >> 1) & 3));
+        const uint4 x = *reinterpret_cast<const uint4*>(tile + c * C::kChunkBytes + r * C::kRowBytes + phys * 16);
+        const int blk = __ldg(table + (pos >> block_log2));
+        if ((unsigned)blk >= (unsigned)num_blocks) continue;
+        const size_t row = (((size_t)blk * n_kv_heads + kvh) << block_log2) + (size_t)(pos & bmask);
+        *reinterpret_cast<uint4*>(pool + row * D + g * 8) = x;
+    }
+}
+
+// Zeroes rows [row0, 128) of a staged tile (whole rows, so the swizzle does
+// not matter).
+template <int D>
+__device__ __noinline__ void zero_tile_rows(uint8_t* tile, int row0, int lane) {
+    using C = Cfg<D>;
+    constexpr int kGran = D / 8;
+    constexpr int kChunkGran = C::kChunkCols / 8;
+    const int total = (kBlockN - row0) * kGran;
+    for (int idx = lane; idx < total; idx += 32) {
+        const int r = row0 + idx / kGran, g = idx % kGran;
+        *reinterpret_cast<uint4*>(tile + (g / kChunkGran) * C::kChunkBytes + r * C::kRowBytes + (g % kChunkGran) * 16) =
+            make_uint4(0, 0, 0, 0);
+    }
+}
+
+// Contiguous cache, one KV ring (K or V): waits for the stage, then
+// TMA-loads tile j (index in the sequence) of unit u from the cache (prefix
+// tiles) or from the new tokens' k/v.  Out of line: the K and the V loader
+// share one copy of this code, which keeps the kernel's hot code within the
+// instruction caches.
+template <int D>
+__device__ __noinline__ bool load_kv_tile(const FwdParams& p, Ctrl* ctl, WorkspaceHeader* hdr, uint8_t* ring,
+                                          int stages, uint64_t* full, uint64_t* empty, const CUtensorMap* tm_cache,
+                                          const CUtensorMap* tm_new, int* last_parity, uint32_t t, int j,
+                                          const Unit& u, const SeqInfo& s, int np) {
+    using C = Cfg<D>;
+    const int st = t % stages;
+    const uint32_t ph = (t / stages) & 1;
+    const int kb = tile_key_base<false>(j, s.P, np);
+    if (!wait_bar(&empty[st], ph ^ 1, ctl, hdr)) return false;
+    mbar_arrive_expect_tx(&full[st], C::kTileBytes);
+    for (int c = 0; c < C::kChunks; ++c) {
+        uint8_t* dst = ring + st * C::kTileBytes + c * C::kChunkBytes;
+        if (j < np)
+            tma_load_3d(dst, tm_cache, &full[st], c * C::kChunkCols, kb, u.b * p.n_kv_heads + u.kvh);
+        else
+            tma_load_3d(dst, tm_new, &full[st], c * C::kChunkCols, u.kvh, s.q_start + kb - s.P);
+    }
+    last_parity[st] = (int)ph;
+    return true;
+}
+
+template <int D, bool kPaged>
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ FwdParams p) {
     using C = Cfg<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -256,6 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         for (int s = 0; s < C::kStagesV; ++s) {
             mbar_init(&ctl->v_full[s], 1);
             mbar_init(&ctl->v_empty[s], 2);
+            mbar_init(&ctl->v_fix[s], 1);  // V cache writer
         }
         for (int i = 0; i < kSlots; ++i) {
             mbar_init(&ctl->s_full[i], 1);
@@ -285,26 +367,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     tc_fence_after();
     const uint32_t tmem = ctl->tmem_base;
 
-    // One KV ring (K or V): waits for the stage, then TMA-loads tile j of the
-    // unit from the cache (prefix tiles) or from the new tokens' k/v.
-    auto load_kv_tile = [&](uint8_t* ring, int stages, uint64_t* full, uint64_t* empty, const CUtensorMap* tm_cache,
-                            const CUtensorMap* tm_new, int* last_parity, uint32_t t, int j, const Unit& u,
-                            const SeqInfo& s, int np) -> bool {  // j: tile index in the sequence
-        const int st = t % stages;
-        const uint32_t ph = (t / stages) & 1;
-        if (!wait_bar(&empty[st], ph ^ 1, ctl, hdr)) return false;
-        const int kb = tile_key_base(j, s.P, np);
-        mbar_arrive_expect_tx(&full[st], C::kTileBytes);
-        for (int c = 0; c < C::kChunks; ++c) {
-            uint8_t* dst = ring + st * C::kTileBytes + c * C::kChunkBytes;
-            if (j < np)
-                tma_load_3d(dst, tm_cache, &full[st], c * C::kChunkCols, kb, u.b * p.n_kv_heads + u.kvh);
-            else
-                tma_load_3d(dst, tm_new, &full[st], c * C::kChunkCols, u.kvh, s.q_start + kb - s.P);
-        }
-        last_parity[st] = (int)ph;
-        return true;
-    };
     // On abort, let every copy a producer thread started land before the CTA exits.
     auto drain = [&](uint64_t* bars, const int* last_parity, int n) {
         const uint64_t t0 = globaltimer_ns();
@@ -315,7 +377,131 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         }
     };
 
-    if (warp == 0) {
+    if (kPaged && warp == 0) {
+        // ------------------------------------- paged cache: unit fetch, Q, K and V loads
+        // Lanes 0-15 load K (lane 0 also fetches units and loads Q), lanes
+        // 16-31 load V.  A prefix tile is one TMA box per (cache block,
+        // 64-column chunk): lane l of a group issues boxes l and l + 16, so a
+        // tile of 16-token blocks costs each lane one or two TMA issues, and
+        // each lane loads the block ids of its boxes one tile ahead.
+        const bool is_v = lane >= 16;
+        const int gl = lane & 15;
+        const unsigned gmask = is_v ? 0xFFFF0000u : 0x0000FFFFu;
+        const int src = lane & 16;  // the group's leader lane
+        const bool gleader = gl == 0;
+        uint8_t* ring = is_v ? v_smem : k_smem;
+        const int stages = is_v ? C::kStagesV : C::kStagesK;
+        uint64_t* full = is_v ? ctl->v_full : ctl->k_full;
+        uint64_t* empty = is_v ? ctl->v_empty : ctl->k_empty;
+        const CUtensorMap* tm_cache = is_v ? &p.tm_cv : &p.tm_ck;
+        const CUtensorMap* tm_new = is_v ? &p.tm_v : &p.tm_k;
+        const int num_units = hdr->num_units;
+        const int br = p.box_rows;
+        const int bmask = (1 << p.block_log2) - 1;
+        int last_parity[4] = {-1, -1, -1, -1};
+        int last_q_parity = -1;
+        uint32_t t = 0;
+        for (int u_it = 0;; ++u_it) {
+            const int sl = u_it & 1;
+            bool ok = true;
+            if (!is_v) {
+                if (gleader) {
+                    ok = wait_bar(&ctl->unit_empty[sl], ((u_it >> 1) & 1) ^ 1, ctl, hdr);
+                    if (ok) {
+                        const int idx = atomicAdd(&hdr->counter, 1);
+                        UnitSlot us;
+                        if (idx < num_units) {
+                            us.u = p.units[idx];
+                            us.s = p.seqs[us.u.b];
+                        } else {
+                            us.u.b = -1;
+                        }
+                        ctl->slot[sl] = us;
+                        mbar_arrive(&ctl->unit_full[sl]);
+                    }
+                }
+                ok = __shfl_sync(gmask, ok, src);
+            } else {
+                ok = gleader ? wait_bar(&ctl->unit_full[sl], (u_it >> 1) & 1, ctl, hdr) : true;
+                ok = __shfl_sync(gmask, ok, src);
+            }
+            if (!ok) break;
+            __syncwarp(gmask);  // the slot written by lane 0 (K) / acquired by lane 16 (V) is visible
+            const Unit u = ctl->slot[sl].u;
+            const SeqInfo s = ctl->slot[sl].s;
+            __syncwarp(gmask);
+            if (is_v && gleader) mbar_arrive(&ctl->unit_empty[sl]);
+            if (u.b < 0) break;
+            if (!is_v && gleader) {
+                // both Q tiles: rows (token, head-in-group) of each slot
+                ok = wait_bar(&ctl->q_empty, (u_it & 1) ^ 1, ctl, hdr);
+                if (ok) {
+                    const int nq = u.q0 + tps < s.n ? 2 : 1;
+                    mbar_arrive_expect_tx(&ctl->q_full, nq * G * tps * C::kRowBytes * C::kChunks);
+                    for (int i = 0; i < nq; ++i)
+                        for (int c = 0; c < C::kChunks; ++c)
+                            tma_load_3d(q_smem + i * C::kTileBytes + c * C::kChunkBytes, &p.tm_q, &ctl->q_full,
+                                        c * C::kChunkCols, u.kvh * G, s.q_start + u.q0 + i * tps);
+                    last_q_parity = u_it & 1;
+                }
+            }
+            if (!is_v && !__shfl_sync(gmask, ok, src)) break;
+            const UnitGeo ug = unit_geo<true>(u, s, tps, p.causal, p.window);
+            const int32_t* tab = p.block_table + (size_t)u.b * p.max_blocks;
+            // this lane's boxes of tile jj: box (pair / kChunks), chunk (pair % kChunks)
+            // for pair = gl and gl + 16; returns the block id of each (prefix tiles)
+            auto fetch_ids = [&](int jj, int& id0, int& id1) {
+                id0 = id1 = 0;
+                if (jj < ug.np) {
+                    const int kb = kBlockN * jj;
+                    const int boxes = (min(kBlockN, s.P - kb) + br - 1) / br;
+                    const int b0 = gl / C::kChunks, b1 = (gl + 16) / C::kChunks;
+                    if (b0 < boxes) id0 = __ldg(tab + ((kb + b0 * br) >> p.block_log2));
+                    if (b1 < boxes) id1 = __ldg(tab + ((kb + b1 * br) >> p.block_log2));
+                }
+            };
+            int id0, id1, nid0 = 0, nid1 = 0;
+            fetch_ids(ug.lo, id0, id1);
+            for (int j = 0; j < ug.ntiles; ++j, ++t) {
+                const int jj = ug.lo + j;
+                if (j + 1 < ug.ntiles) fetch_ids(jj + 1, nid0, nid1);  // in flight during this tile
+                const int st = t % stages;
+                const uint32_t ph = (t / stages) & 1;
+                ok = gleader ? wait_bar(&empty[st], ph ^ 1, ctl, hdr) : true;
+                if (!__shfl_sync(gmask, ok, src)) { ok = false; break; }
+                const int kb = tile_key_base<true>(jj, s.P, ug.np);
+                uint8_t* stage = ring + st * C::kTileBytes;
+                if (jj < ug.np) {
+                    const int boxes = (min(kBlockN, s.P - kb) + br - 1) / br;
+                    if (gleader) mbar_arrive_expect_tx(&full[st], boxes * br * C::kRowBytes * C::kChunks);
+                    __syncwarp(gmask);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int pair = gl + 16 * h;
+                        const int box = pair / C::kChunks, c = pair % C::kChunks;
+                        if (box < boxes)
+                            tma_load_3d(stage + c * C::kChunkBytes + box * br * C::kRowBytes, tm_cache, &full[st],
+                                        c * C::kChunkCols, (kb + box * br) & bmask,
+                                        (h ? id1 : id0) * p.n_kv_heads + u.kvh);
+                    }
+                } else {
+                    if (gleader) mbar_arrive_expect_tx(&full[st], C::kTileBytes);
+                    __syncwarp(gmask);
+                    if (gl < C::kChunks)
+                        tma_load_3d(stage + gl * C::kChunkBytes, tm_new, &full[st], gl * C::kChunkCols, u.kvh,
+                                    s.q_start + kb - s.P);
+                }
+                last_parity[st] = (int)ph;
+                id0 = nid0;
+                id1 = nid1;
+            }
+            if (!ok) break;
+        }
+        if (gleader && aborted(ctl)) {
+            if (!is_v) drain(&ctl->q_full, &last_q_parity, 1);
+            drain(full, last_parity, stages);
+        }
+    } else if (warp == 0) {
         if (lane == 0) {
             // ----------------------------------------- unit fetch, Q and K loads
             const int num_units = hdr->num_units;
@@ -347,11 +533,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                         tma_load_3d(q_smem + i * C::kTileBytes + c * C::kChunkBytes, &p.tm_q, &ctl->q_full,
                                     c * C::kChunkCols, u.kvh * G, s.q_start + u.q0 + i * tps);
                 last_q_parity[0] = u_it & 1;
-                const UnitGeo ug = unit_geo(u, s, tps, p.causal, p.window);
+                const UnitGeo ug = unit_geo<kPaged>(u, s, tps, p.causal, p.window);
                 bool ok = true;
                 for (int j = 0; j < ug.ntiles && ok; ++j, ++t)
-                    ok = load_kv_tile(k_smem, C::kStagesK, ctl->k_full, ctl->k_empty, &p.tm_ck, &p.tm_k,
-                                      last_k_parity, t, ug.lo + j, u, s, ug.np);
+                    ok = load_kv_tile<D>(p, ctl, hdr, k_smem, C::kStagesK, ctl->k_full, ctl->k_empty, &p.tm_ck,
+                                                 &p.tm_k, last_k_parity, t, ug.lo + j, u, s, ug.np);
                 if (!ok) break;
             }
             if (aborted(ctl)) {
@@ -369,11 +555,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 const UnitSlot us = ctl->slot[sl];
                 mbar_arrive(&ctl->unit_empty[sl]);
                 if (us.u.b < 0) break;
-                const UnitGeo ug = unit_geo(us.u, us.s, tps, p.causal, p.window);
+                const UnitGeo ug = unit_geo<kPaged>(us.u, us.s, tps, p.causal, p.window);
                 bool ok = true;
                 for (int j = 0; j < ug.ntiles && ok; ++j, ++t)
-                    ok = load_kv_tile(v_smem, C::kStagesV, ctl->v_full, ctl->v_empty, &p.tm_cv, &p.tm_v,
-                                      last_v_parity, t, ug.lo + j, us.u, us.s, ug.np);
+                    ok = load_kv_tile<D>(p, ctl, hdr, v_smem, C::kStagesV, ctl->v_full, ctl->v_empty, &p.tm_cv,
+                                                 &p.tm_v, last_v_parity, t, ug.lo + j, us.u, us.s, ug.np);
                 if (!ok) break;
             }
             if (aborted(ctl)) drain(ctl->v_full, last_v_parity, C::kStagesV);
@@ -394,6 +580,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         uint32_t t = 0;                // KV tiles of this CTA so far
         uint32_t ns[kSlots] = {0, 0};  // tiles processed per slot so far
         uint32_t no[kSlots] = {0, 0};  // units with the slot active so far
+        uint32_t fixpar = 0;           // paged: parity bit per V stage of v_fix
         bool ok = true;
         auto issue_s = [&](int i, uint32_t tt) {
             if (leader) {
@@ -432,7 +619,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             __syncwarp();
             if (leader) mbar_arrive(&ctl->unit_empty[sl]);
             if (u.b < 0) break;
-            const UnitGeo ug = unit_geo(u, s, tps, p.causal, p.window);
+            const UnitGeo ug = unit_geo<kPaged>(u, s, tps, p.causal, p.window);
             const int ntiles = ug.ntiles;
             if (!warp_wait(&ctl->q_full, u_it & 1, ctl, hdr)) break;
             // prologue: S of tile 0 for the slots that start there
@@ -451,7 +638,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                         if (!warp_wait(&ctl->p_full[i], (ns[i] + j - ug.a[i]) & 1, ctl, hdr)) { ok = false; break; }
                         if (j == ug.a[i] && !warp_wait(&ctl->o_empty[i], (no[i] & 1) ^ 1, ctl, hdr)) { ok = false; break; }
                         if (!v_ready) {
-                            if (!warp_wait(&ctl->v_full[tj % C::kStagesV], (tj / C::kStagesV) & 1, ctl, hdr)) {
+                            const int vst = tj % C::kStagesV;
+                            bool got;
+                            if (kPaged && paged_tail_tile(ug.lo + j, s.P, ug.np)) {
+                                got = warp_wait(&ctl->v_fix[vst], (fixpar >> vst) & 1, ctl, hdr);
+                                fixpar ^= 1u << vst;
+                            } else {
+                                got = warp_wait(&ctl->v_full[vst], (tj / C::kStagesV) & 1, ctl, hdr);
+                            }
+                            if (!got) {
                                 ok = false;
                                 break;
                             }
@@ -516,7 +711,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             __syncwarp();
             if (lane == 0) mbar_arrive(&ctl->unit_empty[sl]);
             if (us.u.b < 0) break;
-            const UnitGeo ug = unit_geo(us.u, us.s, tps, p.causal, p.window);
+            const UnitGeo ug = unit_geo<kPaged>(us.u, us.s, tps, p.causal, p.window);
             const int np = ug.np;
             const int q_end = min(us.u.q0 + kSlots * tps, us.s.n);
             bool ok = true;
@@ -527,9 +722,22 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 int lo_row, nrows;
                 if (own_rows(j, np, us.u.q0, q_end, lo_row, nrows)) {
                     const int first_tok = (j - np) * kBlockN + lo_row;  // token index within the sequence
-                    __nv_bfloat16* dst = cache + (((size_t)us.u.b * p.n_kv_heads + us.u.kvh) * p.max_cache_len +
-                                                  us.s.P + first_tok) * D;
-                    copy_tile_rows<D>(ring + st * C::kTileBytes, dst, lo_row, nrows, lane);
+                    if (kPaged) {
+                        copy_tile_rows_paged<D>(ring + st * C::kTileBytes, cache,
+                                                p.block_table + (size_t)us.u.b * p.max_blocks, p.block_log2,
+                                                p.num_blocks, p.n_kv_heads, us.u.kvh, us.s.P + first_tok, lo_row, nrows, lane);
+                    } else {
+                        __nv_bfloat16* dst = cache + (((size_t)us.u.b * p.n_kv_heads + us.u.kvh) * p.max_cache_len +
+                                                      us.s.P + first_tok) * D;
+                        copy_tile_rows<D>(ring + st * C::kTileBytes, dst, lo_row, nrows, lane);
+                    }
+                } else if (kPaged && !is_k && paged_tail_tile(j, us.s.P, np)) {
+                    // rows from P on may hold anything (NaN included): zero them
+                    // so that P = 0 there contributes exactly 0 to O
+                    zero_tile_rows<D>(ring + st * C::kTileBytes, us.s.P - kBlockN * j, lane);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&ctl->v_fix[st]);
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[st]);
@@ -557,7 +765,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             if (us.u.b < 0) break;
             const Unit u = us.u;
             const SeqInfo s = us.s;
-            const UnitGeo ug = unit_geo(u, s, tps, p.causal, p.window);
+            const UnitGeo ug = unit_geo<kPaged>(u, s, tps, p.causal, p.window);
             const int nt = ug.b[slot] - ug.a[slot];
             if (nt == 0) continue;
             const int qs = u.q0 + slot * tps;
@@ -599,9 +807,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                         sv[96 + i] = __uint_as_float(r3[i]);
                     }
                 }
-                const int kb = tile_key_base(ug.lo + ug.a[slot] + j, s.P, np);
-                if (kb < 0 || kb + kBlockN > slot_hi || kb < slot_lo) {
-                    const int lo = max(-kb, row_lo - kb), hi = row_hi - kb;
+                const int jt = ug.lo + ug.a[slot] + j;  // tile index in the sequence
+                const int kb = tile_key_base<kPaged>(jt, s.P, np);
+                // paged: the last prefix tile holds prefix keys only below P
+                const bool tail = kPaged && jt < np && kb + kBlockN > s.P;
+                if (kb < 0 || kb + kBlockN > slot_hi || kb < slot_lo || tail) {
+                    const int lo = max(-kb, row_lo - kb), hi = (tail ? min(row_hi, s.P) : row_hi) - kb;
 #pragma unroll
                     for (int c = 0; c < kBlockN; ++c)
                         if (c < lo || c >= hi) sv[c] = -INFINITY;
@@ -730,7 +941,7 @@ cudaError_t encode3d(CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, 
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int D>
+template <int D, bool kPaged>
 cudaError_t launch_d(const FwdParams& p, int grid, cudaStream_t st) {
     constexpr int kSmem = smem_bytes<D>();
     static_assert(kSmem <= 232448, "shared memory budget");
@@ -738,17 +949,18 @@ cudaError_t launch_d(const FwdParams& p, int grid, cudaStream_t st) {
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 64 && !configured_for[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+        cudaError_t e =
+            cudaFuncSetAttribute(attn_fwd_kernel<D, kPaged>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
         if (e != cudaSuccess) return e;
         configured_for[dev] = 1;
     }
-    attn_fwd_kernel<D><<<grid, kThreads, kSmem, st>>>(p);
+    attn_fwd_kernel<D, kPaged><<<grid, kThreads, kSmem, st>>>(p);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t encode_fwd_maps(FwdParams& p, const void* q, int total_q, int num_seqs, int head_dim) {
+cudaError_t encode_fwd_maps(FwdParams& p, const void* q, int total_q, int num_seqs, int head_dim, int num_blocks) {
     const uint32_t cc = head_dim >= 64 ? 64 : 32;
     const CUtensorMapSwizzle sw = head_dim >= 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
     const uint64_t D = head_dim, H = p.n_heads, Hk = p.n_kv_heads, T = total_q, cap = p.max_cache_len;
@@ -760,6 +972,15 @@ cudaError_t encode_fwd_maps(FwdParams& p, const void* q, int total_q, int num_se
     if (e != cudaSuccess) return e;
     e = encode3d(&p.tm_v, p.v, D, Hk, T, D * 2, Hk * D * 2, cc, 1, kBlockN, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
     if (e != cudaSuccess) return e;
+    if (p.block_table) {
+        // pool [num_blocks, Hk, bs, D] viewed (D, bs, num_blocks * Hk)
+        const uint64_t bs = 1ull << p.block_log2, Z = (uint64_t)num_blocks * Hk;
+        e = encode3d(&p.tm_ck, p.cache_k, D, bs, Z, D * 2, bs * D * 2, cc, p.box_rows, 1, sw,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+        if (e != cudaSuccess) return e;
+        return encode3d(&p.tm_cv, p.cache_v, D, bs, Z, D * 2, bs * D * 2, cc, p.box_rows, 1, sw,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+    }
     e = encode3d(&p.tm_ck, p.cache_k, D, cap, (uint64_t)num_seqs * Hk, D * 2, cap * D * 2, cc, kBlockN, 1, sw,
                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
     if (e != cudaSuccess) return e;
@@ -768,10 +989,11 @@ cudaError_t encode_fwd_maps(FwdParams& p, const void* q, int total_q, int num_se
 }
 
 cudaError_t launch_attn_fwd(const FwdParams& p, int head_dim, int grid, cudaStream_t st) {
+    const bool paged = p.block_table != nullptr;
     switch (head_dim) {
-        case 32: return launch_d<32>(p, grid, st);
-        case 64: return launch_d<64>(p, grid, st);
-        case 128: return launch_d<128>(p, grid, st);
+        case 32: return paged ? launch_d<32, true>(p, grid, st) : launch_d<32, false>(p, grid, st);
+        case 64: return paged ? launch_d<64, true>(p, grid, st) : launch_d<64, false>(p, grid, st);
+        case 128: return paged ? launch_d<128, true>(p, grid, st) : launch_d<128, false>(p, grid, st);
         default: return cudaErrorInvalidValue;
     }
 }

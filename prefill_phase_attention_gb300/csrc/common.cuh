@@ -57,19 +57,27 @@ struct ScheduleArgs {
     int causal;
     int window;     // sliding window (0: none)
     int max_units;  // capacity of the unit list
+    // paged cache (block_table == nullptr: contiguous slots)
+    const int32_t* block_table;  // [num_seqs][max_blocks]
+    int block_size, max_blocks, num_blocks;
 };
 
-// KV tiles of a sequence with P cached tokens: the prefix [0, P) is cut into
-// tiles that END at P (the first one may start below 0 and is masked there),
-// and the new keys [P, P + n) into tiles that START at P, so no tile ever
-// reads cache entries at or past P.  Tile j < np = ceil(P / 128) covers keys
-// [P - 128 (np - j), ...), tile j >= np covers [P + 128 (j - np), ...).
+// KV tiles of a sequence with P cached tokens.  The new keys [P, P + n) are
+// cut into tiles that START at P: tile j >= np = ceil(P / 128) covers keys
+// [P + 128 (j - np), ...).  The prefix [0, P) is cut into np tiles that
+//  - contiguous cache: END at P (tile j covers [P - 128 (np - j), ...); the
+//    first may start below 0 and is masked there), so no tile ever reads
+//    cache entries at or past P;
+//  - paged cache: START at 0 (tile j covers [128 j, 128 j + 128)), so every
+//    tile is a whole number of cache blocks (or a block-aligned part of one);
+//    the last one is masked from P on.
 __host__ __device__ inline int prefix_tiles(int P) { return (P + kBlockN - 1) / kBlockN; }
 
 // Tile holding key position `key` (0 <= key < P + n).
-__host__ __device__ inline int key_tile(int key, int P) {
+__host__ __device__ inline int key_tile(int key, int P, bool paged) {
     const int np = prefix_tiles(P);
-    return key < P ? np - (P - key + kBlockN - 1) / kBlockN : np + (key - P) / kBlockN;
+    if (key >= P) return np + (key - P) / kBlockN;
+    return paged ? key / kBlockN : np - (P - key + kBlockN - 1) / kBlockN;
 }
 
 struct TileSpan {
@@ -79,19 +87,21 @@ struct TileSpan {
 // Tiles holding the keys that query tokens [qs, qe) (0 <= qs < qe <= n) see:
 // causal -> keys up to P + qe - 1, from P + qs - window + 1 when window > 0;
 // not causal -> all P + n keys.
-__host__ __device__ inline TileSpan query_tiles(int n, int P, int qs, int qe, int causal, int window) {
+__host__ __device__ inline TileSpan query_tiles(int n, int P, int qs, int qe, int causal, int window, bool paged) {
     int klo = 0;
     if (causal && window > 0 && P + qs - window + 1 > 0) klo = P + qs - window + 1;
     const int khi = causal ? P + qe : P + n;  // exclusive
     TileSpan t;
-    t.lo = key_tile(klo, P);
-    t.hi = key_tile(khi - 1, P) + 1;
+    t.lo = key_tile(klo, P, paged);
+    t.hi = key_tile(khi - 1, P, paged) + 1;
     return t;
 }
 
 // KV tiles a work unit streams (its cost): tokens [q0, min(q0 + tokens, n)).
-__host__ __device__ inline int unit_tiles(int n, int P, int q0, int tokens_per_unit, int causal, int window) {
-    const TileSpan t = query_tiles(n, P, q0, (q0 + tokens_per_unit < n) ? q0 + tokens_per_unit : n, causal, window);
+__host__ __device__ inline int unit_tiles(int n, int P, int q0, int tokens_per_unit, int causal, int window,
+                                          bool paged) {
+    const TileSpan t =
+        query_tiles(n, P, q0, (q0 + tokens_per_unit < n) ? q0 + tokens_per_unit : n, causal, window, paged);
     return t.hi - t.lo;
 }
 

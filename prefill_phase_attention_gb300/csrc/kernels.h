@@ -24,7 +24,8 @@ struct FwdParams {
     CUtensorMap tm_q;        // q  [T, H, D]      viewed (D, H, T),        box (C, G, 128/G)
     CUtensorMap tm_k;        // k  [T, Hk, D]     viewed (D, Hk, T),       box (C, 1, 128)
     CUtensorMap tm_v;        // v  same as k
-    CUtensorMap tm_ck;       // cache_k [B, Hk, cap, D] viewed (D, cap, B*Hk), box (C, 128, 1)
+    CUtensorMap tm_ck;       // cache_k [B, Hk, cap, D] viewed (D, cap, B*Hk), box (C, 128, 1); paged:
+                             // pool [NB, Hk, bs, D] viewed (D, bs, NB*Hk), box (C, min(bs, 128), 1)
     CUtensorMap tm_cv;       // cache_v same
     const __nv_bfloat16* k;  // raw pointers for the cache copy
     const __nv_bfloat16* v;
@@ -39,10 +40,17 @@ struct FwdParams {
     float scale_log2;        // scale * log2(e)
     int causal;
     int window;              // sliding window (0: none)
+    // paged cache (block_table == nullptr: contiguous [B, Hk, cap, D] slots)
+    const int32_t* block_table;  // [B][max_blocks]
+    int block_log2;              // block_size = 1 << block_log2 (>= 8)
+    int box_rows;                // min(block_size, 128): rows of one cache TMA box
+    int max_blocks;
+    int num_blocks;
 };
 
 // Encodes the tensor maps of `p` (the pointer fields and sizes must be set).
-cudaError_t encode_fwd_maps(FwdParams& p, const void* q, int total_q, int num_seqs, int head_dim);
+// num_blocks: blocks in the pool when p.block_table is set (else unused).
+cudaError_t encode_fwd_maps(FwdParams& p, const void* q, int total_q, int num_seqs, int head_dim, int num_blocks);
 cudaError_t launch_attn_fwd(const FwdParams& p, int head_dim, int grid, cudaStream_t st);
 
 }  // namespace pa

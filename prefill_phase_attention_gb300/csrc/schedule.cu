@@ -62,12 +62,33 @@ __device__ __forceinline__ int block_owner(const SeqInfo* seqs, int num_seqs, in
 __global__ void __launch_bounds__(1024) build_schedule_kernel(ScheduleArgs a) {
     __shared__ int hist[kCostBins];
     __shared__ int warp_sums[32];
-    __shared__ int s_total;
     const int tid = threadIdx.x;
     const int nthr = blockDim.x;
     const int tpu = kSlots * (kBlockM / a.group);  // query tokens per unit
 
     for (int i = tid; i < kCostBins; i += nthr) hist[i] = 0;
+
+    // Paged cache: every block a sequence touches (positions [0, P + n)) must be
+    // a block of the pool; a sequence that names another is rejected below.
+    // One warp per sequence; the verdict waits in SeqInfo::pad until pass 1.
+    const bool paged = a.block_table != nullptr;
+    if (paged) {
+        const int lane = tid & 31, nwarps = nthr >> 5;
+        for (int b = tid >> 5; b < a.num_seqs; b += nwarps) {
+            const long long lk = (long long)a.cu_seqlens_k[b + 1] - a.cu_seqlens_k[b];
+            const long long used = lk > 0 ? (lk + a.block_size - 1) / a.block_size : 0;
+            const int nb = used < a.max_blocks ? (int)used : a.max_blocks;
+            bool bad = false;
+            for (int L = lane; L < nb; L += 32) {
+                const int blk = a.block_table[(size_t)b * a.max_blocks + L];
+                bad |= blk < 0 || blk >= a.num_blocks;
+            }
+            bad = __any_sync(0xffffffffu, bad);
+            if (lane == 0) a.seqs[b].pad = bad ? 1 : 0;
+        }
+        __threadfence_block();
+        __syncthreads();
+    }
 
     // Pass 1: sanitise each sequence; number its query blocks (first block
     // index of b goes to SeqInfo::pad) with a block-wide scan per 1024 sequences.
@@ -83,7 +104,7 @@ __global__ void __launch_bounds__(1024) build_schedule_kernel(ScheduleArgs a) {
             const long long n = (long long)q_end - q_start;
             const bool ok = q_start >= 0 && n >= 0 && (long long)q_end <= a.total_q && P >= 0 &&
                             (long long)lk == (long long)P + n && (long long)P + n <= a.max_cache_len &&
-                            (b > 0 || q_start == 0);
+                            (b > 0 || q_start == 0) && !(paged && a.seqs[b].pad != 0);
             if (!ok) atomicOr(&a.hdr->error, PA_DEVERR_METADATA);
             si.q_start = ok ? q_start : 0;
             si.n = ok ? (int)n : 0;
@@ -105,7 +126,7 @@ __global__ void __launch_bounds__(1024) build_schedule_kernel(ScheduleArgs a) {
         const int b = block_owner(a.seqs, a.num_seqs, i);
         const SeqInfo si = a.seqs[b];
         const int q0 = (i - si.pad) * tpu;
-        atomicAdd(&hist[clamp_bin(unit_tiles(si.n, si.P, q0, tpu, a.causal, a.window))], a.n_kv_heads);
+        atomicAdd(&hist[clamp_bin(unit_tiles(si.n, si.P, q0, tpu, a.causal, a.window, paged))], a.n_kv_heads);
     }
     __syncthreads();
 
@@ -131,7 +152,7 @@ __global__ void __launch_bounds__(1024) build_schedule_kernel(ScheduleArgs a) {
         const int b = block_owner(a.seqs, a.num_seqs, i);
         const SeqInfo si = a.seqs[b];
         const int q0 = (i - si.pad) * tpu;
-        const int cost = unit_tiles(si.n, si.P, q0, tpu, a.causal, a.window);
+        const int cost = unit_tiles(si.n, si.P, q0, tpu, a.causal, a.window, paged);
         const int base = atomicAdd(&hist[clamp_bin(cost)], a.n_kv_heads);
         for (int kvh = 0; kvh < a.n_kv_heads; ++kvh) {
             const int pos = base + kvh;

@@ -43,16 +43,17 @@ class Guarded:
         return bool((g == GUARD_F32).all())
 
 
-def run_step_gpu(wl, inp, cache_k_dev, cache_v_dev, guarded=True, window=0):
-    """One launch on the GPU; returns (out, lse) CUDA tensors (and checks guards)."""
+def run_step_gpu(wl, inp, cache_k_dev, cache_v_dev, guarded=True, window=0, block_table=None):
+    """One launch on the GPU; returns (out, lse) CUDA tensors (and checks guards).
+    block_table (CUDA int32) selects the paged cache: the caches are then pools."""
     dev = {k: v.cuda() for k, v in inp.items()}
     T = inp["q"].shape[0]
     out = Guarded((T, wl.n_heads, wl.head_dim), torch.bfloat16)
     lse = Guarded((T, wl.n_heads), torch.float32)
-    if window:
+    if window or block_table is not None:
         binding.prefill_attn_varlen_ex(dev["q"], dev["k"], dev["v"], dev["cu_seqlens_q"], dev["cu_seqlens_k"],
                                        cache_k_dev, cache_v_dev, dev["cache_offsets"], out.t, lse.t,
-                                       scale=wl.scale, causal=wl.causal, window=window)
+                                       scale=wl.scale, causal=wl.causal, window=window, block_table=block_table)
     else:
         binding.prefill_attn_varlen(dev["q"], dev["k"], dev["v"], dev["cu_seqlens_q"], dev["cu_seqlens_k"],
                                     cache_k_dev, cache_v_dev, dev["cache_offsets"], out.t, lse.t,
@@ -64,13 +65,19 @@ def run_step_gpu(wl, inp, cache_k_dev, cache_v_dev, guarded=True, window=0):
     return out.t, lse.t
 
 
-def oracle_step(wl, inp, cache_k_bits, cache_v_bits, rows=None, want_cache=True, window=0):
+def oracle_step(wl, inp, cache_k_bits, cache_v_bits, rows=None, want_cache=True, window=0, block_table=None):
+    """The oracle on the same inputs; block_table (CPU int32 [B, max_blocks]) = paged pools."""
+    cap, bs = wl.max_cache_len, 0
+    if block_table is not None:
+        bs = cache_k_bits.shape[2]
+        cap = block_table.shape[1] * bs
+        block_table = np.ascontiguousarray(block_table, np.int32)
     return oracle.prefill_attention(
         W.bf16_bits(inp["q"]), W.bf16_bits(inp["k"]), W.bf16_bits(inp["v"]),
         inp["cu_seqlens_q"].numpy(), inp["cu_seqlens_k"].numpy(), inp["cache_offsets"].numpy(),
         cache_k_bits, cache_v_bits, n_heads=wl.n_heads, n_kv_heads=wl.n_kv_heads, head_dim=wl.head_dim,
-        max_cache_len=wl.max_cache_len, scale=wl.scale, causal=wl.causal, window=window, rows=rows,
-        want_cache=want_cache)
+        max_cache_len=cap, scale=wl.scale, causal=wl.causal, window=window, rows=rows,
+        want_cache=want_cache, block_table=block_table, block_size=bs)
 
 
 def compare(out_gpu, lse_gpu, out_ref, lse_ref, rows=None, label=""):

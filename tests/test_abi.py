@@ -82,14 +82,39 @@ def test_python_binding_refuses_cpu_tensors(lib):
         binding.prefill_attn_varlen(t, t, t, i, i, t[None], t[None], i[:1], t)
 
 
-def _call_ex(lib, window=0, causal=1, struct_size=None):
-    opts = binding.PaOptions(ctypes.sizeof(binding.PaOptions) if struct_size is None else struct_size, window)
+def _call_ex(lib, window=0, causal=1, struct_size=None, block_table=None, block_size=0, max_blocks=0,
+             num_blocks=0, reserved=0):
+    opts = binding.PaOptions(ctypes.sizeof(binding.PaOptions) if struct_size is None else struct_size, window,
+                             block_table, block_size, max_blocks, num_blocks, reserved)
     return lib.prefill_attn_varlen_ex(16, 32, 48, 64, 80, 96, 112, 128, 144, None, 1, 4, 8, 4, 2, 64,
                                       0.125, causal, ctypes.byref(opts), None)
 
 
-@pytest.mark.parametrize("kw,msg", [(dict(window=-1), "window"), (dict(window=8, causal=0), "causal"),
-                                    (dict(struct_size=2), "struct_size")])
-def test_options_are_checked_before_launch(lib, kw, msg):
-    assert _call_ex(lib, **kw) == 1
+_PAGED = dict(block_table=256, block_size=8, max_blocks=1, num_blocks=4)
+
+
+@pytest.mark.parametrize("kw,status,msg", [
+    (dict(window=-1), 1, "window"),
+    (dict(window=8, causal=0), 1, "causal"),
+    (dict(struct_size=2), 1, "struct_size"),
+    (dict(reserved=1), 1, "reserved"),
+    (dict(_PAGED, struct_size=16), 1, "paged"),  # covers the pointer but not the sizes
+    (dict(_PAGED, block_size=12), 2, "power of two"),
+    (dict(_PAGED, block_size=4, max_blocks=2), 2, "power of two"),
+    (dict(_PAGED, block_size=16), 1, "max_cache_len"),
+    (dict(_PAGED, num_blocks=0), 1, "num_blocks"),
+    (dict(_PAGED, block_table=258), 1, "aligned"),
+    (dict(_PAGED, num_blocks=1 << 30), 2, "num_blocks"),
+])
+def test_options_are_checked_before_launch(lib, kw, status, msg):
+    assert _call_ex(lib, **kw) == status
     assert msg in lib.prefill_attn_last_error().decode()
+
+
+def test_options_layout_matches_header():
+    """The binding's pa_options has the header's field offsets (x86-64 and aarch64 LP64)."""
+    P = binding.PaOptions
+    assert [(n, getattr(P, n).offset) for n, _ in P._fields_] == [
+        ("struct_size", 0), ("window", 4), ("block_table", 8), ("block_size", 16),
+        ("max_blocks_per_seq", 20), ("num_blocks", 24), ("reserved", 28)]
+    assert ctypes.sizeof(P) == 32
