@@ -56,7 +56,7 @@ def load_library(path: str):
     P = ctypes.c_void_p
     I = ctypes.c_int
     f.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, I,
-                  ctypes.c_double, I, I, P, I, I, I, P, ctypes.c_int64, I]
+                  ctypes.c_double, I, I, P, I, I, I, ctypes.c_double, P, ctypes.c_int64, I]
     f.restype = I
     return lib
 
@@ -75,7 +75,7 @@ def _ptr(a: Optional[np.ndarray]):
 def prefill_attention(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_offsets, cache_k, cache_v, *,
                       n_heads: int, n_kv_heads: int, head_dim: int, max_cache_len: int,
                       scale: float, causal: bool = True, window: int = 0, block_table=None, block_size: int = 0,
-                      rows: Optional[np.ndarray] = None,
+                      rope_theta: float = 0.0, rows: Optional[np.ndarray] = None,
                       want_cache: bool = True, threads: int = 0, lib=None):
     """Run the oracle.
 
@@ -85,6 +85,7 @@ def prefill_attention(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_offsets, cache_
     window: 0, or W > 0 (causal only): each query sees its W most recent keys.
     block_table: optional int32 [B, max_blocks]; then cache_k/v are block pools
     [num_blocks, Hk, block_size, d] and max_cache_len = max_blocks * block_size.
+    rope_theta > 0: rotary embedding of the new q/k at their absolute positions.
 
     Returns (out float64 [T,H,d], lse float64 [T,H], cache_k', cache_v') where
     unselected rows of out/lse are NaN and the cache images are None when
@@ -116,7 +117,7 @@ def prefill_attention(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_offsets, cache_
         _ptr(q), _ptr(k), _ptr(v), _ptr(cu_q), _ptr(cu_k), _ptr(off), _ptr(cache_k), _ptr(cache_v),
         _ptr(ck), _ptr(cv), _ptr(out), _ptr(lse),
         num_seqs, max_cache_len, n_heads, n_kv_heads, head_dim, float(scale), int(bool(causal)), int(window),
-        _ptr(bt), int(block_size), int(max_blocks), int(num_blocks), _ptr(sel), 0 if sel is None else sel.shape[0], int(threads))
+        _ptr(bt), int(block_size), int(max_blocks), int(num_blocks), float(rope_theta), _ptr(sel), 0 if sel is None else sel.shape[0], int(threads))
     if rc != 0:
         raise ValueError(f"oracle: {ERRORS.get(rc, rc)}")
     if want_cache:

@@ -46,6 +46,14 @@
  *    and position p of sequence b lives in row p % block_size of block
  *    block_table[b][p / block_size].  Reads of the prefix and writes of the new
  *    tokens both go through the table; blocks may be shared between sequences.
+ *  - Rotary position embedding (optional, rope_theta > 0; [mhpn] §5.1): the new
+ *    query and key at absolute position m are rotated by the angles
+ *    m * inv_freq[i], inv_freq[i] = 1 / theta^(2i / head_dim), i < head_dim/2,
+ *    in the rotate-half pairing of the Llama models the page names (dimension i
+ *    pairs with i + head_dim/2).  inv_freq and the angles are fp32, as the
+ *    page's formula computes them; cos/sin and the rotation are fp64.  The
+ *    cache receives the rotated key rounded to bf16 (nearest, ties to even);
+ *    cached prefix keys are used as stored (they were rotated when written).
  *
  * Inputs q, k, v and the caches are bf16 bit patterns (uint16); each value is
  * widened exactly to fp64 before any arithmetic.  Outputs are fp64:
@@ -83,7 +91,38 @@ typedef struct {
     int window; /* 0: none */
     const int32_t *block_table; /* paged cache: [num_seqs][max_blocks]; NULL: contiguous slots */
     int block_size, max_blocks, num_blocks;
+    const double *rope_cos, *rope_sin; /* [max_cache_len][d/2]; NULL: no rotary embedding */
 } problem;
+
+/* The rotation of a head vector x (fp64, length d) to absolute position pos. */
+static void rope_rotate(const problem *pb, int pos, double *x)
+{
+    const int half = pb->d / 2;
+    const double *c = pb->rope_cos + (size_t)pos * half;
+    const double *sn = pb->rope_sin + (size_t)pos * half;
+    for (int i = 0; i < half; ++i) {
+        const double a = x[i], b = x[i + half];
+        x[i] = a * c[i] - b * sn[i];
+        x[i + half] = b * c[i] + a * sn[i];
+    }
+}
+
+/* Nearest bf16 (ties to even) of a finite double, as a bit pattern. */
+static uint16_t double_to_bf16(double x)
+{
+    if (x == 0.0)
+        return signbit(x) ? 0x8000 : 0;
+    int e;
+    frexp(x, &e);            /* |x| = f * 2^e, f in [0.5, 1) */
+    if (e < -125)
+        e = -125;            /* bf16 subnormal spacing 2^-133 */
+    const double q = ldexp(1.0, e - 8); /* spacing of 8-significant-bit values near x */
+    const double r = nearbyint(x / q) * q; /* default rounding mode: ties to even */
+    const float f = (float)r; /* exact: r has at most 8 significant bits */
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return (uint16_t)(u >> 16);
+}
 
 /* Row of the cache holding position `pos` of sequence b, KV head kvh. */
 static size_t cache_row(const problem *pb, int b, int kvh, int pos)
@@ -105,8 +144,21 @@ static const uint16_t *key_row(const problem *pb, const uint16_t *cache, const u
     return fresh + ((size_t)(pb->cu_q[b] + (j - P)) * pb->n_kv_heads + kvh) * pb->d;
 }
 
-/* One query row (sequence b, new token i, head h).  `s` has room for P+n doubles. */
-static void attend_row(const problem *pb, int b, int i, int h, double *s)
+/* Key (or value) row j of sequence b widened to fp64 in `dst`; new keys are
+ * rotated to their position when the rotary embedding is on. */
+static void load_key(const problem *pb, const uint16_t *cache, const uint16_t *fresh, int b, int kvh, int j,
+                     int rotate, double *dst)
+{
+    const uint16_t *r = key_row(pb, cache, fresh, b, kvh, j);
+    for (int e = 0; e < pb->d; ++e)
+        dst[e] = bf16_to_double(r[e]);
+    if (rotate && pb->rope_cos && j >= pb->off[b])
+        rope_rotate(pb, j, dst);
+}
+
+/* One query row (sequence b, new token i, head h).  `s` has room for P+n
+ * doubles, `qv` and `kv` for head_dim each. */
+static void attend_row(const problem *pb, int b, int i, int h, double *s, double *qv, double *kv)
 {
     const int d = pb->d;
     const int P = pb->off[b];
@@ -119,12 +171,16 @@ static void attend_row(const problem *pb, int b, int i, int h, double *s)
     const int last = pb->causal ? P + i : Lk - 1;
     const int first = (pb->causal && pb->window > 0 && P + i - pb->window + 1 > 0) ? P + i - pb->window + 1 : 0;
 
+    for (int e = 0; e < d; ++e)
+        qv[e] = bf16_to_double(qrow[e]);
+    if (pb->rope_cos)
+        rope_rotate(pb, P + i, qv);
     double m = -INFINITY;
     for (int j = first; j <= last; ++j) {
-        const uint16_t *kr = key_row(pb, pb->cache_k, pb->k, b, kvh, j);
+        load_key(pb, pb->cache_k, pb->k, b, kvh, j, 1, kv);
         double dot = 0.0;
         for (int e = 0; e < d; ++e)
-            dot += bf16_to_double(qrow[e]) * bf16_to_double(kr[e]);
+            dot += qv[e] * kv[e];
         s[j] = pb->scale * dot;
         if (s[j] > m)
             m = s[j];
@@ -170,6 +226,8 @@ static int owner(const int32_t *cu_q, int num_seqs, int64_t t)
  * Paged cache: block_table != NULL, the caches are [num_blocks][Hk][block_size]
  * [head_dim] pools and max_cache_len must be max_blocks * block_size.
  *
+ * rope_theta > 0 turns the rotary embedding on (head_dim must be even).
+ *
  * rows: optional list of (t * n_heads + h) query rows to compute; NULL = all.
  * Only the selected rows of out/lse are written.  The cache image
  * (cache_k_out/cache_v_out, may be NULL) is written in full: a copy of the
@@ -184,12 +242,13 @@ int oracle_prefill_attention(
     int num_seqs, int max_cache_len, int n_heads, int n_kv_heads, int head_dim,
     double scale, int causal, int window,
     const int32_t *block_table, int block_size, int max_blocks, int num_blocks,
+    double rope_theta,
     const int64_t *rows, int64_t n_rows, int n_threads)
 {
     if (window < 0 || (window > 0 && !causal))
         return -7;
     if (num_seqs < 0 || max_cache_len < 0 || n_heads <= 0 || n_kv_heads <= 0 || head_dim <= 0 ||
-        n_heads % n_kv_heads != 0)
+        n_heads % n_kv_heads != 0 || rope_theta < 0 || (rope_theta > 0 && head_dim % 2 != 0))
         return -1;
     if (num_seqs > 0 && cu_seqlens_q[0] != 0)
         return -2;
@@ -214,14 +273,36 @@ int oracle_prefill_attention(
 
     problem pb = {q, k, v, cache_k, cache_v, cu_seqlens_q, cache_offsets, out, lse,
                   num_seqs, max_cache_len, n_heads, n_kv_heads, head_dim, scale, causal, window,
-                  block_table, block_size, max_blocks, num_blocks};
+                  block_table, block_size, max_blocks, num_blocks, NULL, NULL};
+
+    /* cos/sin of every position's angles: inv_freq and m * inv_freq in fp32 */
+    double *rope_tab = NULL;
+    if (rope_theta > 0) {
+        const int half = head_dim / 2;
+        const size_t n_tab = (size_t)(max_cache_len > 0 ? max_cache_len : 1) * half;
+        rope_tab = (double *)malloc(2 * n_tab * sizeof(double));
+        if (!rope_tab)
+            return -6;
+        for (int i = 0; i < half; ++i) {
+            const float inv_freq = 1.0f / powf((float)rope_theta, (float)(2 * i) / (float)head_dim);
+            for (int pos = 0; pos < max_cache_len; ++pos) {
+                const float angle = (float)pos * inv_freq;
+                rope_tab[(size_t)pos * half + i] = cos((double)angle);
+                rope_tab[n_tab + (size_t)pos * half + i] = sin((double)angle);
+            }
+        }
+        pb.rope_cos = rope_tab;
+        pb.rope_sin = rope_tab + n_tab;
+    }
 
     const int64_t n_all = total_q * n_heads;
     const int64_t n_work = rows ? n_rows : n_all;
     if (rows) {
         for (int64_t r = 0; r < n_rows; ++r)
-            if (rows[r] < 0 || rows[r] >= n_all)
+            if (rows[r] < 0 || rows[r] >= n_all) {
+                free(rope_tab);
                 return -5;
+            }
     }
 #ifdef _OPENMP
     if (n_threads > 0)
@@ -232,7 +313,8 @@ int oracle_prefill_attention(
     int failed = 0;
 #pragma omp parallel
     {
-        double *s = (double *)malloc(sizeof(double) * (size_t)(max_cache_len > 0 ? max_cache_len : 1));
+        double *s = (double *)malloc(sizeof(double) * ((size_t)(max_cache_len > 0 ? max_cache_len : 1) +
+                                                       2 * (size_t)head_dim));
         if (!s) {
 #pragma omp atomic write
             failed = 1;
@@ -245,12 +327,14 @@ int oracle_prefill_attention(
             const int64_t t = r / n_heads;
             const int h = (int)(r % n_heads);
             const int b = owner(cu_seqlens_q, num_seqs, t);
-            attend_row(&pb, b, (int)(t - cu_seqlens_q[b]), h, s);
+            attend_row(&pb, b, (int)(t - cu_seqlens_q[b]), h, s + 2 * (size_t)head_dim, s, s + head_dim);
         }
         free(s);
     }
-    if (failed)
+    if (failed) {
+        free(rope_tab);
         return -6;
+    }
 
     /* The cache image: everything as it was, plus the new tokens at P + i. */
     const size_t cache_elems = block_table ? (size_t)num_blocks * n_kv_heads * block_size * head_dim
@@ -267,11 +351,22 @@ int oracle_prefill_attention(
             const int P = cache_offsets[b];
             const int n = cu_seqlens_q[b + 1] - cu_seqlens_q[b];
             for (int kvh = 0; kvh < n_kv_heads; ++kvh)
-                for (int i = 0; i < n; ++i)
-                    memcpy(dst + cache_row(&pb, b, kvh, P + i) * head_dim,
-                           fresh + ((size_t)(cu_seqlens_q[b] + i) * n_kv_heads + kvh) * head_dim,
-                           (size_t)head_dim * sizeof(uint16_t));
+                for (int i = 0; i < n; ++i) {
+                    uint16_t *row = dst + cache_row(&pb, b, kvh, P + i) * head_dim;
+                    const uint16_t *in = fresh + ((size_t)(cu_seqlens_q[b] + i) * n_kv_heads + kvh) * head_dim;
+                    if (c == 0 && pb.rope_cos) {
+                        double x[head_dim];
+                        for (int e = 0; e < head_dim; ++e)
+                            x[e] = bf16_to_double(in[e]);
+                        rope_rotate(&pb, P + i, x);
+                        for (int e = 0; e < head_dim; ++e)
+                            row[e] = double_to_bf16(x[e]);
+                    } else {
+                        memcpy(row, in, (size_t)head_dim * sizeof(uint16_t));
+                    }
+                }
         }
     }
+    free(rope_tab);
     return 0;
 }

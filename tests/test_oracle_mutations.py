@@ -32,8 +32,8 @@ MUTATIONS = {
                              "key_row(pb, pb->cache_k, pb->k, b, kvh, j)"),
     "lse_without_max": ("pb->lse[t * pb->n_heads + h] = m + log(Z);",
                         "pb->lse[t * pb->n_heads + h] = log(Z);"),
-    "cache_written_at_zero": ("memcpy(dst + cache_row(&pb, b, kvh, P + i) * head_dim,",
-                              "memcpy(dst + cache_row(&pb, b, kvh, i) * head_dim,"),
+    "cache_written_at_zero": ("uint16_t *row = dst + cache_row(&pb, b, kvh, P + i) * head_dim;",
+                              "uint16_t *row = dst + cache_row(&pb, b, kvh, i) * head_dim;"),
     "prefix_keys_shifted": ("return cache + cache_row(pb, b, kvh, j) * pb->d;",
                             "return cache + cache_row(pb, b, kvh, j > 0 ? j - 1 : 0) * pb->d;"),
     # paged cache (every mutant stays inside the pool: the pin tables fill every entry)
@@ -42,6 +42,20 @@ MUTATIONS = {
                                "((size_t)kvh * pb->num_blocks + blk) * pb->block_size"),
     "paged_table_of_first_seq": ("pb->block_table[(size_t)b * pb->max_blocks + pos / pb->block_size]",
                                  "pb->block_table[pos / pb->block_size]"),
+    # rotary embedding
+    "rope_interleaved_pairs": ("""        const double a = x[i], b = x[i + half];
+        x[i] = a * c[i] - b * sn[i];
+        x[i + half] = b * c[i] + a * sn[i];""", """        const double a = x[2 * i], b = x[2 * i + 1];
+        x[2 * i] = a * c[i] - b * sn[i];
+        x[2 * i + 1] = b * c[i] + a * sn[i];"""),
+    "rope_rotates_backwards": ("""        x[i] = a * c[i] - b * sn[i];
+        x[i + half] = b * c[i] + a * sn[i];""", """        x[i] = a * c[i] + b * sn[i];
+        x[i + half] = b * c[i] - a * sn[i];"""),
+    "rope_frequency_exponent_halved": ("powf((float)rope_theta, (float)(2 * i) / (float)head_dim)",
+                                       "powf((float)rope_theta, (float)(i) / (float)head_dim)"),
+    "rope_query_position_without_prefix": ("rope_rotate(pb, P + i, qv);", "rope_rotate(pb, i, qv);"),
+    "rope_key_position_without_prefix": ("rope_rotate(pb, j, dst);", "rope_rotate(pb, j - pb->off[b], dst);"),
+    "rope_cache_keeps_unrotated_key": ("if (c == 0 && pb.rope_cos) {", "if (0 && pb.rope_cos) {"),
 }
 
 PIN_TESTS = [
@@ -59,6 +73,11 @@ PIN_TESTS = [
     functools.partial(pins.test_window_matches_torch_sdpa_float64, window=37),
     functools.partial(pins.test_paged_equals_contiguous, bs=16, seed=1),
     functools.partial(pins.test_paged_equals_contiguous, bs=5, seed=2),
+    pins.test_rope_position_zero_is_identity,
+    functools.partial(pins.test_rope_closed_form_rotations, m=7),
+    pins.test_rope_relative_position_invariance,
+    pins.test_rope_chunked_equals_one_shot,
+    pins.test_rope_matches_complex_rotation_and_sdpa,
 ]
 
 

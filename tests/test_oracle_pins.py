@@ -22,7 +22,7 @@ GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
 
 def run_oracle(oracle_mod, wl, cache_k, cache_v, inp, rows=None, causal=None, window=0,
-               block_table=None, block_size=0):
+               block_table=None, block_size=0, rope_theta=0.0):
     cap = wl.max_cache_len if block_table is None else block_table.shape[1] * block_size
     return oracle_mod.prefill_attention(
         W.bf16_bits(inp["q"]), W.bf16_bits(inp["k"]), W.bf16_bits(inp["v"]),
@@ -31,7 +31,8 @@ def run_oracle(oracle_mod, wl, cache_k, cache_v, inp, rows=None, causal=None, wi
         n_heads=wl.n_heads, n_kv_heads=wl.n_kv_heads, head_dim=wl.head_dim,
         max_cache_len=cap, scale=wl.scale,
         causal=wl.causal if causal is None else causal, window=window, rows=rows,
-        block_table=None if block_table is None else np.asarray(block_table, np.int32), block_size=block_size)
+        block_table=None if block_table is None else np.asarray(block_table, np.int32), block_size=block_size,
+        rope_theta=rope_theta)
 
 
 def f64(t):
@@ -532,3 +533,144 @@ def test_paged_bad_block_table_is_rejected(oracle_mod):
             inp["cu_seqlens_q"].numpy(), inp["cu_seqlens_k"].numpy(), inp["cache_offsets"].numpy(),
             W.bf16_bits(pk), W.bf16_bits(pv), n_heads=2, n_kv_heads=2, head_dim=32, max_cache_len=9,
             scale=wl.scale, block_table=table.numpy(), block_size=bs)
+
+
+# ---------------------------------------------------------------- rotary (RoPE) ---
+# [mhpn] §5.1: the token at position m has its Q/K rotated by theta_m = m * inv_freq,
+# inv_freq = 1 / 10000^(arange(0, d, 2) / d), for the Llama models (rotate-half
+# pairing: dimension i with i + d/2).
+
+def test_rope_position_zero_is_identity(oracle_mod):
+    """A lone token sits at position 0: no rotation, so the cache gets k bit for
+    bit, out = v exactly and lse = scale * q.k."""
+    wl = _custom("rope0", 4, 2, 64, [1, 1], [0, 0], cap=4)
+    ck, cv, (inp,) = W.make_inputs(wl)
+    out, lse, ck1, _ = run_oracle(oracle_mod, wl, ck, cv, inp, rope_theta=10000.0)
+    for b in range(2):
+        assert np.array_equal(ck1[b, :, 0], W.bf16_bits(inp["k"][b]))
+        assert np.array_equal(out[b], f64(inp["v"][b]).repeat(2, axis=0))
+        qk = (f64(inp["q"][b]).reshape(2, 2, 64) * f64(inp["k"][b])[:, None]).sum(-1).ravel()
+        assert np.allclose(lse[b], wl.scale * qk, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("m", [1, 7, 300, 4095])
+def test_rope_closed_form_rotations(oracle_mod, m):
+    """Frequency 0 has inv_freq = 1 (angle m) and frequency d/4 has inv_freq =
+    10000^-1/2 = 0.01 (angle m / 100): a unit key along dimension i lands on
+    (cos, sin) at dimensions (i, i + d/2) of the cached, rotated key."""
+    d = 32
+    wl = _custom("ropecf", 2, 2, d, [m + 1], [0], cap=m + 1)
+    ck, cv, (inp,) = W.make_inputs(wl)
+    k = inp["k"].clone()
+    k[m] = 0
+    k[m, 0, 0] = 1.0          # head 0: e_0
+    k[m, 1, d // 4] = 1.0     # head 1: e_{d/4}
+    _, _, ck1, _ = run_oracle(oracle_mod, wl, ck, cv, dict(inp, k=k), rope_theta=10000.0)
+    got = ck1[0, :, m].view(np.int16)
+    got = torch.from_numpy(got.copy()).view(torch.bfloat16).double().numpy()
+    a0 = float(np.float32(m))                          # fp32 angle of frequency 0
+    a1 = float(np.float32(np.float32(m) * np.float32(0.01)))
+    exp0 = np.zeros(d); exp0[0], exp0[d // 2] = math.cos(a0), math.sin(a0)
+    exp1 = np.zeros(d); exp1[d // 4], exp1[d // 4 + d // 2] = math.cos(a1), math.sin(a1)
+    bf = lambda x: torch.tensor(x, dtype=torch.float64).to(torch.bfloat16).double().numpy()
+    # frequency d/4's inv_freq is 0.01 up to fp32 rounding of the page's formula
+    assert np.array_equal(got[0], bf(exp0))
+    assert np.allclose(got[1], exp1, atol=2 ** -8 * 1.01 + m * 1e-8)
+
+
+def test_rope_relative_position_invariance(oracle_mod):
+    """With a window of 2 the second of two new tokens sees exactly those two:
+    its scores then depend on positions only through their difference, so moving
+    both tokens from positions 0, 1 to 777, 778 leaves its output unchanged
+    (up to the fp32 rounding of the larger angles)."""
+    H, Hk, d = 4, 2, 64
+    outs = []
+    for P in (0, 777):
+        wl = _custom("roperel", H, Hk, d, [2], [P], cap=P + 2)
+        ck, cv, (inp,) = W.make_inputs(_custom("roperel", H, Hk, d, [2], [0], cap=P + 2, seed=11))
+        inp = dict(inp, cu_seqlens_k=torch.tensor([0, P + 2], dtype=torch.int32),
+                   cache_offsets=torch.tensor([P], dtype=torch.int32))
+        out, lse, _, _ = run_oracle(oracle_mod, wl, ck.nan_to_num(0.0), cv.nan_to_num(0.0), inp,
+                                    window=2, rope_theta=10000.0)
+        outs.append((out[1], lse[1]))
+    assert np.allclose(outs[0][0], outs[1][0], atol=2e-4)
+    assert np.allclose(outs[0][1], outs[1][1], atol=2e-4)
+    # and the rotation matters: without it the two positions are not equivalent to
+    # a plain (unrotated) run
+    wl0 = _custom("roperel", H, Hk, d, [2], [0], cap=2)
+    ck, cv, (inp,) = W.make_inputs(_custom("roperel", H, Hk, d, [2], [0], cap=779, seed=11))
+    plain, _, _, _ = run_oracle(oracle_mod, wl0, ck[:, :, :2].contiguous(), cv[:, :, :2].contiguous(), inp, window=2)
+    assert np.abs(plain[1] - outs[0][0]).max() > 1e-3
+
+
+def test_rope_chunked_equals_one_shot(oracle_mod):
+    """Chunks read the earlier chunks' rotated keys back from the cache (as bf16):
+    the result matches one launch up to that rounding."""
+    H, Hk, d, n, c = 4, 2, 64, 240, 80
+    one = _custom("ropeone", H, Hk, d, [n], [0], cap=n)
+    ck, cv, (inp,) = W.make_inputs(one)
+    out1, _, ck1, _ = run_oracle(oracle_mod, one, ck, cv, inp, rope_theta=10000.0)
+    cur_k, cur_v = W.bf16_bits(ck), W.bf16_bits(cv)
+    outs = []
+    for s_ in range(n // c):
+        sl = slice(s_ * c, (s_ + 1) * c)
+        o, _, cur_k, cur_v = oracle_mod.prefill_attention(
+            W.bf16_bits(inp["q"][sl]), W.bf16_bits(inp["k"][sl]), W.bf16_bits(inp["v"][sl]),
+            np.array([0, c], np.int32), np.array([0, s_ * c + c], np.int32), np.array([s_ * c], np.int32),
+            cur_k, cur_v, n_heads=H, n_kv_heads=Hk, head_dim=d, max_cache_len=n, scale=one.scale,
+            rope_theta=10000.0)
+        outs.append(o)
+    assert np.abs(np.concatenate(outs) - out1).max() < 2e-2
+    assert np.array_equal(cur_k, ck1)  # the same rotated keys, rounded the same way
+
+
+def test_rope_matches_complex_rotation_and_sdpa(oracle_mod):
+    """Independent restatement: RoPE as multiplication of (x_i + j x_{i+d/2}) by
+    exp(j * angle), then PyTorch float64 SDPA, against the oracle."""
+    wl = W.random_workload(81, head_dim=64, group=2, max_len=50, max_prefix=60)
+    ck, cv, (inp,) = W.make_inputs(wl, sentinel=False)
+    theta = 500000.0
+    out, _, _, _ = run_oracle(oracle_mod, wl, ck, cv, inp, rope_theta=theta)
+    d, half = wl.head_dim, wl.head_dim // 2
+    inv = (np.float32(1.0) / np.power(np.float32(theta), np.arange(0, d, 2, dtype=np.float32) / np.float32(d))
+           ).astype(np.float32)
+    cu = inp["cu_seqlens_q"].tolist()
+    off = inp["cache_offsets"].tolist()
+    pos = np.concatenate([off[b] + np.arange(cu[b + 1] - cu[b]) for b in range(len(off))]).astype(np.float32)
+    ang = (pos[:, None] * inv[None, :]).astype(np.float32).astype(np.float64)  # fp32 angles
+    rot = np.exp(1j * ang)[:, None, :]
+
+    def apply(x):
+        x = f64(x)
+        z = (x[..., :half] + 1j * x[..., half:]) * rot
+        return torch.from_numpy(np.concatenate([z.real, z.imag], -1))
+    qr, kr = apply(inp["q"]), apply(inp["k"])
+    ref = _sdpa_reference_f64(wl, ck, cv, qr, kr, f64(inp["v"]), inp)
+    # numpy's fp32 power and the C library's powf may differ in the last bit of
+    # inv_freq, which moves an angle at position m by about m * 6e-8
+    assert np.nanmax(np.abs(out - ref)) < 1e-5
+
+
+def _sdpa_reference_f64(wl, ck, cv, q, k, v, inp):
+    """SDPA per (sequence, head) on already-float64 new q/k/v (rotated)."""
+    import torch.nn.functional as F
+    T = q.shape[0]
+    out = torch.full((T, wl.n_heads, wl.head_dim), float("nan"), dtype=torch.float64)
+    cu = inp["cu_seqlens_q"].tolist()
+    off = inp["cache_offsets"].tolist()
+    G = wl.n_heads // wl.n_kv_heads
+    v = torch.as_tensor(v)
+    for b in range(len(off)):
+        n, P = cu[b + 1] - cu[b], off[b]
+        if n == 0:
+            continue
+        K = torch.cat([ck[b, :, :P].permute(1, 0, 2).double(), k[cu[b]:cu[b + 1]]], 0)
+        V = torch.cat([cv[b, :, :P].permute(1, 0, 2).double(), v[cu[b]:cu[b + 1]]], 0)
+        Q = q[cu[b]:cu[b + 1]]
+        key, qpos = torch.arange(P + n)[None, :], (P + torch.arange(n))[:, None]
+        mask = key <= qpos
+        for h in range(wl.n_heads):
+            o = F.scaled_dot_product_attention(Q[None, :, h], K[None, :, h // G], V[None, :, h // G],
+                                               attn_mask=mask[None], scale=wl.scale)
+            out[cu[b]:cu[b + 1], h] = o[0]
+    return out.numpy()
