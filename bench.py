@@ -179,7 +179,7 @@ def row_flops(wl, step, rows, window=0):
     return int(4 * wl.head_dim * vis.sum())
 
 
-def time_oracle(wl, inputs, rows, threads, window=0):
+def time_oracle(wl, inputs, rows, threads, window=0, rope=0.0):
     import oracle
     from prefill_phase_attention_gb300 import workloads as W
     cache_k, cache_v, steps = inputs
@@ -190,25 +190,26 @@ def time_oracle(wl, inputs, rows, threads, window=0):
                              inp["cu_seqlens_q"].numpy(), inp["cu_seqlens_k"].numpy(),
                              inp["cache_offsets"].numpy(), ck, cv, n_heads=wl.n_heads,
                              n_kv_heads=wl.n_kv_heads, head_dim=wl.head_dim, max_cache_len=wl.max_cache_len,
-                             scale=wl.scale, causal=wl.causal, window=window, rows=rows, want_cache=False,
+                             scale=wl.scale, causal=wl.causal, window=window, rope_theta=rope, rows=rows,
+                             want_cache=False,
                              threads=threads)
     return time.perf_counter() - t0
 
 
-def cpu_baseline(wl, inputs, budget_s: float = 15.0, window: int = 0):
+def cpu_baseline(wl, inputs, budget_s: float = 15.0, window: int = 0, rope: float = 0.0):
     """The oracle on this host's cores over a sample sized to about `budget_s` seconds."""
     import oracle
     oracle.build()
     cores = host_cores()
     step = wl.steps[-1]
-    time_oracle(wl, inputs, oracle_sample_rows(wl, step, 64, seed=10), cores, window)  # threads, page faults
+    time_oracle(wl, inputs, oracle_sample_rows(wl, step, 64, seed=10), cores, window, rope)  # threads, page faults
     cal = oracle_sample_rows(wl, step, 512, seed=11)
-    dt = time_oracle(wl, inputs, cal, cores, window)
+    dt = time_oracle(wl, inputs, cal, cores, window, rope)
     rate = row_flops(wl, step, cal, window) / max(dt, 1e-6)  # FLOP/s of the oracle on this host
     per_row = row_flops(wl, step, cal, window) / cal.size
     n = int(rate * budget_s / max(per_row, 1.0))
     rows = oracle_sample_rows(wl, step, max(512, n), seed=12)
-    dt = time_oracle(wl, inputs, rows, cores, window)
+    dt = time_oracle(wl, inputs, rows, cores, window, rope)
     fl = row_flops(wl, step, rows, window)
     return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
             "sample": f"{rows.size} query rows (token, head) drawn uniformly from {wl.name} "
@@ -247,10 +248,10 @@ def run_ours(args, ws, rank, local):
     stream = torch.cuda.current_stream()
 
     def call(d, o, l):
-        if args.window or args.paged:
+        if args.window or args.paged or args.rope:
             binding.prefill_attn_varlen_ex(d["q"], d["k"], d["v"], d["cu_seqlens_q"], d["cu_seqlens_k"], ck, cv,
                                            d["cache_offsets"], o, l, scale=wl.scale, causal=wl.causal,
-                                           window=args.window, block_table=table_d)
+                                           window=args.window, block_table=table_d, rope_theta=args.rope)
         else:
             binding.prefill_attn_varlen(d["q"], d["k"], d["v"], d["cu_seqlens_q"], d["cu_seqlens_k"], ck, cv,
                                         d["cache_offsets"], o, l, scale=wl.scale, causal=wl.causal)
@@ -311,7 +312,8 @@ def run_ours(args, ws, rank, local):
     t_tot = sum(t for _, t in per_launch)
     achieved = fl_tot / (t_tot * 1e-3) / 1e12
     traffic = None
-    variant = (f"_window{args.window}" if args.window else "") + (f"_paged{args.paged}" if args.paged else "")
+    variant = (f"_window{args.window}" if args.window else "") + (f"_paged{args.paged}" if args.paged else "") \
+        + ("_rope" if args.rope else "")
     tpath = os.path.join(ROOT, "profiles", f"traffic_{wl.name}{variant}.json")
     if os.path.exists(tpath):
         rec = json.load(open(tpath))
@@ -353,9 +355,10 @@ def run_ours(args, ws, rank, local):
         "tokens_per_s": round(tokens_s, 1),
         "pct_of_bf16_peak": round(100 * value / ws / peak, 2),
         "config": {"workload": wl.name + (f"+window{args.window}" if args.window else "")
-                   + (f"+paged{args.paged}" if args.paged else ""),
+                   + (f"+paged{args.paged}" if args.paged else "") + (f"+rope{args.rope:g}" if args.rope else ""),
                    "launches_per_step": n_launch, "window": args.window, "num_seqs": wl.num_seqs,
                    "kv_cache": f"paged, {args.paged}-token blocks" if args.paged else "contiguous per sequence",
+                   "rope_theta": args.rope,
                    "tokens_per_step": wl.tokens(), "n_heads": wl.n_heads, "n_kv_heads": wl.n_kv_heads,
                    "head_dim": wl.head_dim, "causal": wl.causal, "causal_flops_per_step": flops_step,
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
@@ -374,7 +377,8 @@ def run_ours(args, ws, rank, local):
         "clocks": clocks,
     }
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(wl, inputs, budget_s=args.cpu_budget, window=args.window)
+        result["cpu_baseline"] = cpu_baseline(wl, inputs, budget_s=args.cpu_budget, window=args.window,
+                                              rope=args.rope)
     if rank == 0:
         print(json.dumps(result), flush=True)
     if ws > 1:
@@ -397,10 +401,10 @@ def run_reference(args, ws, rank):
     rows = oracle_sample_rows(wl, step, args.ref_rows, seed=13)
     fl = row_flops(wl, step, rows, args.window)
     for _ in range(args.warmup):
-        time_oracle(wl, inputs, rows, cores, args.window)
+        time_oracle(wl, inputs, rows, cores, args.window, args.rope)
     total = 0.0
     for _ in range(args.steps):
-        total += time_oracle(wl, inputs, rows, cores, args.window)
+        total += time_oracle(wl, inputs, rows, cores, args.window, args.rope)
     value = fl * args.steps / total / 1e12
     sample = (f"{rows.size} query rows (token, head) drawn uniformly from {wl.name} per step, "
               f"{fl / 1e9:.2f} GFLOP causal per step")
@@ -424,6 +428,7 @@ def main():
     ap.add_argument("--window", type=int, default=0, help="sliding window (0: none; the bench line counts only "
                                                              "the visible pairs)")
     ap.add_argument("--paged", type=int, default=0, help="block size of a paged KV cache (0: contiguous cache)")
+    ap.add_argument("--rope", type=float, default=0.0, help="rotary embedding base (0: none)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=25.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--ref-rows", type=int, default=128, help="oracle rows per reference step")

@@ -155,6 +155,21 @@ typedef struct pa_options {
     int32_t max_blocks_per_seq;
     int32_t num_blocks;
     int32_t reserved;  /* must be 0 */
+    /* Rotary position embedding ("Prefill不是热身：大模型推理的真正瓶颈与优化核心"
+     * (mhpn.cn) §5.1: the token at position m has its Q/K rotated by the angles
+     * m * inv_freq[i], inv_freq[i] = 1 / rope_theta^(2i / head_dim)).
+     * 0 = none (q and k are used as given).  rope_theta > 0: every new query
+     * and key is rotated to its absolute position cache_offsets[b] + i before
+     * attention, pairing dimension i with i + head_dim/2 (the Llama
+     * "rotate-half" layout), and the cache receives the rotated key; cached
+     * prefix keys are used as stored, i.e. already rotated.  inv_freq is
+     * computed on the host in fp32 as 1.0f / powf(rope_theta, 2i / head_dim),
+     * the angle is one fp32 multiply, and the rotation is fp32 rounded to bf16.
+     * q and k are not modified: the rotated copies live in the library's
+     * per-stream workspace (total_q * (n_heads + n_kv_heads) * head_dim * 2
+     * bytes more).  The call then runs three kernels instead of two. */
+    float rope_theta;
+    int32_t reserved2;  /* must be 0 */
 } pa_options;
 
 /*

@@ -25,7 +25,7 @@ class PaOptions(ctypes.Structure):
     _fields_ = [("struct_size", ctypes.c_uint32), ("window", ctypes.c_int32),
                 ("block_table", ctypes.c_void_p), ("block_size", ctypes.c_int32),
                 ("max_blocks_per_seq", ctypes.c_int32), ("num_blocks", ctypes.c_int32),
-                ("reserved", ctypes.c_int32)]
+                ("reserved", ctypes.c_int32), ("rope_theta", ctypes.c_float), ("reserved2", ctypes.c_int32)]
 
 
 # Entry points declared in include/prefill_attn.h: name -> (restype, argtypes)
@@ -124,10 +124,12 @@ def prefill_attn_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_k, cache_v, c
     _check(load().prefill_attn_varlen(*args))
 
 
-def make_options(window: int = 0, block_table=None, block_size: int = 0, num_blocks: int = 0) -> PaOptions:
+def make_options(window: int = 0, block_table=None, block_size: int = 0, num_blocks: int = 0,
+                 rope_theta: float = 0.0) -> PaOptions:
     o = PaOptions()
     o.struct_size = ctypes.sizeof(PaOptions)
     o.window = int(window)
+    o.rope_theta = float(rope_theta)
     if block_table is not None:
         o.block_table = block_table.data_ptr()
         o.block_size = int(block_size)
@@ -138,7 +140,7 @@ def make_options(window: int = 0, block_table=None, block_size: int = 0, num_blo
 
 def prefill_attn_varlen_ex(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_k, cache_v, cache_offsets, out, lse=None, *,
                            scale: Optional[float] = None, causal: bool = True, window: int = 0,
-                           block_table=None, stream=None) -> None:
+                           block_table=None, rope_theta: float = 0.0, stream=None) -> None:
     """prefill_attn_varlen with options.
 
     window > 0 restricts each query to its `window` most recent keys (causal only).
@@ -146,6 +148,8 @@ def prefill_attn_varlen_ex(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_k, cache_v
     cache_k/v are then block pools [num_blocks, n_kv_heads, block_size, head_dim]
     and position p of sequence b lives in row p % block_size of block
     block_table[b, p // block_size].
+    rope_theta > 0 rotates every new q/k to its absolute position (rotary
+    embedding, rotate-half pairing) before attention and the cache write.
     """
     cap = None
     if block_table is not None:
@@ -155,7 +159,7 @@ def prefill_attn_varlen_ex(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_k, cache_v
         cap = block_table.shape[1] * cache_k.shape[2]
     args = _varlen_args(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_k, cache_v, cache_offsets, out, lse,
                         scale, causal, stream, max_cache_len=cap)
-    opts = make_options(window, block_table, cache_k.shape[2], cache_k.shape[0])
+    opts = make_options(window, block_table, cache_k.shape[2], cache_k.shape[0], rope_theta)
     _check(load().prefill_attn_varlen_ex(*args[:-1], ctypes.byref(opts), args[-1]))
 
 

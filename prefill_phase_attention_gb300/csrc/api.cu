@@ -41,6 +41,8 @@ struct Workspace {
     size_t bytes = 0;
     int max_units = 0;
     int max_seqs = 0;
+    void* rope = nullptr;  // rotated q/k copies (grown on demand)
+    size_t rope_bytes = 0;
 };
 
 std::mutex g_mu;
@@ -81,8 +83,25 @@ pa_status get_workspace(int dev, cudaStream_t st, int num_seqs, int max_units, W
         return cuda_fail(e, "workspace init");
     }
     if (w.ptr) cudaFreeAsync(w.ptr, st);
+    nw.rope = w.rope;  // the rotary scratch is grown on its own
+    nw.rope_bytes = w.rope_bytes;
     w = nw;
     *out = &w;
+    return PA_OK;
+}
+
+// Grows (stream-ordered) the rotated-q/k scratch of a workspace to `bytes`.
+pa_status get_rope_scratch(Workspace* w, cudaStream_t st, size_t bytes, void** out) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (w->rope_bytes < bytes) {
+        void* nptr = nullptr;
+        cudaError_t e = cudaMallocAsync(&nptr, bytes, st);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync(rotary scratch)");
+        if (w->rope) cudaFreeAsync(w->rope, st);
+        w->rope = nptr;
+        w->rope_bytes = bytes;
+    }
+    *out = w->rope;
     return PA_OK;
 }
 
@@ -131,6 +150,7 @@ struct Options {
     int window = 0;
     const int32_t* block_table = nullptr;  // paged cache when set
     int block_size = 0, max_blocks = 0, num_blocks = 0;
+    float rope_theta = 0.f;                // rotary embedding when > 0
 };
 
 // Reads the caller's options; fields past the caller's struct_size count as zero.
@@ -163,6 +183,13 @@ pa_status read_options(const pa_options* opts, int causal, Options* o) {
         return fail(PA_ERR_INVALID_ARG, "pa_options.struct_size %u does not cover the paged-cache fields",
                     (unsigned)opts->struct_size);
     }
+    if (have >= offsetof(pa_options, rope_theta) + sizeof(float)) {
+        o->rope_theta = opts->rope_theta;
+        if (!(o->rope_theta >= 0.f) || !std::isfinite(o->rope_theta))
+            return fail(PA_ERR_INVALID_ARG, "rope_theta must be finite and >= 0 (got %g)", (double)o->rope_theta);
+    }
+    if (have >= offsetof(pa_options, reserved2) + sizeof(int32_t) && opts->reserved2 != 0)
+        return fail(PA_ERR_INVALID_ARG, "pa_options.reserved2 must be 0");
     return PA_OK;
 }
 
@@ -189,6 +216,7 @@ struct Scratch {
     pa::SeqInfo* seqs;
     pa::Unit* units;
     int max_units;
+    void* rope = nullptr;  // room for the rotated q and k when the rotary embedding is on
 };
 
 // Enqueues the scheduler and the attention kernel (arguments already checked).
@@ -219,6 +247,30 @@ pa_status enqueue(const void* q, const void* k, const void* v, const int32_t* cu
     sa.num_blocks = o.num_blocks;
     cudaError_t e = pa::launch_build_schedule(sa, stream);
     if (e != cudaSuccess) return cuda_fail(e, "schedule launch");
+
+    int launches = 2;
+    if (o.rope_theta > 0.f) {
+        // rotary prologue: attention then reads the rotated copies
+        pa::RopeParams rp;
+        rp.q = static_cast<const __nv_bfloat16*>(q);
+        rp.k = static_cast<const __nv_bfloat16*>(k);
+        rp.q_rot = static_cast<__nv_bfloat16*>(scr.rope);
+        rp.k_rot = rp.q_rot + (size_t)total_q * n_heads * head_dim;
+        rp.cu_seqlens_q = cu_seqlens_q;
+        rp.seqs = scr.seqs;
+        rp.total_q = total_q;
+        rp.num_seqs = num_seqs;
+        rp.n_heads = n_heads;
+        rp.n_kv_heads = n_kv_heads;
+        rp.head_dim = head_dim;
+        for (int i = 0; i < head_dim / 2; ++i)
+            rp.inv_freq[i] = 1.0f / std::pow(o.rope_theta, (float)(2 * i) / (float)head_dim);
+        e = pa::launch_rope(rp, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "rotary prologue launch");
+        q = rp.q_rot;
+        k = rp.k_rot;
+        launches = 3;
+    }
 
     pa::FwdParams p;
     p.k = static_cast<const __nv_bfloat16*>(k);
@@ -251,7 +303,7 @@ pa_status enqueue(const void* q, const void* k, const void* v, const int32_t* cu
     const int grid = (int)std::min<long long>(sms, units_bound);
     e = pa::launch_attn_fwd(p, head_dim, grid, stream);
     if (e != cudaSuccess) return cuda_fail(e, "attention launch");
-    g_last_launches = 2;
+    g_last_launches = launches;
     return PA_OK;
 }
 
@@ -312,6 +364,10 @@ pa_status prefill_attn_varlen_ex(const void* q, const void* k, const void* v, co
     s = get_workspace(dev, stream, num_seqs, (int)max_units_ll, &ws);
     if (s != PA_OK) return s;
     Scratch scr{static_cast<pa::WorkspaceHeader*>(ws->ptr), ws_seqs(*ws), ws_units(*ws), ws->max_units};
+    if (o.rope_theta > 0.f) {
+        s = get_rope_scratch(ws, stream, (size_t)total_q * (n_heads + n_kv_heads) * head_dim * 2, &scr.rope);
+        if (s != PA_OK) return s;
+    }
     return enqueue(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_k, cache_v, cache_offsets, out, lse, num_seqs, total_q,
                    max_cache_len, n_heads, n_kv_heads, head_dim, scale, causal, o, scr, max_units_ll, dev, stream);
 }
@@ -381,9 +437,9 @@ void prefill_attn_release(void) {
     int cur = 0;
     cudaGetDevice(&cur);
     for (auto& kv : g_ws) {
-        if (!kv.second.ptr) continue;
         cudaSetDevice(kv.first.first);
-        cudaFree(kv.second.ptr);
+        if (kv.second.ptr) cudaFree(kv.second.ptr);
+        if (kv.second.rope) cudaFree(kv.second.rope);
     }
     cudaSetDevice(cur);
     g_ws.clear();

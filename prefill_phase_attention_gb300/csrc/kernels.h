@@ -10,6 +10,20 @@ namespace pa {
 
 cudaError_t launch_build_schedule(const ScheduleArgs& a, cudaStream_t stream);
 
+// Rotary embedding prologue: q_rot/k_rot = q/k rotated to each token's
+// absolute position (runs after the scheduler, whose SeqInfo it reads).
+struct RopeParams {
+    const __nv_bfloat16* q;  // [T, H, d]
+    const __nv_bfloat16* k;  // [T, Hk, d]
+    __nv_bfloat16* q_rot;
+    __nv_bfloat16* k_rot;
+    const int32_t* cu_seqlens_q;
+    const SeqInfo* seqs;
+    int total_q, num_seqs, n_heads, n_kv_heads, head_dim;
+    float inv_freq[64];  // inv_freq[i] = 1 / base^(2i / d), i < d/2
+};
+cudaError_t launch_rope(const RopeParams& p, cudaStream_t stream);
+
 
 
 }  // namespace pa

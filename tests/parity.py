@@ -43,17 +43,18 @@ class Guarded:
         return bool((g == GUARD_F32).all())
 
 
-def run_step_gpu(wl, inp, cache_k_dev, cache_v_dev, guarded=True, window=0, block_table=None):
+def run_step_gpu(wl, inp, cache_k_dev, cache_v_dev, guarded=True, window=0, block_table=None, rope_theta=0.0):
     """One launch on the GPU; returns (out, lse) CUDA tensors (and checks guards).
     block_table (CUDA int32) selects the paged cache: the caches are then pools."""
     dev = {k: v.cuda() for k, v in inp.items()}
     T = inp["q"].shape[0]
     out = Guarded((T, wl.n_heads, wl.head_dim), torch.bfloat16)
     lse = Guarded((T, wl.n_heads), torch.float32)
-    if window or block_table is not None:
+    if window or block_table is not None or rope_theta:
         binding.prefill_attn_varlen_ex(dev["q"], dev["k"], dev["v"], dev["cu_seqlens_q"], dev["cu_seqlens_k"],
                                        cache_k_dev, cache_v_dev, dev["cache_offsets"], out.t, lse.t,
-                                       scale=wl.scale, causal=wl.causal, window=window, block_table=block_table)
+                                       scale=wl.scale, causal=wl.causal, window=window, block_table=block_table,
+                                       rope_theta=rope_theta)
     else:
         binding.prefill_attn_varlen(dev["q"], dev["k"], dev["v"], dev["cu_seqlens_q"], dev["cu_seqlens_k"],
                                     cache_k_dev, cache_v_dev, dev["cache_offsets"], out.t, lse.t,
@@ -65,7 +66,8 @@ def run_step_gpu(wl, inp, cache_k_dev, cache_v_dev, guarded=True, window=0, bloc
     return out.t, lse.t
 
 
-def oracle_step(wl, inp, cache_k_bits, cache_v_bits, rows=None, want_cache=True, window=0, block_table=None):
+def oracle_step(wl, inp, cache_k_bits, cache_v_bits, rows=None, want_cache=True, window=0, block_table=None,
+                rope_theta=0.0):
     """The oracle on the same inputs; block_table (CPU int32 [B, max_blocks]) = paged pools."""
     cap, bs = wl.max_cache_len, 0
     if block_table is not None:
@@ -77,7 +79,7 @@ def oracle_step(wl, inp, cache_k_bits, cache_v_bits, rows=None, want_cache=True,
         inp["cu_seqlens_q"].numpy(), inp["cu_seqlens_k"].numpy(), inp["cache_offsets"].numpy(),
         cache_k_bits, cache_v_bits, n_heads=wl.n_heads, n_kv_heads=wl.n_kv_heads, head_dim=wl.head_dim,
         max_cache_len=cap, scale=wl.scale, causal=wl.causal, window=window, rows=rows,
-        want_cache=want_cache, block_table=block_table, block_size=bs)
+        want_cache=want_cache, block_table=block_table, block_size=bs, rope_theta=rope_theta)
 
 
 def compare(out_gpu, lse_gpu, out_ref, lse_ref, rows=None, label=""):
@@ -116,3 +118,22 @@ def sample_rows(step, n_heads, n, seed):
         for t in cand + extra:
             picks.append(int(t) * n_heads + int(rng.integers(0, n_heads)))
     return np.unique(np.array(picks, dtype=np.int64))
+
+
+def compare_rotated_cache(got_bits, ref_bits, label=""):
+    """Cache entries holding a rotated key: GPU (fp32 rotation rounded to bf16)
+    and oracle (fp64 rotation rounded to bf16) may differ by one bf16 ulp where
+    the exact value sits next to a rounding boundary, or, where x cos - y sin
+    cancels, by the fp32 rotation's absolute error (a few 1e-7 * (|x| + |y|):
+    2^-16 covers |x|, |y| up to 8); everything else is bit-identical."""
+    as_f = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).double().numpy()
+    diff = got_bits != ref_bits
+    if not diff.any():
+        return 0
+    g, r = as_f(got_bits[diff]), as_f(ref_bits[diff])
+    assert np.isfinite(g).all(), f"{label}: non-finite rotated key"
+    tol = np.maximum(np.abs(g), np.abs(r)) * 2.0 ** -7 + 2.0 ** -16
+    assert (np.abs(g - r) <= tol).all(), \
+        f"{label}: rotated key off by {np.abs(g - r).max():.3e} (more than one bf16 ulp + 2^-16)"
+    assert diff.mean() < 0.01, f"{label}: {diff.mean():.2%} of cache entries differ"
+    return int(diff.sum())

@@ -83,9 +83,9 @@ def test_python_binding_refuses_cpu_tensors(lib):
 
 
 def _call_ex(lib, window=0, causal=1, struct_size=None, block_table=None, block_size=0, max_blocks=0,
-             num_blocks=0, reserved=0):
+             num_blocks=0, reserved=0, rope_theta=0.0, reserved2=0):
     opts = binding.PaOptions(ctypes.sizeof(binding.PaOptions) if struct_size is None else struct_size, window,
-                             block_table, block_size, max_blocks, num_blocks, reserved)
+                             block_table, block_size, max_blocks, num_blocks, reserved, rope_theta, reserved2)
     return lib.prefill_attn_varlen_ex(16, 32, 48, 64, 80, 96, 112, 128, 144, None, 1, 4, 8, 4, 2, 64,
                                       0.125, causal, ctypes.byref(opts), None)
 
@@ -105,6 +105,10 @@ _PAGED = dict(block_table=256, block_size=8, max_blocks=1, num_blocks=4)
     (dict(_PAGED, num_blocks=0), 1, "num_blocks"),
     (dict(_PAGED, block_table=258), 1, "aligned"),
     (dict(_PAGED, num_blocks=1 << 30), 2, "num_blocks"),
+    (dict(rope_theta=-1.0), 1, "rope_theta"),
+    (dict(rope_theta=float("nan")), 1, "rope_theta"),
+    (dict(rope_theta=float("inf")), 1, "rope_theta"),
+    (dict(reserved2=3), 1, "reserved2"),
 ])
 def test_options_are_checked_before_launch(lib, kw, status, msg):
     assert _call_ex(lib, **kw) == status
@@ -116,5 +120,6 @@ def test_options_layout_matches_header():
     P = binding.PaOptions
     assert [(n, getattr(P, n).offset) for n, _ in P._fields_] == [
         ("struct_size", 0), ("window", 4), ("block_table", 8), ("block_size", 16),
-        ("max_blocks_per_seq", 20), ("num_blocks", 24), ("reserved", 28)]
-    assert ctypes.sizeof(P) == 32
+        ("max_blocks_per_seq", 20), ("num_blocks", 24), ("reserved", 28), ("rope_theta", 32),
+        ("reserved2", 36)]
+    assert ctypes.sizeof(P) == 40
