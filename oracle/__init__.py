@@ -56,7 +56,7 @@ def load_library(path: str):
     P = ctypes.c_void_p
     I = ctypes.c_int
     f.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, I,
-                  ctypes.c_double, I, I, P, I, I, I, ctypes.c_double, P, ctypes.c_int64, I]
+                  ctypes.c_double, I, I, P, I, I, I, ctypes.c_double, I, P, P, P, P, P, ctypes.c_int64, I]
     f.restype = I
     return lib
 
@@ -75,8 +75,8 @@ def _ptr(a: Optional[np.ndarray]):
 def prefill_attention(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_offsets, cache_k, cache_v, *,
                       n_heads: int, n_kv_heads: int, head_dim: int, max_cache_len: int,
                       scale: float, causal: bool = True, window: int = 0, block_table=None, block_size: int = 0,
-                      rope_theta: float = 0.0, rows: Optional[np.ndarray] = None,
-                      want_cache: bool = True, threads: int = 0, lib=None):
+                      rope_theta: float = 0.0, kv_quant: int = 0, cache_k_scale=None, cache_v_scale=None,
+                      rows: Optional[np.ndarray] = None, want_cache: bool = True, threads: int = 0, lib=None):
     """Run the oracle.
 
     q [T,H,d], k/v [T,Hk,d], cache_k/v [B,Hk,cap,d]: uint16 bf16 bit patterns.
@@ -86,6 +86,9 @@ def prefill_attention(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_offsets, cache_
     block_table: optional int32 [B, max_blocks]; then cache_k/v are block pools
     [num_blocks, Hk, block_size, d] and max_cache_len = max_blocks * block_size.
     rope_theta > 0: rotary embedding of the new q/k at their absolute positions.
+    kv_quant = 1: cache_k/v are int8 codes (same shapes) and cache_k_scale /
+    cache_v_scale float32 arrays of shape cache.shape[:-1]; the returned cache
+    images are then (codes, scales) pairs.
 
     Returns (out float64 [T,H,d], lse float64 [T,H], cache_k', cache_v') where
     unselected rows of out/lse are NaN and the cache images are None when
@@ -94,7 +97,16 @@ def prefill_attention(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_offsets, cache_
     lib = lib or _load()
     u16 = lambda a: np.ascontiguousarray(a, dtype=np.uint16)
     i32 = lambda a: np.ascontiguousarray(a, dtype=np.int32)
-    q, k, v, cache_k, cache_v = map(u16, (q, k, v, cache_k, cache_v))
+    q, k, v = map(u16, (q, k, v))
+    if kv_quant:
+        cache_k = np.ascontiguousarray(cache_k, dtype=np.int8)
+        cache_v = np.ascontiguousarray(cache_v, dtype=np.int8)
+        sk = np.ascontiguousarray(cache_k_scale, dtype=np.float32)
+        sv = np.ascontiguousarray(cache_v_scale, dtype=np.float32)
+        assert sk.shape == cache_k.shape[:-1] == sv.shape
+    else:
+        cache_k, cache_v = map(u16, (cache_k, cache_v))
+        sk = sv = None
     cu_q, cu_k, off = map(i32, (cu_seqlens_q, cu_seqlens_k, cache_offsets))
     num_seqs = off.shape[0]
     total_q = int(cu_q[-1]) if num_seqs else 0
@@ -112,15 +124,20 @@ def prefill_attention(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_offsets, cache_
     lse = np.full((total_q, n_heads), np.nan, dtype=np.float64)
     ck = np.empty_like(cache_k) if want_cache else None
     cv = np.empty_like(cache_v) if want_cache else None
+    sk_out = np.empty_like(sk) if (want_cache and kv_quant) else None
+    sv_out = np.empty_like(sv) if (want_cache and kv_quant) else None
     sel = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
     rc = lib.oracle_prefill_attention(
         _ptr(q), _ptr(k), _ptr(v), _ptr(cu_q), _ptr(cu_k), _ptr(off), _ptr(cache_k), _ptr(cache_v),
         _ptr(ck), _ptr(cv), _ptr(out), _ptr(lse),
         num_seqs, max_cache_len, n_heads, n_kv_heads, head_dim, float(scale), int(bool(causal)), int(window),
-        _ptr(bt), int(block_size), int(max_blocks), int(num_blocks), float(rope_theta), _ptr(sel), 0 if sel is None else sel.shape[0], int(threads))
+        _ptr(bt), int(block_size), int(max_blocks), int(num_blocks), float(rope_theta),
+        int(kv_quant), _ptr(sk), _ptr(sv), _ptr(sk_out), _ptr(sv_out), _ptr(sel), 0 if sel is None else sel.shape[0], int(threads))
     if rc != 0:
         raise ValueError(f"oracle: {ERRORS.get(rc, rc)}")
     if want_cache:
         ck = ck.reshape(cache_k.shape)
         cv = cv.reshape(cache_v.shape)
+        if kv_quant:
+            ck, cv = (ck, sk_out), (cv, sv_out)
     return out, lse, ck, cv

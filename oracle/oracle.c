@@ -54,6 +54,15 @@
  *    page's formula computes them; cos/sin and the rotation are fp64.  The
  *    cache receives the rotated key rounded to bf16 (nearest, ties to even);
  *    cached prefix keys are used as stored (they were rotated when written).
+ *  - Quantised cache (optional, kv_quant = 1; [zskr] §4.3: INT8 keys and values,
+ *    queries at full precision, per-token granularity among the page's
+ *    options): each cached (token, KV head) row is int8 codes plus one fp32
+ *    scale; the value it stands for is code * scale.  A new row x (its bf16
+ *    values; the rotated key rounded to bf16 when RoPE is on) is stored as
+ *    scale = max|x| / 127 and code = nearest integer (ties to even) of x / scale,
+ *    all in fp32 (the precision the codes are decided in on the GPU too); a
+ *    zero row is stored as scale 0, codes 0.  The prefix is read dequantised;
+ *    the chunk's own keys and values are used at full precision.
  *
  * Inputs q, k, v and the caches are bf16 bit patterns (uint16); each value is
  * widened exactly to fp64 before any arithmetic.  Outputs are fp64:
@@ -82,7 +91,7 @@ static double bf16_to_double(uint16_t bits)
 
 typedef struct {
     const uint16_t *q, *k, *v;            /* [T][H][d], [T][Hk][d], [T][Hk][d] */
-    const uint16_t *cache_k, *cache_v;     /* [B][Hk][cap][d], read for the prefix */
+    const void *cache_k, *cache_v;         /* [B][Hk][cap][d] bf16 (or int8 codes), read for the prefix */
     const int32_t *cu_q, *off;
     double *out, *lse;
     int num_seqs, cap, n_heads, n_kv_heads, d;
@@ -92,6 +101,8 @@ typedef struct {
     const int32_t *block_table; /* paged cache: [num_seqs][max_blocks]; NULL: contiguous slots */
     int block_size, max_blocks, num_blocks;
     const double *rope_cos, *rope_sin; /* [max_cache_len][d/2]; NULL: no rotary embedding */
+    int kv_quant;                      /* 1: int8 codes + fp32 per-row scales */
+    const float *scale_k, *scale_v;    /* [B][Hk][cap] (or the pool's rows) */
 } problem;
 
 /* The rotation of a head vector x (fp64, length d) to absolute position pos. */
@@ -134,25 +145,32 @@ static size_t cache_row(const problem *pb, int b, int kvh, int pos)
     return ((size_t)b * pb->n_kv_heads + kvh) * pb->cap + (size_t)pos;
 }
 
-/* Key j of sequence b, KV head kvh: the cached prefix, then the new tokens. */
-static const uint16_t *key_row(const problem *pb, const uint16_t *cache, const uint16_t *fresh,
-                               int b, int kvh, int j)
+/* Key (which = 0) or value (which = 1) j of sequence b, KV head kvh, widened
+ * to fp64 in `dst`: the cached prefix (dequantised when the cache is int8),
+ * then the new tokens (rotated to their position when RoPE is on and
+ * `rotate` is set). */
+static void load_key(const problem *pb, int which, int b, int kvh, int j, int rotate, double *dst)
 {
-    int P = pb->off[b];
-    if (j < P)
-        return cache + cache_row(pb, b, kvh, j) * pb->d;
-    return fresh + ((size_t)(pb->cu_q[b] + (j - P)) * pb->n_kv_heads + kvh) * pb->d;
-}
-
-/* Key (or value) row j of sequence b widened to fp64 in `dst`; new keys are
- * rotated to their position when the rotary embedding is on. */
-static void load_key(const problem *pb, const uint16_t *cache, const uint16_t *fresh, int b, int kvh, int j,
-                     int rotate, double *dst)
-{
-    const uint16_t *r = key_row(pb, cache, fresh, b, kvh, j);
-    for (int e = 0; e < pb->d; ++e)
+    const int d = pb->d;
+    const int P = pb->off[b];
+    if (j < P) {
+        const size_t row = cache_row(pb, b, kvh, j);
+        if (pb->kv_quant) {
+            const int8_t *codes = (const int8_t *)(which ? pb->cache_v : pb->cache_k) + row * d;
+            const double sc = (double)(which ? pb->scale_v : pb->scale_k)[row];
+            for (int e = 0; e < d; ++e)
+                dst[e] = (double)codes[e] * sc;
+        } else {
+            const uint16_t *r = (const uint16_t *)(which ? pb->cache_v : pb->cache_k) + row * d;
+            for (int e = 0; e < d; ++e)
+                dst[e] = bf16_to_double(r[e]);
+        }
+        return;
+    }
+    const uint16_t *r = (which ? pb->v : pb->k) + ((size_t)(pb->cu_q[b] + (j - P)) * pb->n_kv_heads + kvh) * d;
+    for (int e = 0; e < d; ++e)
         dst[e] = bf16_to_double(r[e]);
-    if (rotate && pb->rope_cos && j >= pb->off[b])
+    if (rotate && pb->rope_cos)
         rope_rotate(pb, j, dst);
 }
 
@@ -177,7 +195,7 @@ static void attend_row(const problem *pb, int b, int i, int h, double *s, double
         rope_rotate(pb, P + i, qv);
     double m = -INFINITY;
     for (int j = first; j <= last; ++j) {
-        load_key(pb, pb->cache_k, pb->k, b, kvh, j, 1, kv);
+        load_key(pb, 0, b, kvh, j, 1, kv);
         double dot = 0.0;
         for (int e = 0; e < d; ++e)
             dot += qv[e] * kv[e];
@@ -194,9 +212,9 @@ static void attend_row(const problem *pb, int b, int i, int h, double *s, double
         orow[e] = 0.0;
     for (int j = first; j <= last; ++j) {
         const double w = exp(s[j] - m) / Z;
-        const uint16_t *vr = key_row(pb, pb->cache_v, pb->v, b, kvh, j);
+        load_key(pb, 1, b, kvh, j, 0, kv);
         for (int e = 0; e < d; ++e)
-            orow[e] += w * bf16_to_double(vr[e]);
+            orow[e] += w * kv[e];
     }
     if (pb->lse)
         pb->lse[t * pb->n_heads + h] = m + log(Z);
@@ -228,6 +246,10 @@ static int owner(const int32_t *cu_q, int num_seqs, int64_t t)
  *
  * rope_theta > 0 turns the rotary embedding on (head_dim must be even).
  *
+ * kv_quant = 1: the caches are int8 codes and scale_k/scale_v (fp32, one per
+ * cache row) their scales; scale_k_out/scale_v_out receive the scales of the
+ * cache image (may be NULL when the cache images are).
+ *
  * rows: optional list of (t * n_heads + h) query rows to compute; NULL = all.
  * Only the selected rows of out/lse are written.  The cache image
  * (cache_k_out/cache_v_out, may be NULL) is written in full: a copy of the
@@ -236,19 +258,21 @@ static int owner(const int32_t *cu_q, int num_seqs, int64_t t)
 int oracle_prefill_attention(
     const uint16_t *q, const uint16_t *k, const uint16_t *v,
     const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, const int32_t *cache_offsets,
-    const uint16_t *cache_k, const uint16_t *cache_v,
-    uint16_t *cache_k_out, uint16_t *cache_v_out,
+    const void *cache_k, const void *cache_v,
+    void *cache_k_out, void *cache_v_out,
     double *out, double *lse,
     int num_seqs, int max_cache_len, int n_heads, int n_kv_heads, int head_dim,
     double scale, int causal, int window,
     const int32_t *block_table, int block_size, int max_blocks, int num_blocks,
     double rope_theta,
+    int kv_quant, const float *scale_k, const float *scale_v, float *scale_k_out, float *scale_v_out,
     const int64_t *rows, int64_t n_rows, int n_threads)
 {
     if (window < 0 || (window > 0 && !causal))
         return -7;
     if (num_seqs < 0 || max_cache_len < 0 || n_heads <= 0 || n_kv_heads <= 0 || head_dim <= 0 ||
-        n_heads % n_kv_heads != 0 || rope_theta < 0 || (rope_theta > 0 && head_dim % 2 != 0))
+        n_heads % n_kv_heads != 0 || rope_theta < 0 || (rope_theta > 0 && head_dim % 2 != 0) ||
+        kv_quant < 0 || kv_quant > 1 || (kv_quant && (!scale_k || !scale_v)))
         return -1;
     if (num_seqs > 0 && cu_seqlens_q[0] != 0)
         return -2;
@@ -273,7 +297,7 @@ int oracle_prefill_attention(
 
     problem pb = {q, k, v, cache_k, cache_v, cu_seqlens_q, cache_offsets, out, lse,
                   num_seqs, max_cache_len, n_heads, n_kv_heads, head_dim, scale, causal, window,
-                  block_table, block_size, max_blocks, num_blocks, NULL, NULL};
+                  block_table, block_size, max_blocks, num_blocks, NULL, NULL, kv_quant, scale_k, scale_v};
 
     /* cos/sin of every position's angles: inv_freq and m * inv_freq in fp32 */
     double *rope_tab = NULL;
@@ -337,33 +361,65 @@ int oracle_prefill_attention(
     }
 
     /* The cache image: everything as it was, plus the new tokens at P + i. */
-    const size_t cache_elems = block_table ? (size_t)num_blocks * n_kv_heads * block_size * head_dim
-                                           : (size_t)num_seqs * n_kv_heads * max_cache_len * head_dim;
+    const size_t cache_rows = block_table ? (size_t)num_blocks * n_kv_heads * block_size
+                                          : (size_t)num_seqs * n_kv_heads * max_cache_len;
+    const size_t elem = kv_quant ? sizeof(int8_t) : sizeof(uint16_t);
     for (int c = 0; c < 2; ++c) {
-        uint16_t *dst = c == 0 ? cache_k_out : cache_v_out;
-        const uint16_t *src = c == 0 ? cache_k : cache_v;
+        uint8_t *dst = (uint8_t *)(c == 0 ? cache_k_out : cache_v_out);
+        const uint8_t *src = (const uint8_t *)(c == 0 ? cache_k : cache_v);
+        float *sdst = c == 0 ? scale_k_out : scale_v_out;
+        const float *ssrc = c == 0 ? scale_k : scale_v;
         const uint16_t *fresh = c == 0 ? k : v;
         if (!dst)
             continue;
         if (dst != src)
-            memcpy(dst, src, cache_elems * sizeof(uint16_t));
+            memcpy(dst, src, cache_rows * head_dim * elem);
+        if (kv_quant && sdst && sdst != ssrc)
+            memcpy(sdst, ssrc, cache_rows * sizeof(float));
         for (int b = 0; b < num_seqs; ++b) {
             const int P = cache_offsets[b];
             const int n = cu_seqlens_q[b + 1] - cu_seqlens_q[b];
             for (int kvh = 0; kvh < n_kv_heads; ++kvh)
                 for (int i = 0; i < n; ++i) {
-                    uint16_t *row = dst + cache_row(&pb, b, kvh, P + i) * head_dim;
+                    const size_t row = cache_row(&pb, b, kvh, P + i);
                     const uint16_t *in = fresh + ((size_t)(cu_seqlens_q[b] + i) * n_kv_heads + kvh) * head_dim;
+                    uint16_t x[head_dim]; /* the row as bf16: rotated and rounded when RoPE is on */
                     if (c == 0 && pb.rope_cos) {
-                        double x[head_dim];
+                        double xr[head_dim];
                         for (int e = 0; e < head_dim; ++e)
-                            x[e] = bf16_to_double(in[e]);
-                        rope_rotate(&pb, P + i, x);
+                            xr[e] = bf16_to_double(in[e]);
+                        rope_rotate(&pb, P + i, xr);
                         for (int e = 0; e < head_dim; ++e)
-                            row[e] = double_to_bf16(x[e]);
+                            x[e] = double_to_bf16(xr[e]);
                     } else {
-                        memcpy(row, in, (size_t)head_dim * sizeof(uint16_t));
+                        memcpy(x, in, (size_t)head_dim * sizeof(uint16_t));
                     }
+                    if (!kv_quant) {
+                        memcpy(dst + row * head_dim * elem, x, (size_t)head_dim * sizeof(uint16_t));
+                        continue;
+                    }
+                    /* int8 codes with one fp32 scale per row, decided in fp32 */
+                    float amax = 0.0f;
+                    for (int e = 0; e < head_dim; ++e) {
+                        const float a = fabsf((float)bf16_to_double(x[e]));
+                        if (a > amax)
+                            amax = a;
+                    }
+                    const float sc = amax / 127.0f;
+                    int8_t *codes = (int8_t *)dst + row * head_dim;
+                    for (int e = 0; e < head_dim; ++e) {
+                        float qv = 0.0f;
+                        if (sc > 0.0f) {
+                            qv = rintf((float)bf16_to_double(x[e]) / sc);
+                            if (qv > 127.0f)
+                                qv = 127.0f;
+                            if (qv < -127.0f)
+                                qv = -127.0f;
+                        }
+                        codes[e] = (int8_t)qv;
+                    }
+                    if (sdst)
+                        sdst[row] = sc;
                 }
         }
     }

@@ -28,14 +28,13 @@ MUTATIONS = {
                              "P + i - pb->window + 2 > 0) ? P + i - pb->window + 2 : 0;"),
     "window_ignores_prefix": ("P + i - pb->window + 1 > 0) ? P + i - pb->window + 1 : 0;",
                               "i - pb->window + 1 > 0) ? P + i - pb->window + 1 : P;"),
-    "value_read_from_keys": ("key_row(pb, pb->cache_v, pb->v, b, kvh, j)",
-                             "key_row(pb, pb->cache_k, pb->k, b, kvh, j)"),
+    "value_read_from_keys": ("load_key(pb, 1, b, kvh, j, 0, kv);", "load_key(pb, 0, b, kvh, j, 0, kv);"),
     "lse_without_max": ("pb->lse[t * pb->n_heads + h] = m + log(Z);",
                         "pb->lse[t * pb->n_heads + h] = log(Z);"),
-    "cache_written_at_zero": ("uint16_t *row = dst + cache_row(&pb, b, kvh, P + i) * head_dim;",
-                              "uint16_t *row = dst + cache_row(&pb, b, kvh, i) * head_dim;"),
-    "prefix_keys_shifted": ("return cache + cache_row(pb, b, kvh, j) * pb->d;",
-                            "return cache + cache_row(pb, b, kvh, j > 0 ? j - 1 : 0) * pb->d;"),
+    "cache_written_at_zero": ("const size_t row = cache_row(&pb, b, kvh, P + i);",
+                              "const size_t row = cache_row(&pb, b, kvh, i);"),
+    "prefix_keys_shifted": ("const size_t row = cache_row(pb, b, kvh, j);",
+                            "const size_t row = cache_row(pb, b, kvh, j > 0 ? j - 1 : 0);"),
     # paged cache (every mutant stays inside the pool: the pin tables fill every entry)
     "paged_row_off_by_one": ("(size_t)(pos % pb->block_size);", "(size_t)((pos + 1) % pb->block_size);"),
     "paged_pool_heads_outer": ("((size_t)blk * pb->n_kv_heads + kvh) * pb->block_size",
@@ -56,6 +55,12 @@ MUTATIONS = {
     "rope_query_position_without_prefix": ("rope_rotate(pb, P + i, qv);", "rope_rotate(pb, i, qv);"),
     "rope_key_position_without_prefix": ("rope_rotate(pb, j, dst);", "rope_rotate(pb, j - pb->off[b], dst);"),
     "rope_cache_keeps_unrotated_key": ("if (c == 0 && pb.rope_cos) {", "if (0 && pb.rope_cos) {"),
+    # int8 cache
+    "quant_scale_over_128": ("const float sc = amax / 127.0f;", "const float sc = amax / 128.0f;"),
+    "quant_truncates": ("qv = rintf((float)bf16_to_double(x[e]) / sc);", "qv = truncf((float)bf16_to_double(x[e]) / sc);"),
+    "quant_dequant_drops_scale": ("dst[e] = (double)codes[e] * sc;", "dst[e] = (double)codes[e];"),
+    "quant_scale_from_first_element": ("if (a > amax)\n                            amax = a;",
+                                       "if (e == 0)\n                            amax = a;"),
 }
 
 PIN_TESTS = [
@@ -78,6 +83,9 @@ PIN_TESTS = [
     pins.test_rope_relative_position_invariance,
     pins.test_rope_chunked_equals_one_shot,
     pins.test_rope_matches_complex_rotation_and_sdpa,
+    pins.test_quant_codes_closed_form,
+    pins.test_quant_rounding_bound_and_extremes,
+    pins.test_quant_prefix_read_matches_sdpa_on_dequantised_cache,
 ]
 
 

@@ -674,3 +674,91 @@ def _sdpa_reference_f64(wl, ck, cv, q, k, v, inp):
                                                attn_mask=mask[None], scale=wl.scale)
             out[cu[b]:cu[b + 1], h] = o[0]
     return out.numpy()
+
+
+# ------------------------------------------------------------ int8 cache ---
+# [zskr] §4.3: INT8 keys and values, queries at full precision, per-token
+# granularity among the page's options.  Reading taken: symmetric, one fp32
+# scale per (token, KV head) row, scale = max|x| / 127, code = nearest integer
+# (ties to even) of x / scale, value = code * scale.
+
+def _q8_case(oracle_mod, wl, inp, ck8=None, cs=None, **kw):
+    B, Hk, cap, d = wl.num_seqs, wl.n_kv_heads, wl.max_cache_len, wl.head_dim
+    if ck8 is None:
+        ck8 = (np.zeros((B, Hk, cap, d), np.int8), np.zeros((B, Hk, cap, d), np.int8))
+        cs = (np.zeros((B, Hk, cap), np.float32), np.zeros((B, Hk, cap), np.float32))
+    return oracle_mod.prefill_attention(
+        W.bf16_bits(inp["q"]), W.bf16_bits(inp["k"]), W.bf16_bits(inp["v"]),
+        inp["cu_seqlens_q"].numpy(), inp["cu_seqlens_k"].numpy(), inp["cache_offsets"].numpy(),
+        ck8[0], ck8[1], n_heads=wl.n_heads, n_kv_heads=wl.n_kv_heads, head_dim=d, max_cache_len=cap,
+        scale=wl.scale, causal=wl.causal, kv_quant=1, cache_k_scale=cs[0], cache_v_scale=cs[1], **kw)
+
+
+def test_quant_codes_closed_form(oracle_mod):
+    """A key row whose largest magnitude is 127 has scale 1 exactly, so its codes
+    are the values rounded to the nearest integer, ties to even: 2.5 -> 2,
+    3.5 -> 4, -2.5 -> -2, 0.5 -> 0, 1.5 -> 2; a value row scaled by 2^-3 keeps
+    the same codes with scale 2^-3; an all-zero row is scale 0, codes 0."""
+    d = 32
+    wl = _custom("q8cf", 2, 2, d, [1], [0], cap=2)
+    _, _, (inp,) = W.make_inputs(wl)
+    vals = torch.zeros(d)
+    vals[:7] = torch.tensor([127.0, 2.5, 3.5, -2.5, 0.5, 1.5, -127.0])
+    k = torch.zeros(1, 2, d, dtype=torch.bfloat16)
+    k[0, 0] = vals
+    v = torch.zeros(1, 2, d, dtype=torch.bfloat16)
+    v[0, 0] = vals / 8
+    _, _, (ck, sk), (cv, sv) = _q8_case(oracle_mod, wl, dict(inp, k=k, v=v))
+    exp = np.zeros(d, np.int8)
+    exp[:7] = [127, 2, 4, -2, 0, 2, -127]
+    assert np.array_equal(ck[0, 0, 0], exp) and sk[0, 0, 0] == 1.0
+    assert np.array_equal(cv[0, 0, 0], exp) and sv[0, 0, 0] == np.float32(1 / 8)
+    assert not ck[0, 1, 0].any() and sk[0, 1, 0] == 0.0       # zero row
+    assert not ck[0, :, 1].any() and sk[0, 0, 1] == 0.0       # untouched row
+
+
+def test_quant_rounding_bound_and_extremes(oracle_mod):
+    """Every stored row: |x - code * scale| <= scale / 2 (nearest rounding), the
+    largest |x| maps to a code of magnitude 127, and |code| <= 127."""
+    wl = W.random_workload(90, head_dim=64, group=2, max_len=40, max_prefix=0)
+    _, _, (inp,) = W.make_inputs(wl)
+    _, _, (ck, sk), (cv, sv) = _q8_case(oracle_mod, wl, inp)
+    cu = inp["cu_seqlens_q"].tolist()
+    for b in range(wl.num_seqs):
+        for i in range(cu[b + 1] - cu[b]):
+            for codes, scales, src in ((ck, sk, inp["k"]), (cv, sv, inp["v"])):
+                x = src[cu[b] + i].double().numpy()  # [Hk, d]
+                c, sc = codes[b, :, i].astype(np.float64), scales[b, :, i].astype(np.float64)
+                # x / scale is an fp32 quotient (relative error 2^-24 on values up to 127)
+                assert (np.abs(x - c * sc[:, None]) <= sc[:, None] * (0.5 + 127 * 2.0 ** -23)).all()
+                assert (np.abs(c).max(axis=1) == 127).all()
+                assert np.allclose(sc, np.abs(x).max(axis=1) / 127, rtol=1e-7)
+
+
+def test_quant_prefix_read_matches_sdpa_on_dequantised_cache(oracle_mod):
+    """A chunk over an int8 prefix: SDPA (float64) on the cache written out as
+    code * scale, with the chunk's own keys/values at full precision."""
+    wl = W.random_workload(91, head_dim=64, group=4, max_len=40, max_prefix=80, allow_empty=False)
+    _, _, (inp,) = W.make_inputs(wl)
+    rng = np.random.default_rng(3)
+    shape = (wl.num_seqs, wl.n_kv_heads, wl.max_cache_len, wl.head_dim)
+    codes = (rng.integers(-127, 128, size=shape).astype(np.int8), rng.integers(-127, 128, size=shape).astype(np.int8))
+    scales = (rng.uniform(0.001, 0.03, size=shape[:-1]).astype(np.float32),
+              rng.uniform(0.001, 0.03, size=shape[:-1]).astype(np.float32))
+    out, _, _, _ = _q8_case(oracle_mod, wl, inp, codes, scales)
+    deq = [torch.from_numpy(c.astype(np.float64) * s.astype(np.float64)[..., None]) for c, s in zip(codes, scales)]
+    ref = _sdpa_reference_f64(wl, deq[0], deq[1], torch.from_numpy(f64(inp["q"])),
+                              torch.from_numpy(f64(inp["k"])), f64(inp["v"]), inp)
+    assert np.nanmax(np.abs(out - ref)) < 1e-12
+
+
+def test_quant_zero_cache_rows_read_as_zero(oracle_mod):
+    """Prefix rows with scale 0 are zero keys: every such score is 0."""
+    wl = _custom("q8z", 2, 2, 32, [1], [5], cap=6)
+    _, _, (inp,) = W.make_inputs(wl)
+    out, lse, _, _ = _q8_case(oracle_mod, wl, inp)  # all-zero codes and scales
+    s_new = wl.scale * float((inp["q"][0].double() * inp["k"][0].double()).sum(-1)[0])
+    # 5 zero scores and one score s_new: lse = ln(5 + e^s_new); out = e^s_new v / (5 + e^s_new)
+    assert lse[0, 0] == pytest.approx(math.log(5 + math.exp(s_new)), abs=1e-12)
+    w = math.exp(s_new) / (5 + math.exp(s_new))
+    assert np.allclose(out[0, 0], w * f64(inp["v"][0, 0]), atol=1e-12)
