@@ -52,8 +52,10 @@
  *    in the rotate-half pairing of the Llama models the page names (dimension i
  *    pairs with i + head_dim/2).  inv_freq and the angles are fp32, as the
  *    page's formula computes them; cos/sin and the rotation are fp64.  The
- *    cache receives the rotated key rounded to bf16 (nearest, ties to even);
- *    cached prefix keys are used as stored (they were rotated when written).
+ *    rotated query and key are model-dtype tensors (the page discusses RoPE for
+ *    FP16/BF16 models): both are rounded to bf16 (nearest, ties to even), and
+ *    that rotated key is what attention uses and what the cache receives.
+ *    Cached prefix keys are used as stored (they were rotated when written).
  *  - Quantised cache (optional, kv_quant = 1; [zskr] §4.3: INT8 keys and values,
  *    queries at full precision, per-token granularity among the page's
  *    options): each cached (token, KV head) row is int8 codes plus one fp32
@@ -118,6 +120,16 @@ static void rope_rotate(const problem *pb, int pos, double *x)
     }
 }
 
+static uint16_t double_to_bf16(double x);
+
+/* The rotated head vector as the model-dtype (bf16) tensor it is. */
+static void rope_rotate_bf16(const problem *pb, int pos, double *x)
+{
+    rope_rotate(pb, pos, x);
+    for (int e = 0; e < pb->d; ++e)
+        x[e] = bf16_to_double(double_to_bf16(x[e]));
+}
+
 /* Nearest bf16 (ties to even) of a finite double, as a bit pattern. */
 static uint16_t double_to_bf16(double x)
 {
@@ -171,7 +183,7 @@ static void load_key(const problem *pb, int which, int b, int kvh, int j, int ro
     for (int e = 0; e < d; ++e)
         dst[e] = bf16_to_double(r[e]);
     if (rotate && pb->rope_cos)
-        rope_rotate(pb, j, dst);
+        rope_rotate_bf16(pb, j, dst);
 }
 
 /* One query row (sequence b, new token i, head h).  `s` has room for P+n
@@ -192,7 +204,7 @@ static void attend_row(const problem *pb, int b, int i, int h, double *s, double
     for (int e = 0; e < d; ++e)
         qv[e] = bf16_to_double(qrow[e]);
     if (pb->rope_cos)
-        rope_rotate(pb, P + i, qv);
+        rope_rotate_bf16(pb, P + i, qv);
     double m = -INFINITY;
     for (int j = first; j <= last; ++j) {
         load_key(pb, 0, b, kvh, j, 1, kv);

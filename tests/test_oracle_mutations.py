@@ -52,8 +52,8 @@ MUTATIONS = {
         x[i + half] = b * c[i] - a * sn[i];"""),
     "rope_frequency_exponent_halved": ("powf((float)rope_theta, (float)(2 * i) / (float)head_dim)",
                                        "powf((float)rope_theta, (float)(i) / (float)head_dim)"),
-    "rope_query_position_without_prefix": ("rope_rotate(pb, P + i, qv);", "rope_rotate(pb, i, qv);"),
-    "rope_key_position_without_prefix": ("rope_rotate(pb, j, dst);", "rope_rotate(pb, j - pb->off[b], dst);"),
+    "rope_query_position_without_prefix": ("rope_rotate_bf16(pb, P + i, qv);", "rope_rotate_bf16(pb, i, qv);"),
+    "rope_key_position_without_prefix": ("rope_rotate_bf16(pb, j, dst);", "rope_rotate_bf16(pb, j - pb->off[b], dst);"),
     "rope_cache_keeps_unrotated_key": ("if (c == 0 && pb.rope_cos) {", "if (0 && pb.rope_cos) {"),
     # int8 cache
     "quant_scale_over_128": ("const float sc = amax / 127.0f;", "const float sc = amax / 128.0f;"),

@@ -582,7 +582,7 @@ def test_rope_relative_position_invariance(oracle_mod):
     """With a window of 2 the second of two new tokens sees exactly those two:
     its scores then depend on positions only through their difference, so moving
     both tokens from positions 0, 1 to 777, 778 leaves its output unchanged
-    (up to the fp32 rounding of the larger angles)."""
+    (up to the bf16 rounding of the rotated vectors)."""
     H, Hk, d = 4, 2, 64
     outs = []
     for P in (0, 777):
@@ -593,19 +593,21 @@ def test_rope_relative_position_invariance(oracle_mod):
         out, lse, _, _ = run_oracle(oracle_mod, wl, ck.nan_to_num(0.0), cv.nan_to_num(0.0), inp,
                                     window=2, rope_theta=10000.0)
         outs.append((out[1], lse[1]))
-    assert np.allclose(outs[0][0], outs[1][0], atol=2e-4)
-    assert np.allclose(outs[0][1], outs[1][1], atol=2e-4)
+    # the rotated q and k are rounded to bf16 at each position (|ds| <= scale *
+    # 2^-8 * |q| |k| ~ 2e-2 here): equal up to that rounding
+    assert np.allclose(outs[0][0], outs[1][0], atol=1e-2)
+    assert np.allclose(outs[0][1], outs[1][1], atol=1e-2)
     # and the rotation matters: without it the two positions are not equivalent to
     # a plain (unrotated) run
     wl0 = _custom("roperel", H, Hk, d, [2], [0], cap=2)
     ck, cv, (inp,) = W.make_inputs(_custom("roperel", H, Hk, d, [2], [0], cap=779, seed=11))
     plain, _, _, _ = run_oracle(oracle_mod, wl0, ck[:, :, :2].contiguous(), cv[:, :, :2].contiguous(), inp, window=2)
-    assert np.abs(plain[1] - outs[0][0]).max() > 1e-3
+    assert np.abs(plain[1] - outs[0][0]).max() > 5e-2
 
 
 def test_rope_chunked_equals_one_shot(oracle_mod):
-    """Chunks read the earlier chunks' rotated keys back from the cache (as bf16):
-    the result matches one launch up to that rounding."""
+    """Chunks read the earlier chunks' rotated keys back from the cache: the same
+    bf16 tensors one launch attends to, so the results are identical, bit for bit."""
     H, Hk, d, n, c = 4, 2, 64, 240, 80
     one = _custom("ropeone", H, Hk, d, [n], [0], cap=n)
     ck, cv, (inp,) = W.make_inputs(one)
@@ -620,7 +622,7 @@ def test_rope_chunked_equals_one_shot(oracle_mod):
             cur_k, cur_v, n_heads=H, n_kv_heads=Hk, head_dim=d, max_cache_len=n, scale=one.scale,
             rope_theta=10000.0)
         outs.append(o)
-    assert np.abs(np.concatenate(outs) - out1).max() < 2e-2
+    assert np.array_equal(np.concatenate(outs), out1)
     assert np.array_equal(cur_k, ck1)  # the same rotated keys, rounded the same way
 
 
@@ -640,15 +642,17 @@ def test_rope_matches_complex_rotation_and_sdpa(oracle_mod):
     ang = (pos[:, None] * inv[None, :]).astype(np.float32).astype(np.float64)  # fp32 angles
     rot = np.exp(1j * ang)[:, None, :]
 
-    def apply(x):
+    def apply(x):  # rotate, then round to the model dtype (bf16)
         x = f64(x)
         z = (x[..., :half] + 1j * x[..., half:]) * rot
-        return torch.from_numpy(np.concatenate([z.real, z.imag], -1))
+        return torch.from_numpy(np.concatenate([z.real, z.imag], -1)).to(torch.bfloat16).double()
     qr, kr = apply(inp["q"]), apply(inp["k"])
     ref = _sdpa_reference_f64(wl, ck, cv, qr, kr, f64(inp["v"]), inp)
     # numpy's fp32 power and the C library's powf may differ in the last bit of
-    # inv_freq, which moves an angle at position m by about m * 6e-8
-    assert np.nanmax(np.abs(out - ref)) < 1e-5
+    # inv_freq, which moves an angle at position m by about m * 6e-8 and can flip
+    # the bf16 rounding of a rotated element next to a tie
+    err = np.abs(out - ref)
+    assert np.nanmax(err) < 2e-3 and np.nanmean(err) < 1e-5
 
 
 def _sdpa_reference_f64(wl, ck, cv, q, k, v, inp):
