@@ -234,7 +234,14 @@ def run_ours(args, ws, rank, local):
     inputs = W.make_inputs(wl, sentinel=False)
     cache_k, cache_v, steps = inputs
     table_d = None
-    if args.paged:
+    sk_d = sv_d = None
+    if args.kv_quant:
+        # the same workload over an int8 cache (codes + fp32 row scales)
+        codes_k, scales_k, codes_v, scales_v = W.make_q8_cache(wl, torch.Generator().manual_seed(wl.seed),
+                                                               sentinel=False)
+        ck, sk_d, cv, sv_d = codes_k.cuda(), scales_k.cuda(), codes_v.cuda(), scales_v.cuda()
+        del codes_k, codes_v
+    elif args.paged:
         # the same workload over a paged cache: a block pool + per-sequence block table
         table, pool_k, pool_v = W.make_paged_cache(wl, args.paged, torch.Generator().manual_seed(wl.seed),
                                                    sentinel=False)
@@ -248,10 +255,11 @@ def run_ours(args, ws, rank, local):
     stream = torch.cuda.current_stream()
 
     def call(d, o, l):
-        if args.window or args.paged or args.rope:
+        if args.window or args.paged or args.rope or args.kv_quant:
             binding.prefill_attn_varlen_ex(d["q"], d["k"], d["v"], d["cu_seqlens_q"], d["cu_seqlens_k"], ck, cv,
                                            d["cache_offsets"], o, l, scale=wl.scale, causal=wl.causal,
-                                           window=args.window, block_table=table_d, rope_theta=args.rope)
+                                           window=args.window, block_table=table_d, rope_theta=args.rope,
+                                           cache_k_scale=sk_d, cache_v_scale=sv_d)
         else:
             binding.prefill_attn_varlen(d["q"], d["k"], d["v"], d["cu_seqlens_q"], d["cu_seqlens_k"], ck, cv,
                                         d["cache_offsets"], o, l, scale=wl.scale, causal=wl.causal)
@@ -313,7 +321,7 @@ def run_ours(args, ws, rank, local):
     achieved = fl_tot / (t_tot * 1e-3) / 1e12
     traffic = None
     variant = (f"_window{args.window}" if args.window else "") + (f"_paged{args.paged}" if args.paged else "") \
-        + ("_rope" if args.rope else "")
+        + ("_rope" if args.rope else "") + ("_int8kv" if args.kv_quant else "")
     tpath = os.path.join(ROOT, "profiles", f"traffic_{wl.name}{variant}.json")
     if os.path.exists(tpath):
         rec = json.load(open(tpath))
@@ -355,9 +363,11 @@ def run_ours(args, ws, rank, local):
         "tokens_per_s": round(tokens_s, 1),
         "pct_of_bf16_peak": round(100 * value / ws / peak, 2),
         "config": {"workload": wl.name + (f"+window{args.window}" if args.window else "")
-                   + (f"+paged{args.paged}" if args.paged else "") + (f"+rope{args.rope:g}" if args.rope else ""),
+                   + (f"+paged{args.paged}" if args.paged else "") + (f"+rope{args.rope:g}" if args.rope else "")
+                   + ("+int8kv" if args.kv_quant else ""),
                    "launches_per_step": n_launch, "window": args.window, "num_seqs": wl.num_seqs,
-                   "kv_cache": f"paged, {args.paged}-token blocks" if args.paged else "contiguous per sequence",
+                   "kv_cache": (f"paged, {args.paged}-token blocks" if args.paged else "contiguous per sequence")
+                   + (", int8 codes + fp32 row scales" if args.kv_quant else ", bf16"),
                    "rope_theta": args.rope,
                    "tokens_per_step": wl.tokens(), "n_heads": wl.n_heads, "n_kv_heads": wl.n_kv_heads,
                    "head_dim": wl.head_dim, "causal": wl.causal, "causal_flops_per_step": flops_step,
@@ -429,6 +439,7 @@ def main():
                                                              "the visible pairs)")
     ap.add_argument("--paged", type=int, default=0, help="block size of a paged KV cache (0: contiguous cache)")
     ap.add_argument("--rope", type=float, default=0.0, help="rotary embedding base (0: none)")
+    ap.add_argument("--kv-quant", action="store_true", help="int8 KV cache with per-token fp32 scales")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=25.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--ref-rows", type=int, default=128, help="oracle rows per reference step")

@@ -170,6 +170,23 @@ typedef struct pa_options {
      * bytes more).  The call then runs three kernels instead of two. */
     float rope_theta;
     int32_t reserved2;  /* must be 0 */
+    /* Quantised KV cache ("大模型推理优化：Prefill、Decode与KV Cache的工程实践"
+     * (zskr.cn) §4.3: INT8 keys and values, queries at full precision,
+     * per-token granularity).  0 = bf16 cache.  1 = int8: cache_k and cache_v
+     * are int8 [num_seqs, n_kv_heads, max_cache_len, head_dim] codes and
+     * cache_k_scale / cache_v_scale fp32 [num_seqs, n_kv_heads, max_cache_len]
+     * (4-byte aligned) hold one scale per cached (token, KV head) row; the row
+     * stands for code * scale.  Each new row x (the rotated key when RoPE is on,
+     * rounded to bf16) is written as scale = max|x| / 127 and code = the
+     * nearest integer, ties to even, of x / scale (fp32 division), clamped to
+     * +-127; an all-zero row is scale 0, codes 0.  The cached prefix is read
+     * dequantised (code * scale, rounded to bf16 for the tensor cores); the
+     * chunk's own keys and values are used at full precision.  Not combined
+     * with block_table (PA_ERR_UNSUPPORTED). */
+    int32_t kv_quant;
+    int32_t reserved3;  /* must be 0 */
+    float *cache_k_scale;
+    float *cache_v_scale;
 } pa_options;
 
 /*

@@ -25,7 +25,9 @@ class PaOptions(ctypes.Structure):
     _fields_ = [("struct_size", ctypes.c_uint32), ("window", ctypes.c_int32),
                 ("block_table", ctypes.c_void_p), ("block_size", ctypes.c_int32),
                 ("max_blocks_per_seq", ctypes.c_int32), ("num_blocks", ctypes.c_int32),
-                ("reserved", ctypes.c_int32), ("rope_theta", ctypes.c_float), ("reserved2", ctypes.c_int32)]
+                ("reserved", ctypes.c_int32), ("rope_theta", ctypes.c_float), ("reserved2", ctypes.c_int32),
+                ("kv_quant", ctypes.c_int32), ("reserved3", ctypes.c_int32),
+                ("cache_k_scale", ctypes.c_void_p), ("cache_v_scale", ctypes.c_void_p)]
 
 
 # Entry points declared in include/prefill_attn.h: name -> (restype, argtypes)
@@ -87,9 +89,9 @@ def _stream_handle(stream) -> int:
 
 
 def _varlen_args(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_k, cache_v, cache_offsets, out, lse,
-                 scale, causal, stream, max_cache_len=None):
+                 scale, causal, stream, max_cache_len=None, cache_dtype=torch.bfloat16):
     for name, t, dt in (("q", q, torch.bfloat16), ("k", k, torch.bfloat16), ("v", v, torch.bfloat16),
-                        ("cache_k", cache_k, torch.bfloat16), ("cache_v", cache_v, torch.bfloat16),
+                        ("cache_k", cache_k, cache_dtype), ("cache_v", cache_v, cache_dtype),
                         ("out", out, torch.bfloat16), ("cu_seqlens_q", cu_seqlens_q, torch.int32),
                         ("cu_seqlens_k", cu_seqlens_k, torch.int32), ("cache_offsets", cache_offsets, torch.int32)):
         if t.dtype != dt or not t.is_cuda or not t.is_contiguous():
@@ -125,11 +127,15 @@ def prefill_attn_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_k, cache_v, c
 
 
 def make_options(window: int = 0, block_table=None, block_size: int = 0, num_blocks: int = 0,
-                 rope_theta: float = 0.0) -> PaOptions:
+                 rope_theta: float = 0.0, cache_k_scale=None, cache_v_scale=None) -> PaOptions:
     o = PaOptions()
     o.struct_size = ctypes.sizeof(PaOptions)
     o.window = int(window)
     o.rope_theta = float(rope_theta)
+    if cache_k_scale is not None:
+        o.kv_quant = 1
+        o.cache_k_scale = cache_k_scale.data_ptr()
+        o.cache_v_scale = cache_v_scale.data_ptr()
     if block_table is not None:
         o.block_table = block_table.data_ptr()
         o.block_size = int(block_size)
@@ -140,7 +146,8 @@ def make_options(window: int = 0, block_table=None, block_size: int = 0, num_blo
 
 def prefill_attn_varlen_ex(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_k, cache_v, cache_offsets, out, lse=None, *,
                            scale: Optional[float] = None, causal: bool = True, window: int = 0,
-                           block_table=None, rope_theta: float = 0.0, stream=None) -> None:
+                           block_table=None, rope_theta: float = 0.0, cache_k_scale=None, cache_v_scale=None,
+                           stream=None) -> None:
     """prefill_attn_varlen with options.
 
     window > 0 restricts each query to its `window` most recent keys (causal only).
@@ -150,6 +157,9 @@ def prefill_attn_varlen_ex(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_k, cache_v
     block_table[b, p // block_size].
     rope_theta > 0 rotates every new q/k to its absolute position (rotary
     embedding, rotate-half pairing) before attention and the cache write.
+    cache_k_scale / cache_v_scale (fp32 CUDA [num_seqs, n_kv_heads, max_cache_len])
+    select the int8 cache: cache_k/v are then int8 codes and row (b, h, p) stands
+    for code * scale.
     """
     cap = None
     if block_table is not None:
@@ -157,9 +167,17 @@ def prefill_attn_varlen_ex(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_k, cache_v
                 or block_table.dim() != 2:
             raise ValueError("block_table must be a contiguous 2-D CUDA int32 tensor")
         cap = block_table.shape[1] * cache_k.shape[2]
+    quant = cache_k_scale is not None or cache_v_scale is not None
+    if quant:
+        for name, t in (("cache_k_scale", cache_k_scale), ("cache_v_scale", cache_v_scale)):
+            if t is None or t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous() \
+                    or tuple(t.shape) != tuple(cache_k.shape[:-1]):
+                raise ValueError(f"{name} must be a contiguous CUDA float32 tensor of shape cache.shape[:-1]")
     args = _varlen_args(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_k, cache_v, cache_offsets, out, lse,
-                        scale, causal, stream, max_cache_len=cap)
-    opts = make_options(window, block_table, cache_k.shape[2], cache_k.shape[0], rope_theta)
+                        scale, causal, stream, max_cache_len=cap,
+                        cache_dtype=torch.int8 if quant else torch.bfloat16)
+    opts = make_options(window, block_table, cache_k.shape[2], cache_k.shape[0], rope_theta,
+                        cache_k_scale, cache_v_scale)
     _check(load().prefill_attn_varlen_ex(*args[:-1], ctypes.byref(opts), args[-1]))
 
 

@@ -151,6 +151,9 @@ struct Options {
     const int32_t* block_table = nullptr;  // paged cache when set
     int block_size = 0, max_blocks = 0, num_blocks = 0;
     float rope_theta = 0.f;                // rotary embedding when > 0
+    int kv_quant = 0;                      // 1: int8 cache with fp32 row scales
+    float* scale_k = nullptr;
+    float* scale_v = nullptr;
 };
 
 // Reads the caller's options; fields past the caller's struct_size count as zero.
@@ -190,6 +193,21 @@ pa_status read_options(const pa_options* opts, int causal, Options* o) {
     }
     if (have >= offsetof(pa_options, reserved2) + sizeof(int32_t) && opts->reserved2 != 0)
         return fail(PA_ERR_INVALID_ARG, "pa_options.reserved2 must be 0");
+    if (have >= offsetof(pa_options, kv_quant) + sizeof(int32_t) && opts->kv_quant != 0) {
+        if (have < offsetof(pa_options, cache_v_scale) + sizeof(float*))
+            return fail(PA_ERR_INVALID_ARG, "pa_options.struct_size %u does not cover the scale pointers",
+                        (unsigned)opts->struct_size);
+        if (opts->kv_quant != 1) return fail(PA_ERR_INVALID_ARG, "kv_quant must be 0 or 1 (got %d)", opts->kv_quant);
+        if (opts->reserved3 != 0) return fail(PA_ERR_INVALID_ARG, "pa_options.reserved3 must be 0");
+        if (!opts->cache_k_scale || !opts->cache_v_scale)
+            return fail(PA_ERR_INVALID_ARG, "kv_quant = 1 needs cache_k_scale and cache_v_scale");
+        if ((reinterpret_cast<uintptr_t>(opts->cache_k_scale) | reinterpret_cast<uintptr_t>(opts->cache_v_scale)) & 3u)
+            return fail(PA_ERR_INVALID_ARG, "cache scales must be 4-byte aligned");
+        if (o->block_table) return fail(PA_ERR_UNSUPPORTED, "kv_quant is not combined with a paged cache");
+        o->kv_quant = 1;
+        o->scale_k = opts->cache_k_scale;
+        o->scale_v = opts->cache_v_scale;
+    }
     return PA_OK;
 }
 
@@ -295,6 +313,9 @@ pa_status enqueue(const void* q, const void* k, const void* v, const int32_t* cu
     p.box_rows = std::min(o.block_size, pa::kBlockN);
     p.max_blocks = o.max_blocks;
     p.num_blocks = o.num_blocks;
+    p.kv_quant = o.kv_quant;
+    p.scale_k = o.scale_k;
+    p.scale_v = o.scale_v;
     e = pa::encode_fwd_maps(p, q, total_q, num_seqs, head_dim, o.num_blocks);
     if (e != cudaSuccess) return cuda_fail(e, "tensor map encoding");
     int sms = 0;

@@ -85,12 +85,17 @@ struct __align__(8) Ctrl {
     uint64_t q_full, q_empty;
     uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
     uint64_t v_fix[4];  // paged cache: last prefix V tile with the rows past P zeroed
+    uint64_t k_conv[4], v_conv[4];  // int8 cache: prefix tile expanded to bf16
+    uint64_t ks_full[4];            // int8 cache: row scales of K tile t in kscale[t % 4]
     uint64_t s_full[kSlots], p_full[kSlots], pv_done[kSlots], o_empty[kSlots];
     uint64_t mma_drain;
     uint64_t unit_full[2], unit_empty[2];
     UnitSlot slot[2];
     uint32_t tmem_base;
     int abort;
+    // int8 cache: the row scales of K tile t (CTA tile counter) in slot t % 4,
+    // folded into the scores by the softmax warps (the K tile holds the codes)
+    alignas(16) float kscale[4][kBlockN];
 };
 
 // Tiles first (the dynamic shared window starts 1024-byte aligned, which the
@@ -281,12 +286,96 @@ __device__ __noinline__ void zero_tile_rows(uint8_t* tile, int row0, int lane) {
     }
 }
 
+// int8 cache, prefix tile: the TMA box of codes (row r = D bytes) lands in the
+// upper half of a bf16 stage; this expands it in place into the swizzled bf16
+// tile the MMA reads, value = code * scale[row] rounded to bf16 (one warp;
+// sc[q] holds the scale of row 32 q + lane).  Rows go in increasing order and
+// each batch of rows is read before it is written: the bf16 image of row r
+// ends within the codes of rows <= r, so no code is overwritten unread.
+template <int D>
+__device__ __noinline__ void dequant_tile(uint8_t* stage, const float (&sc)[4], int lane) {
+    using C = Cfg<D>;
+    constexpr int kGran = D / 8;  // 8-column granules per row
+    constexpr int kRows = 32 / kGran;  // rows per batch
+    constexpr int kChunkGran = C::kChunkCols / 8;
+    const uint8_t* codes = stage + C::kTileBytes / 2;
+    const int g = lane % kGran;
+    const int c = g / kChunkGran, gg = g % kChunkGran;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+#pragma unroll 2
+        for (int r0 = 32 * q; r0 < 32 * q + 32; r0 += kRows) {
+            const int r = r0 + lane / kGran;
+            const uint2 w = *reinterpret_cast<const uint2*>(codes + r * D + g * 8);
+            const float s = __shfl_sync(0xffffffffu, sc[q], r & 31);
+            __syncwarp();
+            // code + 128 as the low mantissa byte of 2^23, minus 2^23 + 128: exact
+            const uint32_t x = w.x ^ 0x80808080u, y = w.y ^ 0x80808080u;
+            float f[8];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                f[e] = (__uint_as_float(__byte_perm(x, 0x4B000000u, 0x7540u + e)) - 8388736.0f) * s;
+                f[e + 4] = (__uint_as_float(__byte_perm(y, 0x4B000000u, 0x7540u + e)) - 8388736.0f) * s;
+            }
+            const int phys = D >= 64 ? (gg ^ (r & 7)) : (gg ^ ((r >> 1) & 3));
+            *reinterpret_cast<uint4*>(stage + c * C::kChunkBytes + r * C::kRowBytes + phys * 16) =
+                make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]),
+                           pack_bf16(f[6], f[7]));
+        }
+    }
+}
+
+// int8 cache write: rows [lo_row, lo_row + nrows) of a staged bf16 tile as
+// int8 codes at codes + i * D and their scales at scales[i] (consecutive cache
+// rows).  Per row, in fp32: scale = max|x| / 127, code = nearest integer (ties
+// to even) of x / scale, clamped to +-127; a zero row is scale 0, codes 0.
+template <int D>
+__device__ __noinline__ void quant_tile_rows(const uint8_t* tile, int8_t* codes, float* scales, int lo_row,
+                                             int nrows, int lane) {
+    using C = Cfg<D>;
+    constexpr int kGran = D / 8;  // lanes per row
+    constexpr int kRows = 32 / kGran;
+    constexpr int kChunkGran = C::kChunkCols / 8;
+    const int g = lane % kGran;
+    const int c = g / kChunkGran, gg = g % kChunkGran;
+    for (int i0 = 0; i0 < nrows; i0 += kRows) {
+        const int i = i0 + lane / kGran;
+        const bool valid = i < nrows;
+        const int r = lo_row + (valid ? i : 0);
+        const int phys = D >= 64 ? (gg ^ (r & 7)) : (gg ^ ((r >> 1) & 3));
+        const uint4 x = *reinterpret_cast<const uint4*>(tile + c * C::kChunkBytes + r * C::kRowBytes + phys * 16);
+        const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
+        float v[8];
+        float am = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            v[2 * e] = __uint_as_float(xw[e] << 16);
+            v[2 * e + 1] = __uint_as_float(xw[e] & 0xffff0000u);
+            am = fmaxf(am, fmaxf(fabsf(v[2 * e]), fabsf(v[2 * e + 1])));
+        }
+#pragma unroll
+        for (int o = 1; o < kGran; o <<= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+        const float sc = __fdiv_rn(am, 127.0f);
+        uint32_t packed[2] = {0u, 0u};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            int qv = 0;
+            if (sc > 0.f) qv = max(-127, min(127, __float2int_rn(__fdiv_rn(v[e], sc))));
+            packed[e >> 2] |= (uint32_t)(qv & 0xff) << (8 * (e & 3));
+        }
+        if (valid) {
+            *reinterpret_cast<uint2*>(codes + (size_t)i * D + g * 8) = make_uint2(packed[0], packed[1]);
+            if (g == 0) scales[i] = sc;
+        }
+    }
+}
+
 // Contiguous cache, one KV ring (K or V): waits for the stage, then
 // TMA-loads tile j (index in the sequence) of unit u from the cache (prefix
 // tiles) or from the new tokens' k/v.  Out of line: the K and the V loader
 // share one copy of this code, which keeps the kernel's hot code within the
 // instruction caches.
-template <int D>
+template <int D, bool kQuant>
 __device__ __noinline__ bool load_kv_tile(const FwdParams& p, Ctrl* ctl, WorkspaceHeader* hdr, uint8_t* ring,
                                           int stages, uint64_t* full, uint64_t* empty, const CUtensorMap* tm_cache,
                                           const CUtensorMap* tm_new, int* last_parity, uint32_t t, int j,
@@ -296,6 +385,15 @@ __device__ __noinline__ bool load_kv_tile(const FwdParams& p, Ctrl* ctl, Workspa
     const uint32_t ph = (t / stages) & 1;
     const int kb = tile_key_base<false>(j, s.P, np);
     if (!wait_bar(&empty[st], ph ^ 1, ctl, hdr)) return false;
+    if (kQuant && j < np) {
+        // int8 codes of the prefix tile into the stage's upper half (one box of
+        // 128 rows x D bytes), expanded to bf16 by the cache writer
+        mbar_arrive_expect_tx(&full[st], kBlockN * D);
+        tma_load_3d(ring + st * C::kTileBytes + C::kTileBytes / 2, tm_cache, &full[st], 0, kb,
+                    u.b * p.n_kv_heads + u.kvh);
+        last_parity[st] = (int)ph;
+        return true;
+    }
     mbar_arrive_expect_tx(&full[st], C::kTileBytes);
     for (int c = 0; c < C::kChunks; ++c) {
         uint8_t* dst = ring + st * C::kTileBytes + c * C::kChunkBytes;
@@ -308,7 +406,7 @@ __device__ __noinline__ bool load_kv_tile(const FwdParams& p, Ctrl* ctl, Workspa
     return true;
 }
 
-template <int D, bool kPaged>
+template <int D, bool kPaged, bool kQuant>
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ FwdParams p) {
     using C = Cfg<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -338,7 +436,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             mbar_init(&ctl->v_full[s], 1);
             mbar_init(&ctl->v_empty[s], 2);
             mbar_init(&ctl->v_fix[s], 1);  // V cache writer
+            mbar_init(&ctl->v_conv[s], 1);
         }
+        for (int s = 0; s < C::kStagesK; ++s) mbar_init(&ctl->k_conv[s], 1);  // K cache writer
+        for (int s = 0; s < 4; ++s) mbar_init(&ctl->ks_full[s], 1);          // K cache writer
         for (int i = 0; i < kSlots; ++i) {
             mbar_init(&ctl->s_full[i], 1);
             mbar_init(&ctl->p_full[i], 4);  // the slot's 4 softmax warps
@@ -536,7 +637,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 const UnitGeo ug = unit_geo<kPaged>(u, s, tps, p.causal, p.window);
                 bool ok = true;
                 for (int j = 0; j < ug.ntiles && ok; ++j, ++t)
-                    ok = load_kv_tile<D>(p, ctl, hdr, k_smem, C::kStagesK, ctl->k_full, ctl->k_empty, &p.tm_ck,
+                    ok = load_kv_tile<D, kQuant>(p, ctl, hdr, k_smem, C::kStagesK, ctl->k_full, ctl->k_empty, &p.tm_ck,
                                                  &p.tm_k, last_k_parity, t, ug.lo + j, u, s, ug.np);
                 if (!ok) break;
             }
@@ -558,7 +659,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 const UnitGeo ug = unit_geo<kPaged>(us.u, us.s, tps, p.causal, p.window);
                 bool ok = true;
                 for (int j = 0; j < ug.ntiles && ok; ++j, ++t)
-                    ok = load_kv_tile<D>(p, ctl, hdr, v_smem, C::kStagesV, ctl->v_full, ctl->v_empty, &p.tm_cv,
+                    ok = load_kv_tile<D, kQuant>(p, ctl, hdr, v_smem, C::kStagesV, ctl->v_full, ctl->v_empty, &p.tm_cv,
                                                  &p.tm_v, last_v_parity, t, ug.lo + j, us.u, us.s, ug.np);
                 if (!ok) break;
             }
@@ -581,6 +682,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         uint32_t ns[kSlots] = {0, 0};  // tiles processed per slot so far
         uint32_t no[kSlots] = {0, 0};  // units with the slot active so far
         uint32_t fixpar = 0;           // paged: parity bit per V stage of v_fix
+        uint32_t kcpar = 0, vcpar = 0; // int8 cache: parity bit per stage of k_conv / v_conv
+        // K tile tt (index jt in the sequence) ready for S: a prefix tile of an
+        // int8 cache once the K writer has expanded it, else once TMA landed
+        auto wait_k = [&](uint32_t tt, int jt, int np) -> bool {
+            const int kst = tt % C::kStagesK;
+            if (kQuant && jt < np) {
+                const bool got = warp_wait(&ctl->k_conv[kst], (kcpar >> kst) & 1, ctl, hdr);
+                kcpar ^= 1u << kst;
+                return got;
+            }
+            return warp_wait(&ctl->k_full[kst], (tt / C::kStagesK) & 1, ctl, hdr);
+        };
         bool ok = true;
         auto issue_s = [&](int i, uint32_t tt) {
             if (leader) {
@@ -623,7 +736,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             const int ntiles = ug.ntiles;
             if (!warp_wait(&ctl->q_full, u_it & 1, ctl, hdr)) break;
             // prologue: S of tile 0 for the slots that start there
-            if (!warp_wait(&ctl->k_full[t % C::kStagesK], (t / C::kStagesK) & 1, ctl, hdr)) break;
+            if (!wait_k(t, ug.lo, ug.np)) break;
             tc_fence_after();
             for (int i = 0; i < kSlots; ++i)
                 if (ug.a[i] == 0 && ug.b[i] > 0) issue_s(i, t);
@@ -643,6 +756,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                             if (kPaged && paged_tail_tile(ug.lo + j, s.P, ug.np)) {
                                 got = warp_wait(&ctl->v_fix[vst], (fixpar >> vst) & 1, ctl, hdr);
                                 fixpar ^= 1u << vst;
+                            } else if (kQuant && ug.lo + j < ug.np) {
+                                got = warp_wait(&ctl->v_conv[vst], (vcpar >> vst) & 1, ctl, hdr);
+                                vcpar ^= 1u << vst;
                             } else {
                                 got = warp_wait(&ctl->v_full[vst], (tj / C::kStagesV) & 1, ctl, hdr);
                             }
@@ -658,8 +774,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                     if (j + 1 >= ug.a[i] && j + 1 < ug.b[i]) {
                         // S_i(j+1) overwrites P_i(j): issued after PV_i(j) on the in-order tensor pipe
                         if (!k_ready) {
-                            const uint32_t tn = tj + 1;
-                            if (!warp_wait(&ctl->k_full[tn % C::kStagesK], (tn / C::kStagesK) & 1, ctl, hdr)) {
+                            if (!wait_k(tj + 1, ug.lo + j + 1, ug.np)) {
                                 ok = false;
                                 break;
                             }
@@ -718,11 +833,47 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             for (int jr = 0; jr < ug.ntiles; ++jr, ++t) {
                 const int j = ug.lo + jr;  // tile index in the sequence
                 const int st = t % stages;
+                if (kQuant && j < np) {
+                    // int8 prefix tile: expand the codes for the MMA.  V rows
+                    // become code * scale; K rows stay the (exact) codes and
+                    // their scales go to the scale ring, folded into the scores.
+                    const int kb = tile_key_base<false>(j, us.s.P, np);
+                    const float* srow = (is_k ? p.scale_k : p.scale_v) +
+                                        ((size_t)us.u.b * p.n_kv_heads + us.u.kvh) * p.max_cache_len;
+                    float sc[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int row = kb + 32 * q + lane;  // rows below 0 are zero-filled codes
+                        sc[q] = row >= 0 ? __ldg(srow + row) : 0.f;
+                    }
+                    if (!warp_wait(&full[st], (t / stages) & 1, ctl, hdr)) { ok = false; break; }
+                    if (is_k) {
+                        const float one[4] = {1.f, 1.f, 1.f, 1.f};
+                        dequant_tile<D>(ring + st * C::kTileBytes, one, lane);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) ctl->kscale[t & 3][32 * q + lane] = sc[q];
+                    } else {
+                        dequant_tile<D>(ring + st * C::kTileBytes, sc, lane);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(is_k ? &ctl->k_conv[st] : &ctl->v_conv[st]);
+                        if (is_k) mbar_arrive(&ctl->ks_full[t & 3]);
+                        mbar_arrive(&empty[st]);
+                    }
+                    continue;
+                }
                 if (!warp_wait(&full[st], (t / stages) & 1, ctl, hdr)) { ok = false; break; }
                 int lo_row, nrows;
                 if (own_rows(j, np, us.u.q0, q_end, lo_row, nrows)) {
                     const int first_tok = (j - np) * kBlockN + lo_row;  // token index within the sequence
-                    if (kPaged) {
+                    if (kQuant) {
+                        const size_t row0 = ((size_t)us.u.b * p.n_kv_heads + us.u.kvh) * p.max_cache_len +
+                                            us.s.P + first_tok;
+                        quant_tile_rows<D>(ring + st * C::kTileBytes, reinterpret_cast<int8_t*>(cache) + row0 * D,
+                                           (is_k ? p.scale_k : p.scale_v) + row0, lo_row, nrows, lane);
+                    } else if (kPaged) {
                         copy_tile_rows_paged<D>(ring + st * C::kTileBytes, cache,
                                                 p.block_table + (size_t)us.u.b * p.max_blocks, p.block_log2,
                                                 p.num_blocks, p.n_kv_heads, us.u.kvh, us.s.P + first_tok, lo_row, nrows, lane);
@@ -740,7 +891,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                     if (lane == 0) mbar_arrive(&ctl->v_fix[st]);
                 }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&empty[st]);
+                if (lane == 0) {
+                    // int8 cache: one ks_full phase per K tile (none for this one's
+                    // scales), only after the tile landed, so that the ring never
+                    // runs two phases ahead of a softmax warp
+                    if (kQuant && is_k) mbar_arrive(&ctl->ks_full[t & 3]);
+                    mbar_arrive(&empty[st]);
+                }
             }
             if (!ok) break;
         }
@@ -756,6 +913,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         const uint32_t o_col = s_col + kColO;
         const float sl2 = p.scale_log2;
         uint32_t ns = 0;  // tiles this slot has processed
+        uint32_t tg = 0;  // CTA tiles before the current unit (int8 cache: scale ring index)
         for (int u_it = 0;; ++u_it) {
             const int sl = u_it & 1;
             if (!warp_wait(&ctl->unit_full[sl], (u_it >> 1) & 1, ctl, hdr)) break;
@@ -767,6 +925,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             const SeqInfo s = us.s;
             const UnitGeo ug = unit_geo<kPaged>(u, s, tps, p.causal, p.window);
             const int nt = ug.b[slot] - ug.a[slot];
+            const uint32_t tg0 = tg;
+            tg += ug.ntiles;
             if (nt == 0) continue;
             const int qs = u.q0 + slot * tps;
             const int qe = min(qs + tps, s.n);
@@ -808,6 +968,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                     }
                 }
                 const int jt = ug.lo + ug.a[slot] + j;  // tile index in the sequence
+                if (kQuant && jt < np) {
+                    // int8 prefix tile: S holds q . code; scale column c by its row's scale
+                    const uint32_t tc = tg0 + ug.a[slot] + j;
+                    if (!warp_wait(&ctl->ks_full[tc & 3], (tc >> 2) & 1, ctl, hdr)) { ok = false; break; }
+                    const float4* ksc = reinterpret_cast<const float4*>(ctl->kscale[tc & 3]);
+#pragma unroll
+                    for (int c4 = 0; c4 < kBlockN / 4; ++c4) {
+                        const float4 f = ksc[c4];
+                        sv[4 * c4] *= f.x;
+                        sv[4 * c4 + 1] *= f.y;
+                        sv[4 * c4 + 2] *= f.z;
+                        sv[4 * c4 + 3] *= f.w;
+                    }
+                }
                 const int kb = tile_key_base<kPaged>(jt, s.P, np);
                 // paged: the last prefix tile holds prefix keys only below P
                 const bool tail = kPaged && jt < np && kb + kBlockN > s.P;
@@ -929,19 +1103,19 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 cudaError_t encode3d(CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1_bytes,
                      uint64_t s2_bytes, uint32_t b0, uint32_t b1, uint32_t b2, CUtensorMapSwizzle sw,
-                     CUtensorMapL2promotion l2) {
+                     CUtensorMapL2promotion l2, CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
     auto fn = encode_fn();
     if (!fn) return cudaErrorNotSupported;
     cuuint64_t dims[3] = {d0, d1, d2};
     cuuint64_t strides[2] = {s1_bytes, s2_bytes};
     cuuint32_t box[3] = {b0, b1, b2};
     cuuint32_t es[3] = {1, 1, 1};
-    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
+    CUresult r = fn(m, dt, 3, const_cast<void*>(ptr), dims, strides, box, es,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, sw, l2, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int D, bool kPaged>
+template <int D, bool kPaged, bool kQuant>
 cudaError_t launch_d(const FwdParams& p, int grid, cudaStream_t st) {
     constexpr int kSmem = smem_bytes<D>();
     static_assert(kSmem <= 232448, "shared memory budget");
@@ -950,11 +1124,11 @@ cudaError_t launch_d(const FwdParams& p, int grid, cudaStream_t st) {
     cudaGetDevice(&dev);
     if (dev < 64 && !configured_for[dev]) {
         cudaError_t e =
-            cudaFuncSetAttribute(attn_fwd_kernel<D, kPaged>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+            cudaFuncSetAttribute(attn_fwd_kernel<D, kPaged, kQuant>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
         if (e != cudaSuccess) return e;
         configured_for[dev] = 1;
     }
-    attn_fwd_kernel<D, kPaged><<<grid, kThreads, kSmem, st>>>(p);
+    attn_fwd_kernel<D, kPaged, kQuant><<<grid, kThreads, kSmem, st>>>(p);
     return cudaGetLastError();
 }
 
@@ -981,6 +1155,14 @@ cudaError_t encode_fwd_maps(FwdParams& p, const void* q, int total_q, int num_se
         return encode3d(&p.tm_cv, p.cache_v, D, bs, Z, D * 2, bs * D * 2, cc, p.box_rows, 1, sw,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
     }
+    if (p.kv_quant) {
+        // int8 codes [B, Hk, cap, D] viewed (D, cap, B*Hk), box (D, 128, 1), no swizzle
+        e = encode3d(&p.tm_ck, p.cache_k, D, cap, (uint64_t)num_seqs * Hk, D, cap * D, (uint32_t)D, kBlockN, 1,
+                     CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_DATA_TYPE_UINT8);
+        if (e != cudaSuccess) return e;
+        return encode3d(&p.tm_cv, p.cache_v, D, cap, (uint64_t)num_seqs * Hk, D, cap * D, (uint32_t)D, kBlockN, 1,
+                        CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_DATA_TYPE_UINT8);
+    }
     e = encode3d(&p.tm_ck, p.cache_k, D, cap, (uint64_t)num_seqs * Hk, D * 2, cap * D * 2, cc, kBlockN, 1, sw,
                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
     if (e != cudaSuccess) return e;
@@ -990,10 +1172,18 @@ cudaError_t encode_fwd_maps(FwdParams& p, const void* q, int total_q, int num_se
 
 cudaError_t launch_attn_fwd(const FwdParams& p, int head_dim, int grid, cudaStream_t st) {
     const bool paged = p.block_table != nullptr;
+    if (paged && p.kv_quant) return cudaErrorNotSupported;  // not built: the int8 cache is contiguous only
     switch (head_dim) {
-        case 32: return paged ? launch_d<32, true>(p, grid, st) : launch_d<32, false>(p, grid, st);
-        case 64: return paged ? launch_d<64, true>(p, grid, st) : launch_d<64, false>(p, grid, st);
-        case 128: return paged ? launch_d<128, true>(p, grid, st) : launch_d<128, false>(p, grid, st);
+        case 32:
+            return paged ? launch_d<32, true, false>(p, grid, st)
+                         : (p.kv_quant ? launch_d<32, false, true>(p, grid, st) : launch_d<32, false, false>(p, grid, st));
+        case 64:
+            return paged ? launch_d<64, true, false>(p, grid, st)
+                         : (p.kv_quant ? launch_d<64, false, true>(p, grid, st) : launch_d<64, false, false>(p, grid, st));
+        case 128:
+            return paged ? launch_d<128, true, false>(p, grid, st)
+                         : (p.kv_quant ? launch_d<128, false, true>(p, grid, st)
+                                       : launch_d<128, false, false>(p, grid, st));
         default: return cudaErrorInvalidValue;
     }
 }

@@ -60,6 +60,11 @@ struct FwdParams {
     int box_rows;                // min(block_size, 128): rows of one cache TMA box
     int max_blocks;
     int num_blocks;
+    // int8 cache (kv_quant): cache_k/cache_v hold int8 codes, these the fp32
+    // scale of each cache row ([B, Hk, cap])
+    float* scale_k;
+    float* scale_v;
+    int kv_quant;
 };
 
 // Encodes the tensor maps of `p` (the pointer fields and sizes must be set).

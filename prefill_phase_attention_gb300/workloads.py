@@ -233,6 +233,34 @@ def make_paged_cache(wl: Workload, block_size: int, g: torch.Generator, extra_bl
     return table, pools[0], pools[1]
 
 
+def make_q8_cache(wl: Workload, g: torch.Generator, sentinel: bool = True):
+    """An int8 cache: (codes_k, scales_k, codes_v, scales_v) on the CPU.
+
+    Codes int8 [num_seqs, n_kv_heads, max_cache_len, head_dim], scales fp32
+    [num_seqs, n_kv_heads, max_cache_len].  The first ``wl.prefilled[b]`` rows of
+    slot b hold uniform codes in [-127, 127] (one code of each row set to +-127)
+    and scales uniform in [0.005, 0.03]; every other row holds random codes and a
+    NaN scale (or zero codes and scale 0), so a read of it shows.
+    """
+    shape = (wl.num_seqs, wl.n_kv_heads, wl.max_cache_len, wl.head_dim)
+    out = []
+    for _ in range(2):
+        codes = torch.randint(-127, 128, shape, generator=g, dtype=torch.int32).to(torch.int8)
+        scales = torch.full(shape[:-1], float("nan") if sentinel else 0.0, dtype=torch.float32)
+        if not sentinel:
+            codes.zero_()
+        for b, p in enumerate(wl.prefilled):
+            if p:
+                c = torch.randint(-127, 128, (wl.n_kv_heads, p, wl.head_dim), generator=g, dtype=torch.int32)
+                col = torch.randint(0, wl.head_dim, (wl.n_kv_heads, p, 1), generator=g)
+                sign = torch.randint(0, 2, (wl.n_kv_heads, p, 1), generator=g) * 2 - 1
+                c.scatter_(2, col, (127 * sign).to(torch.int32))
+                codes[b, :, :p] = c.to(torch.int8)
+                scales[b, :, :p] = torch.rand((wl.n_kv_heads, p), generator=g) * 0.025 + 0.005
+        out += [codes, scales]
+    return tuple(out)
+
+
 def make_step_inputs(wl: Workload, step: Step, g: torch.Generator):
     """q [T,H,d], k/v [T,Hk,d] bf16 and the int32 metadata of one launch (CPU)."""
     t = step.total_q

@@ -137,3 +137,28 @@ def compare_rotated_cache(got_bits, ref_bits, label=""):
         f"{label}: rotated key off by {np.abs(g - r).max():.3e} (more than one bf16 ulp + 2^-16)"
     assert diff.mean() < 0.01, f"{label}: {diff.mean():.2%} of cache entries differ"
     return int(diff.sum())
+
+
+def run_step_gpu_q8(wl, inp, ck, sk, cv, sv, window=0, rope_theta=0.0):
+    """One launch over an int8 cache (codes + fp32 row scales, CUDA tensors)."""
+    dev = {k: v.cuda() for k, v in inp.items()}
+    T = inp["q"].shape[0]
+    out = Guarded((T, wl.n_heads, wl.head_dim), torch.bfloat16)
+    lse = Guarded((T, wl.n_heads), torch.float32)
+    binding.prefill_attn_varlen_ex(dev["q"], dev["k"], dev["v"], dev["cu_seqlens_q"], dev["cu_seqlens_k"],
+                                   ck, cv, dev["cache_offsets"], out.t, lse.t, scale=wl.scale, causal=wl.causal,
+                                   window=window, rope_theta=rope_theta, cache_k_scale=sk, cache_v_scale=sv)
+    torch.cuda.synchronize()
+    assert out.guards_intact() and lse.guards_intact(), "write outside out/lse"
+    assert binding.prefill_attn_device_status() == 0
+    return out.t, lse.t
+
+
+def oracle_step_q8(wl, inp, ck, sk, cv, sv, rows=None, window=0, rope_theta=0.0, want_cache=True):
+    """The oracle over an int8 cache (numpy codes/scales); cache images are (codes, scales)."""
+    return oracle.prefill_attention(
+        W.bf16_bits(inp["q"]), W.bf16_bits(inp["k"]), W.bf16_bits(inp["v"]),
+        inp["cu_seqlens_q"].numpy(), inp["cu_seqlens_k"].numpy(), inp["cache_offsets"].numpy(),
+        ck, cv, n_heads=wl.n_heads, n_kv_heads=wl.n_kv_heads, head_dim=wl.head_dim,
+        max_cache_len=wl.max_cache_len, scale=wl.scale, causal=wl.causal, window=window, rows=rows,
+        rope_theta=rope_theta, kv_quant=1, cache_k_scale=sk, cache_v_scale=sv, want_cache=want_cache)

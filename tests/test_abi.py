@@ -83,9 +83,10 @@ def test_python_binding_refuses_cpu_tensors(lib):
 
 
 def _call_ex(lib, window=0, causal=1, struct_size=None, block_table=None, block_size=0, max_blocks=0,
-             num_blocks=0, reserved=0, rope_theta=0.0, reserved2=0):
+             num_blocks=0, reserved=0, rope_theta=0.0, reserved2=0, kv_quant=0, reserved3=0, sk=None, sv=None):
     opts = binding.PaOptions(ctypes.sizeof(binding.PaOptions) if struct_size is None else struct_size, window,
-                             block_table, block_size, max_blocks, num_blocks, reserved, rope_theta, reserved2)
+                             block_table, block_size, max_blocks, num_blocks, reserved, rope_theta, reserved2,
+                             kv_quant, reserved3, sk, sv)
     return lib.prefill_attn_varlen_ex(16, 32, 48, 64, 80, 96, 112, 128, 144, None, 1, 4, 8, 4, 2, 64,
                                       0.125, causal, ctypes.byref(opts), None)
 
@@ -109,6 +110,12 @@ _PAGED = dict(block_table=256, block_size=8, max_blocks=1, num_blocks=4)
     (dict(rope_theta=float("nan")), 1, "rope_theta"),
     (dict(rope_theta=float("inf")), 1, "rope_theta"),
     (dict(reserved2=3), 1, "reserved2"),
+    (dict(kv_quant=2, sk=512, sv=1024), 1, "kv_quant"),
+    (dict(kv_quant=1), 1, "cache_k_scale"),
+    (dict(kv_quant=1, sk=514, sv=1024), 1, "aligned"),
+    (dict(kv_quant=1, sk=512, sv=1024, reserved3=1), 1, "reserved3"),
+    (dict(kv_quant=1, sk=512, sv=1024, struct_size=48), 1, "scale pointers"),
+    (dict(_PAGED, kv_quant=1, sk=512, sv=1024), 2, "paged"),
 ])
 def test_options_are_checked_before_launch(lib, kw, status, msg):
     assert _call_ex(lib, **kw) == status
@@ -121,5 +128,5 @@ def test_options_layout_matches_header():
     assert [(n, getattr(P, n).offset) for n, _ in P._fields_] == [
         ("struct_size", 0), ("window", 4), ("block_table", 8), ("block_size", 16),
         ("max_blocks_per_seq", 20), ("num_blocks", 24), ("reserved", 28), ("rope_theta", 32),
-        ("reserved2", 36)]
-    assert ctypes.sizeof(P) == 40
+        ("reserved2", 36), ("kv_quant", 40), ("reserved3", 44), ("cache_k_scale", 48), ("cache_v_scale", 56)]
+    assert ctypes.sizeof(P) == 64
