@@ -288,39 +288,54 @@ __device__ __noinline__ void zero_tile_rows(uint8_t* tile, int row0, int lane) {
 
 // int8 cache, prefix tile: the TMA box of codes (row r = D bytes) lands in the
 // upper half of a bf16 stage; this expands it in place into the swizzled bf16
-// tile the MMA reads, value = code * scale[row] rounded to bf16 (one warp;
-// sc[q] holds the scale of row 32 q + lane).  Rows go in increasing order and
-// each batch of rows is read before it is written: the bf16 image of row r
-// ends within the codes of rows <= r, so no code is overwritten unread.
-template <int D>
+// tile the MMA reads (one warp): value = code * scale[row] rounded to bf16 when
+// kScale (sc[q] holds the scale of row 32 q + lane), else the code itself
+// (exact in bf16).  Rows go in increasing order, kGroup batches of rows at a
+// time, each group read before it is written: the bf16 image of row r ends
+// within the codes of rows <= r, so no code is overwritten unread.
+template <int D, bool kScale>
 __device__ __noinline__ void dequant_tile(uint8_t* stage, const float (&sc)[4], int lane) {
     using C = Cfg<D>;
-    constexpr int kGran = D / 8;  // 8-column granules per row
-    constexpr int kRows = 32 / kGran;  // rows per batch
+    constexpr int kGran = D / 8;       // 8-column granules per row
+    constexpr int kRows = 32 / kGran;  // rows per batch (one granule per lane)
+    constexpr int kGroup = 4;          // batches loaded before any is written
     constexpr int kChunkGran = C::kChunkCols / 8;
     const uint8_t* codes = stage + C::kTileBytes / 2;
     const int g = lane % kGran;
     const int c = g / kChunkGran, gg = g % kChunkGran;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-#pragma unroll 2
-        for (int r0 = 32 * q; r0 < 32 * q + 32; r0 += kRows) {
-            const int r = r0 + lane / kGran;
-            const uint2 w = *reinterpret_cast<const uint2*>(codes + r * D + g * 8);
-            const float s = __shfl_sync(0xffffffffu, sc[q], r & 31);
-            __syncwarp();
-            // code + 128 as the low mantissa byte of 2^23, minus 2^23 + 128: exact
-            const uint32_t x = w.x ^ 0x80808080u, y = w.y ^ 0x80808080u;
-            float f[8];
+#pragma unroll 1
+        for (int r0 = 32 * q; r0 < 32 * q + 32; r0 += kRows * kGroup) {
+            uint2 w[kGroup];
+            float s[kGroup];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                f[e] = (__uint_as_float(__byte_perm(x, 0x4B000000u, 0x7540u + e)) - 8388736.0f) * s;
-                f[e + 4] = (__uint_as_float(__byte_perm(y, 0x4B000000u, 0x7540u + e)) - 8388736.0f) * s;
+            for (int b = 0; b < kGroup; ++b) {
+                const int r = r0 + b * kRows + lane / kGran;
+                w[b] = *reinterpret_cast<const uint2*>(codes + r * D + g * 8);
+                s[b] = kScale ? __shfl_sync(0xffffffffu, sc[q], r & 31) : 1.f;
             }
-            const int phys = D >= 64 ? (gg ^ (r & 7)) : (gg ^ ((r >> 1) & 3));
-            *reinterpret_cast<uint4*>(stage + c * C::kChunkBytes + r * C::kRowBytes + phys * 16) =
-                make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]),
-                           pack_bf16(f[6], f[7]));
+            __syncwarp();
+#pragma unroll
+            for (int b = 0; b < kGroup; ++b) {
+                const int r = r0 + b * kRows + lane / kGran;
+                // code + 128 as the low mantissa byte of 2^23, minus 2^23 + 128: exact
+                const uint32_t x = w[b].x ^ 0x80808080u, y = w[b].y ^ 0x80808080u;
+                float f[8];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    f[e] = __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7540u + e)) - 8388736.0f;
+                    f[e + 4] = __uint_as_float(__byte_perm(y, 0x4B000000u, 0x7540u + e)) - 8388736.0f;
+                    if (kScale) {
+                        f[e] *= s[b];
+                        f[e + 4] *= s[b];
+                    }
+                }
+                const int phys = D >= 64 ? (gg ^ (r & 7)) : (gg ^ ((r >> 1) & 3));
+                *reinterpret_cast<uint4*>(stage + c * C::kChunkBytes + r * C::kRowBytes + phys * 16) =
+                    make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]),
+                               pack_bf16(f[6], f[7]));
+            }
         }
     }
 }
@@ -848,12 +863,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                     }
                     if (!warp_wait(&full[st], (t / stages) & 1, ctl, hdr)) { ok = false; break; }
                     if (is_k) {
-                        const float one[4] = {1.f, 1.f, 1.f, 1.f};
-                        dequant_tile<D>(ring + st * C::kTileBytes, one, lane);
+                        dequant_tile<D, false>(ring + st * C::kTileBytes, sc, lane);
 #pragma unroll
                         for (int q = 0; q < 4; ++q) ctl->kscale[t & 3][32 * q + lane] = sc[q];
                     } else {
-                        dequant_tile<D>(ring + st * C::kTileBytes, sc, lane);
+                        dequant_tile<D, true>(ring + st * C::kTileBytes, sc, lane);
                     }
                     fence_proxy_async_smem();
                     __syncwarp();

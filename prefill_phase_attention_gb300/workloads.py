@@ -238,9 +238,12 @@ def make_q8_cache(wl: Workload, g: torch.Generator, sentinel: bool = True):
 
     Codes int8 [num_seqs, n_kv_heads, max_cache_len, head_dim], scales fp32
     [num_seqs, n_kv_heads, max_cache_len].  The first ``wl.prefilled[b]`` rows of
-    slot b hold uniform codes in [-127, 127] (one code of each row set to +-127)
-    and scales uniform in [0.005, 0.03]; every other row holds random codes and a
-    NaN scale (or zero codes and scale 0), so a read of it shows.
+    slot b hold what int8 rows of N(0,1)-like activations look like: codes drawn
+    N(0, 36^2), rounded and clipped to [-127, 127], one code of each row set to
+    +-127 (the row maximum), and scales uniform in [0.02, 0.035], so the values
+    code * scale have about the spread of the bf16 tests' N(0,1) data.  Every
+    other row holds random codes and a NaN scale (or zero codes and scale 0), so
+    a read of it shows.
     """
     shape = (wl.num_seqs, wl.n_kv_heads, wl.max_cache_len, wl.head_dim)
     out = []
@@ -251,12 +254,12 @@ def make_q8_cache(wl: Workload, g: torch.Generator, sentinel: bool = True):
             codes.zero_()
         for b, p in enumerate(wl.prefilled):
             if p:
-                c = torch.randint(-127, 128, (wl.n_kv_heads, p, wl.head_dim), generator=g, dtype=torch.int32)
+                c = (torch.randn((wl.n_kv_heads, p, wl.head_dim), generator=g) * 36).round().clamp(-127, 127)
                 col = torch.randint(0, wl.head_dim, (wl.n_kv_heads, p, 1), generator=g)
                 sign = torch.randint(0, 2, (wl.n_kv_heads, p, 1), generator=g) * 2 - 1
-                c.scatter_(2, col, (127 * sign).to(torch.int32))
+                c.scatter_(2, col, (127 * sign).to(c.dtype))
                 codes[b, :, :p] = c.to(torch.int8)
-                scales[b, :, :p] = torch.rand((wl.n_kv_heads, p), generator=g) * 0.025 + 0.005
+                scales[b, :, :p] = torch.rand((wl.n_kv_heads, p), generator=g) * 0.015 + 0.02
         out += [codes, scales]
     return tuple(out)
 
