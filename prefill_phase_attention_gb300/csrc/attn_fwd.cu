@@ -227,7 +227,7 @@ __device__ __forceinline__ bool own_rows(int j, int np, int q0, int q_end, int& 
 // memory to consecutive cache rows starting at `dst` (one warp; 16-byte
 // granules, the warp's stores cover contiguous cache rows).
 template <int D>
-__device__ __noinline__ void copy_tile_rows(const uint8_t* tile, __nv_bfloat16* dst, int lo_row, int nrows,
+__device__ __forceinline__ void copy_tile_rows(const uint8_t* tile, __nv_bfloat16* dst, int lo_row, int nrows,
                                                int lane) {
     using C = Cfg<D>;
     constexpr int kGran = D / 8;  // 16-byte granules per row
@@ -391,7 +391,7 @@ __device__ __noinline__ void quant_tile_rows(const uint8_t* tile, int8_t* codes,
 // share one copy of this code, which keeps the kernel's hot code within the
 // instruction caches.
 template <int D, bool kQuant>
-__device__ __noinline__ bool load_kv_tile(const FwdParams& p, Ctrl* ctl, WorkspaceHeader* hdr, uint8_t* ring,
+__device__ __forceinline__ bool load_kv_tile(const FwdParams& p, Ctrl* ctl, WorkspaceHeader* hdr, uint8_t* ring,
                                           int stages, uint64_t* full, uint64_t* empty, const CUtensorMap* tm_cache,
                                           const CUtensorMap* tm_new, int* last_parity, uint32_t t, int j,
                                           const Unit& u, const SeqInfo& s, int np) {
