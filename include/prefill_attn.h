@@ -187,6 +187,16 @@ typedef struct pa_options {
     int32_t reserved3;  /* must be 0 */
     float *cache_k_scale;
     float *cache_v_scale;
+    /* Test hook, 0 in normal use.  1: in the first CTA the tensor-core warp
+     * first waits on a barrier that nothing completes.  The wait gives up
+     * after its bound (2 s), the CTA records PA_DEVERR_TIMEOUT in the device
+     * error word, drains its copies, frees its tensor memory and exits; the
+     * other CTAs finish their work units, and the rows of the units the first
+     * CTA had taken are left unwritten.  It lets a test run the timeout path on
+     * a healthy GPU: the call returns normally, prefill_attn_device_status
+     * reports PA_ERR_DEVICE_TIMEOUT, and the context stays usable. */
+    int32_t wait_timeout_test;
+    int32_t reserved4;  /* must be 0 */
 } pa_options;
 
 /*

@@ -27,7 +27,8 @@ class PaOptions(ctypes.Structure):
                 ("max_blocks_per_seq", ctypes.c_int32), ("num_blocks", ctypes.c_int32),
                 ("reserved", ctypes.c_int32), ("rope_theta", ctypes.c_float), ("reserved2", ctypes.c_int32),
                 ("kv_quant", ctypes.c_int32), ("reserved3", ctypes.c_int32),
-                ("cache_k_scale", ctypes.c_void_p), ("cache_v_scale", ctypes.c_void_p)]
+                ("cache_k_scale", ctypes.c_void_p), ("cache_v_scale", ctypes.c_void_p),
+                ("wait_timeout_test", ctypes.c_int32), ("reserved4", ctypes.c_int32)]
 
 
 # Entry points declared in include/prefill_attn.h: name -> (restype, argtypes)
@@ -127,11 +128,13 @@ def prefill_attn_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_k, cache_v, c
 
 
 def make_options(window: int = 0, block_table=None, block_size: int = 0, num_blocks: int = 0,
-                 rope_theta: float = 0.0, cache_k_scale=None, cache_v_scale=None) -> PaOptions:
+                 rope_theta: float = 0.0, cache_k_scale=None, cache_v_scale=None,
+                 wait_timeout_test: bool = False) -> PaOptions:
     o = PaOptions()
     o.struct_size = ctypes.sizeof(PaOptions)
     o.window = int(window)
     o.rope_theta = float(rope_theta)
+    o.wait_timeout_test = int(bool(wait_timeout_test))
     if cache_k_scale is not None:
         o.kv_quant = 1
         o.cache_k_scale = cache_k_scale.data_ptr()
@@ -147,7 +150,7 @@ def make_options(window: int = 0, block_table=None, block_size: int = 0, num_blo
 def prefill_attn_varlen_ex(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_k, cache_v, cache_offsets, out, lse=None, *,
                            scale: Optional[float] = None, causal: bool = True, window: int = 0,
                            block_table=None, rope_theta: float = 0.0, cache_k_scale=None, cache_v_scale=None,
-                           stream=None) -> None:
+                           wait_timeout_test: bool = False, stream=None) -> None:
     """prefill_attn_varlen with options.
 
     window > 0 restricts each query to its `window` most recent keys (causal only).
@@ -177,7 +180,7 @@ def prefill_attn_varlen_ex(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_k, cache_v
                         scale, causal, stream, max_cache_len=cap,
                         cache_dtype=torch.int8 if quant else torch.bfloat16)
     opts = make_options(window, block_table, cache_k.shape[2], cache_k.shape[0], rope_theta,
-                        cache_k_scale, cache_v_scale)
+                        cache_k_scale, cache_v_scale, wait_timeout_test)
     _check(load().prefill_attn_varlen_ex(*args[:-1], ctypes.byref(opts), args[-1]))
 
 

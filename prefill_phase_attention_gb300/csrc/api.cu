@@ -154,6 +154,7 @@ struct Options {
     int kv_quant = 0;                      // 1: int8 cache with fp32 row scales
     float* scale_k = nullptr;
     float* scale_v = nullptr;
+    int wait_timeout_test = 0;
 };
 
 // Reads the caller's options; fields past the caller's struct_size count as zero.
@@ -207,6 +208,12 @@ pa_status read_options(const pa_options* opts, int causal, Options* o) {
         o->kv_quant = 1;
         o->scale_k = opts->cache_k_scale;
         o->scale_v = opts->cache_v_scale;
+    }
+    if (have >= offsetof(pa_options, reserved4) + sizeof(int32_t)) {
+        if (opts->wait_timeout_test != 0 && opts->wait_timeout_test != 1)
+            return fail(PA_ERR_INVALID_ARG, "wait_timeout_test must be 0 or 1");
+        if (opts->reserved4 != 0) return fail(PA_ERR_INVALID_ARG, "pa_options.reserved4 must be 0");
+        o->wait_timeout_test = opts->wait_timeout_test;
     }
     return PA_OK;
 }
@@ -314,6 +321,7 @@ pa_status enqueue(const void* q, const void* k, const void* v, const int32_t* cu
     p.max_blocks = o.max_blocks;
     p.num_blocks = o.num_blocks;
     p.kv_quant = o.kv_quant;
+    p.wait_timeout_test = o.wait_timeout_test;
     p.scale_k = o.scale_k;
     p.scale_v = o.scale_v;
     e = pa::encode_fwd_maps(p, q, total_q, num_seqs, head_dim, o.num_blocks);

@@ -87,6 +87,7 @@ struct __align__(8) Ctrl {
     uint64_t v_fix[4];  // paged cache: last prefix V tile with the rows past P zeroed
     uint64_t k_conv[4], v_conv[4];  // int8 cache: prefix tile expanded to bf16
     uint64_t ks_full[4];            // int8 cache: row scales of K tile t in kscale[t % 4]
+    uint64_t never;                 // test hook: a barrier nothing completes
     uint64_t s_full[kSlots], p_full[kSlots], pv_done[kSlots], o_empty[kSlots];
     uint64_t mma_drain;
     uint64_t unit_full[2], unit_empty[2];
@@ -466,6 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             mbar_init(&ctl->unit_empty[b], 12);  // MMA + V loader + 2 cache writers + 8 softmax warps
         }
         mbar_init(&ctl->mma_drain, 1);
+        mbar_init(&ctl->never, 1);
         ctl->abort = 0;
         fence_mbar_init();
         prefetch_tmap(&p.tm_q);
@@ -710,6 +712,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             return warp_wait(&ctl->k_full[kst], (tt / C::kStagesK) & 1, ctl, hdr);
         };
         bool ok = true;
+        // Test hook: a wait that runs out, so that the timeout path (error word,
+        // abort, drain, TMEM release) runs on a healthy GPU.
+        if (p.wait_timeout_test && blockIdx.x == 0) ok = warp_wait(&ctl->never, 0, ctl, hdr);
         auto issue_s = [&](int i, uint32_t tt) {
             if (leader) {
                 const uint32_t koff = (tt % C::kStagesK) * C::kTileBytes;

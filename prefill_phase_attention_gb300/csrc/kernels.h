@@ -65,6 +65,7 @@ struct FwdParams {
     float* scale_k;
     float* scale_v;
     int kv_quant;
+    int wait_timeout_test;  // test hook: CTA 0 waits on a barrier nothing completes
 };
 
 // Encodes the tensor maps of `p` (the pointer fields and sizes must be set).
