@@ -187,8 +187,9 @@ typedef struct pa_options {
     int32_t reserved3;  /* must be 0 */
     float *cache_k_scale;
     float *cache_v_scale;
-    /* Test hook, 0 in normal use.  1: in the first CTA the tensor-core warp
-     * first waits on a barrier that nothing completes.  The wait gives up
+    /* Test hook, 0 in normal use; head_dim 128, contiguous bf16 cache only
+     * (PA_ERR_CUDA otherwise).  1: in the first CTA the producer thread first
+     * waits on a barrier that nothing completes.  The wait gives up
      * after its bound (2 s), the CTA records PA_DEVERR_TIMEOUT in the device
      * error word, drains its copies, frees its tensor memory and exits; the
      * other CTAs finish their work units, and the rows of the units the first

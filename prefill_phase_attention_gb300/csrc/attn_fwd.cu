@@ -422,10 +422,13 @@ __device__ __forceinline__ bool load_kv_tile(const FwdParams& p, Ctrl* ctl, Work
     return true;
 }
 
-template <int D, bool kPaged, bool kQuant>
+template <int D, bool kPaged, bool kQuant, bool kHook = false>
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ FwdParams p) {
     using C = Cfg<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // launched with programmatic stream serialisation: wait for the scheduler
+    // (and rotary) kernels of this call before anything else
+    griddep_wait();
     if (smem_u32(smem_raw) & 1023u) {  // swizzled TMA/UMMA tiles need 1024-byte alignment
         if (threadIdx.x == 0) atomicOr(&p.hdr->error, PA_DEVERR_TIMEOUT);
         return;
@@ -494,6 +497,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             }
         }
     };
+
+    // Test hook (a kernel of its own, so that the product kernels' code is not
+    // touched by it): the first CTA's producer thread waits on a barrier
+    // nothing completes, so that the timeout path (error word, abort, drains,
+    // TMEM release in every role) runs on a healthy GPU.
+    if (kHook && blockIdx.x == 0 && threadIdx.x == 0) wait_bar(&ctl->never, 0, ctl, hdr);
 
     if (kPaged && warp == 0) {
         // ------------------------------------- paged cache: unit fetch, Q, K and V loads
@@ -712,9 +721,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             return warp_wait(&ctl->k_full[kst], (tt / C::kStagesK) & 1, ctl, hdr);
         };
         bool ok = true;
-        // Test hook: a wait that runs out, so that the timeout path (error word,
-        // abort, drain, TMEM release) runs on a healthy GPU.
-        if (p.wait_timeout_test && blockIdx.x == 0) ok = warp_wait(&ctl->never, 0, ctl, hdr);
         auto issue_s = [&](int i, uint32_t tt) {
             if (leader) {
                 const uint32_t koff = (tt % C::kStagesK) * C::kTileBytes;
@@ -1134,7 +1140,7 @@ cudaError_t encode3d(CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, 
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int D, bool kPaged, bool kQuant>
+template <int D, bool kPaged, bool kQuant, bool kHook = false>
 cudaError_t launch_d(const FwdParams& p, int grid, cudaStream_t st) {
     constexpr int kSmem = smem_bytes<D>();
     static_assert(kSmem <= 232448, "shared memory budget");
@@ -1143,12 +1149,24 @@ cudaError_t launch_d(const FwdParams& p, int grid, cudaStream_t st) {
     cudaGetDevice(&dev);
     if (dev < 64 && !configured_for[dev]) {
         cudaError_t e =
-            cudaFuncSetAttribute(attn_fwd_kernel<D, kPaged, kQuant>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+            cudaFuncSetAttribute(attn_fwd_kernel<D, kPaged, kQuant, kHook>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmem);
         if (e != cudaSuccess) return e;
         configured_for[dev] = 1;
     }
-    attn_fwd_kernel<D, kPaged, kQuant><<<grid, kThreads, kSmem, st>>>(p);
-    return cudaGetLastError();
+    // programmatic dependent launch: the prologue may run while the previous
+    // kernel of the call finishes (the kernel waits for it before reading its output)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, attn_fwd_kernel<D, kPaged, kQuant, kHook>, p);
 }
 
 }  // namespace
@@ -1192,6 +1210,10 @@ cudaError_t encode_fwd_maps(FwdParams& p, const void* q, int total_q, int num_se
 cudaError_t launch_attn_fwd(const FwdParams& p, int head_dim, int grid, cudaStream_t st) {
     const bool paged = p.block_table != nullptr;
     if (paged && p.kv_quant) return cudaErrorNotSupported;  // not built: the int8 cache is contiguous only
+    if (p.wait_timeout_test) {  // the test hook exists for the plain d = 128 kernel only
+        if (head_dim != 128 || paged || p.kv_quant) return cudaErrorNotSupported;
+        return launch_d<128, false, false, true>(p, grid, st);
+    }
     switch (head_dim) {
         case 32:
             return paged ? launch_d<32, true, false>(p, grid, st)

@@ -239,4 +239,11 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn, in
 }
 
 }  // namespace ptx
+// Programmatic dependent launch (sm_90+): a kernel launched with programmatic
+// stream serialisation may start before the previous kernel of its stream has
+// finished; griddep_wait() blocks until that kernel has completed and its
+// memory is visible, griddep_launch() lets the next such kernel start early.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 }  // namespace pa

@@ -18,6 +18,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "ptx.cuh"
 
 namespace pa {
 
@@ -48,6 +49,7 @@ __global__ void __launch_bounds__(kRopeThreads) rope_kernel(const RopeParams p) 
     const int groups = half / 8;
     const int heads = p.n_heads + p.n_kv_heads;
     const long long t0 = (long long)blockIdx.x * tpb;
+    griddep_wait();  // the scheduler's SeqInfo
     {
         const int tt = threadIdx.x / half, i = threadIdx.x % half;
         const long long t = t0 + tt;
@@ -117,6 +119,10 @@ __global__ void __launch_bounds__(kRopeThreads) rope_kernel(const RopeParams p) 
             *reinterpret_cast<uint4*>(dst[u] + half) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
         }
     }
+    // let the attention kernel launch once every block got here (it waits for
+    // this kernel to finish before reading the rotated copies); triggering at
+    // the end keeps its persistent blocks from taking SMs this grid still needs
+    griddep_launch();
 }
 
 }  // namespace
@@ -125,8 +131,16 @@ cudaError_t launch_rope(const RopeParams& p, cudaStream_t stream) {
     const int tpb = kRopeThreads / (p.head_dim / 2);
     const long long blocks = ((long long)p.total_q + tpb - 1) / tpb;
     if (blocks == 0) return cudaSuccess;
-    rope_kernel<<<(unsigned)blocks, kRopeThreads, 0, stream>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(kRopeThreads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, rope_kernel, p);
 }
 
 }  // namespace pa

@@ -13,6 +13,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "ptx.cuh"
 #include "prefill_attn.h"
 
 namespace pa {
@@ -65,6 +66,9 @@ __global__ void __launch_bounds__(1024) build_schedule_kernel(ScheduleArgs a) {
     const int tid = threadIdx.x;
     const int nthr = blockDim.x;
     const int tpu = kSlots * (kBlockM / a.group);  // query tokens per unit
+    // the next kernel (launched with programmatic stream serialisation) may
+    // start its prologue now; it waits for this kernel before reading the list
+    griddep_launch();
 
     for (int i = tid; i < kCostBins; i += nthr) hist[i] = 0;
 

@@ -1,6 +1,6 @@
 """The device-side timeout path on a healthy GPU (no fault, no trap, no hang).
 
-With the test hook pa_options.wait_timeout_test = 1 the tensor-core warp of the
+With the test hook pa_options.wait_timeout_test = 1 the producer thread of the
 first CTA waits on a barrier that nothing completes.  The bounded wait gives up
 after 2 s; that CTA records PA_DEVERR_TIMEOUT, drains its copies, frees its
 tensor memory and exits while the other CTAs finish.  The host then reads the
