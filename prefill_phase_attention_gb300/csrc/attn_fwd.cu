@@ -81,7 +81,7 @@ struct UnitSlot {
     SeqInfo s;
 };
 
-struct __align__(8) Ctrl {
+struct __align__(16) Ctrl {
     uint64_t q_full, q_empty;
     uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
     uint64_t v_fix[4];  // paged cache: last prefix V tile with the rows past P zeroed
