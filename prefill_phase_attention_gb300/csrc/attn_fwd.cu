@@ -156,6 +156,13 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// max of three (one instruction on sm_100+)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 __device__ __forceinline__ float lg2(float x) {
     float y;
     asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -1001,10 +1008,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 #pragma unroll
                     for (int c4 = 0; c4 < kBlockN / 4; ++c4) {
                         const float4 f = ksc[c4];
-                        sv[4 * c4] *= f.x;
-                        sv[4 * c4 + 1] *= f.y;
-                        sv[4 * c4 + 2] *= f.z;
-                        sv[4 * c4 + 3] *= f.w;
+                        const float2 a = __fmul2_rn(make_float2(sv[4 * c4], sv[4 * c4 + 1]), make_float2(f.x, f.y));
+                        const float2 b = __fmul2_rn(make_float2(sv[4 * c4 + 2], sv[4 * c4 + 3]), make_float2(f.z, f.w));
+                        sv[4 * c4] = a.x;
+                        sv[4 * c4 + 1] = a.y;
+                        sv[4 * c4 + 2] = b.x;
+                        sv[4 * c4 + 3] = b.y;
                     }
                 }
                 const int kb = tile_key_base<kPaged>(jt, s.P, np);
@@ -1016,15 +1025,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                     for (int c = 0; c < kBlockN; ++c)
                         if (c < lo || c >= hi) sv[c] = -INFINITY;
                 }
-                float mx0 = sv[0], mx1 = sv[1], mx2 = sv[2], mx3 = sv[3];
+                // row max: four chains of three-input maxima
+                float mx0 = fmaxf(sv[0], sv[1]), mx1 = fmaxf(sv[2], sv[3]);
+                float mx2 = fmaxf(sv[4], sv[5]), mx3 = fmaxf(sv[6], sv[7]);
 #pragma unroll
-                for (int c = 4; c < kBlockN; c += 4) {
-                    mx0 = fmaxf(mx0, sv[c]);
-                    mx1 = fmaxf(mx1, sv[c + 1]);
-                    mx2 = fmaxf(mx2, sv[c + 2]);
-                    mx3 = fmaxf(mx3, sv[c + 3]);
+                for (int c = 8; c < kBlockN; c += 8) {
+                    mx0 = fmax3(mx0, sv[c], sv[c + 1]);
+                    mx1 = fmax3(mx1, sv[c + 2], sv[c + 3]);
+                    mx2 = fmax3(mx2, sv[c + 4], sv[c + 5]);
+                    mx3 = fmax3(mx3, sv[c + 6], sv[c + 7]);
                 }
-                const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+                const float m_tile = fmaxf(fmax3(mx0, mx1, mx2), mx3) * sl2;
                 const float m_new = fmaxf(m, m_tile);
                 float alpha = 1.f;
                 bool rescale = false;
@@ -1041,21 +1052,23 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 const float m_use = m == -INFINITY ? 0.f : m;
                 // P as bf16 pairs over the first 64 columns of S: chunk c4 of 32
                 // scores goes to the 16 columns at 16 c4, all already read above.
-                float sum0 = 0.f, sum1 = 0.f;
+                // exponent arguments and the row sum on packed fp32 pairs
+                const float2 sl2v = make_float2(sl2, sl2), negm = make_float2(-m_use, -m_use);
+                float2 sum2 = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int c4 = 0; c4 < 4; ++c4) {
                     uint32_t pk[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        const float p0 = ex2(fmaf(sv[c4 * 32 + 2 * i], sl2, -m_use));
-                        const float p1 = ex2(fmaf(sv[c4 * 32 + 2 * i + 1], sl2, -m_use));
-                        sum0 += p0;
-                        sum1 += p1;
+                        const float2 a = __ffma2_rn(make_float2(sv[c4 * 32 + 2 * i], sv[c4 * 32 + 2 * i + 1]), sl2v, negm);
+                        const float p0 = ex2(a.x);
+                        const float p1 = ex2(a.y);
+                        sum2 = __fadd2_rn(sum2, make_float2(p0, p1));
                         pk[i] = pack_bf16(p0, p1);
                     }
                     tmem_st16(s_col + c4 * 16, pk);
                 }
-                l = l * alpha + (sum0 + sum1);
+                l = l * alpha + (sum2.x + sum2.y);
                 if (rescale) {
 #pragma unroll
                     for (int c = 0; c < D; c += 32) {
@@ -1064,7 +1077,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                         tmem_wait_ld();
                         reg_fence(o);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                        for (int i = 0; i < 32; i += 2) {
+                            const float2 r = __fmul2_rn(make_float2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])),
+                                                        make_float2(alpha, alpha));
+                            o[i] = __float_as_uint(r.x);
+                            o[i + 1] = __float_as_uint(r.y);
+                        }
                         tmem_st32(o_col + c, o);
                     }
                 }
