@@ -146,3 +146,32 @@ def test_sliding_window_chunk_over_cached_prefix():
                     seed=31)
     for window in (64, 333, 1024):
         _run_single_step(wl, window=window)
+
+
+def test_many_sequences_sampled():
+    """5000 sequences in one launch (more than one 1024-sequence pass of the
+    scheduler): mostly one-token decode rows over cached contexts, some short
+    prompts, some empty; GQA 16/2, d 64; sampled rows and the whole cache."""
+    rng = np.random.default_rng(77)
+    B = 5000
+    lens = rng.choice([0, 1, 1, 1, 3, 17, 130], size=B).tolist()
+    pref = rng.integers(0, 300, size=B).tolist()
+    cap = max(p + n for p, n in zip(pref, lens)) + 1
+    wl = W.Workload("many", 16, 2, 64, cap, [W.Step(lens, pref)], pref, seed=78)
+    rows = PT.sample_rows(wl.steps[0], wl.n_heads, 2, seed=79)
+    _run_single_step(wl, rows=rows)
+
+
+def test_single_token_total():
+    """total_q = 1: one decode row, nothing else."""
+    wl = W.Workload("one_tok", 8, 2, 64, 70, [W.Step([1], [64])], [64], seed=80)
+    _run_single_step(wl)
+
+
+def test_query_block_edges():
+    """Prompts whose lengths sit on and next to the 128-row tile and the 256-row
+    work-unit edges, over prefixes on and next to tile edges."""
+    lens = [127, 128, 129, 255, 256, 257]
+    pref = [0, 127, 128, 129, 255, 256]
+    wl = W.Workload("edges", 16, 4, 128, 600, [W.Step(lens, pref)], pref, seed=81)
+    _run_single_step(wl)
