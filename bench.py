@@ -235,7 +235,13 @@ def run_ours(args, ws, rank, local):
     cache_k, cache_v, steps = inputs
     table_d = None
     sk_d = sv_d = None
-    if args.kv_quant:
+    if args.kv_quant and args.paged:
+        # int8 codes + fp32 row scales in block pools
+        table, codes_k, scales_k, codes_v, scales_v = W.make_paged_q8_cache(
+            wl, args.paged, torch.Generator().manual_seed(wl.seed), sentinel=False)
+        ck, sk_d, cv, sv_d, table_d = codes_k.cuda(), scales_k.cuda(), codes_v.cuda(), scales_v.cuda(), table.cuda()
+        del codes_k, codes_v
+    elif args.kv_quant:
         # the same workload over an int8 cache (codes + fp32 row scales)
         codes_k, scales_k, codes_v, scales_v = W.make_q8_cache(wl, torch.Generator().manual_seed(wl.seed),
                                                                sentinel=False)

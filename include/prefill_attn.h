@@ -181,8 +181,10 @@ typedef struct pa_options {
      * nearest integer, ties to even, of x / scale (fp32 division), clamped to
      * +-127; an all-zero row is scale 0, codes 0.  The cached prefix is read
      * dequantised (code * scale, rounded to bf16 for the tensor cores); the
-     * chunk's own keys and values are used at full precision.  Not combined
-     * with block_table (PA_ERR_UNSUPPORTED). */
+     * chunk's own keys and values are used at full precision.  With a
+     * block_table the code and scale pools are [num_blocks, n_kv_heads,
+     * block_size, head_dim] int8 and [num_blocks, n_kv_heads, block_size]
+     * fp32, addressed through the table like the bf16 pools. */
     int32_t kv_quant;
     int32_t reserved3;  /* must be 0 */
     float *cache_k_scale;

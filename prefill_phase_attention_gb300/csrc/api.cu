@@ -204,7 +204,6 @@ pa_status read_options(const pa_options* opts, int causal, Options* o) {
             return fail(PA_ERR_INVALID_ARG, "kv_quant = 1 needs cache_k_scale and cache_v_scale");
         if ((reinterpret_cast<uintptr_t>(opts->cache_k_scale) | reinterpret_cast<uintptr_t>(opts->cache_v_scale)) & 3u)
             return fail(PA_ERR_INVALID_ARG, "cache scales must be 4-byte aligned");
-        if (o->block_table) return fail(PA_ERR_UNSUPPORTED, "kv_quant is not combined with a paged cache");
         o->kv_quant = 1;
         o->scale_k = opts->cache_k_scale;
         o->scale_v = opts->cache_v_scale;

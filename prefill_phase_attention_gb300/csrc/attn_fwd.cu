@@ -349,12 +349,12 @@ __device__ __noinline__ void dequant_tile(uint8_t* stage, const float (&sc)[4], 
 }
 
 // int8 cache write: rows [lo_row, lo_row + nrows) of a staged bf16 tile as
-// int8 codes at codes + i * D and their scales at scales[i] (consecutive cache
-// rows).  Per row, in fp32: scale = max|x| / 127, code = nearest integer (ties
+// int8 codes at codes + row * D and their scales at scales[row], row =
+// row_index(i) (~0: skip).  Per row, in fp32: scale = max|x| / 127, code = nearest integer (ties
 // to even) of x / scale, clamped to +-127; a zero row is scale 0, codes 0.
-template <int D>
-__device__ __noinline__ void quant_tile_rows(const uint8_t* tile, int8_t* codes, float* scales, int lo_row,
-                                             int nrows, int lane) {
+template <int D, class RowIndex>
+__device__ __noinline__ void quant_tile_rows(const uint8_t* tile, int8_t* codes, float* scales, RowIndex row_index,
+                                             int lo_row, int nrows, int lane) {
     using C = Cfg<D>;
     constexpr int kGran = D / 8;  // lanes per row
     constexpr int kRows = 32 / kGran;
@@ -387,8 +387,11 @@ __device__ __noinline__ void quant_tile_rows(const uint8_t* tile, int8_t* codes,
             packed[e >> 2] |= (uint32_t)(qv & 0xff) << (8 * (e & 3));
         }
         if (valid) {
-            *reinterpret_cast<uint2*>(codes + (size_t)i * D + g * 8) = make_uint2(packed[0], packed[1]);
-            if (g == 0) scales[i] = sc;
+            const size_t row = row_index(i);  // cache row of the staged row lo_row + i
+            if (row != ~size_t(0)) {
+                *reinterpret_cast<uint2*>(codes + row * D + g * 8) = make_uint2(packed[0], packed[1]);
+                if (g == 0) scales[row] = sc;
+            }
         }
     }
 }
@@ -589,7 +592,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 if (jj < ug.np) {
                     const int kb = kBlockN * jj;
                     const int boxes = (min(kBlockN, s.P - kb) + br - 1) / br;
-                    const int b0 = gl / C::kChunks, b1 = (gl + 16) / C::kChunks;
+                    // int8 cache: one box per block (all D columns); bf16: one per (block, chunk)
+                    const int b0 = kQuant ? gl : gl / C::kChunks, b1 = kQuant ? gl + 16 : (gl + 16) / C::kChunks;
                     if (b0 < boxes) id0 = __ldg(tab + ((kb + b0 * br) >> p.block_log2));
                     if (b1 < boxes) id1 = __ldg(tab + ((kb + b1 * br) >> p.block_log2));
                 }
@@ -605,7 +609,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 if (!__shfl_sync(gmask, ok, src)) { ok = false; break; }
                 const int kb = tile_key_base<true>(jj, s.P, ug.np);
                 uint8_t* stage = ring + st * C::kTileBytes;
-                if (jj < ug.np) {
+                if (kQuant && jj < ug.np) {
+                    // int8 codes, one box of br rows x D bytes per block, into the
+                    // stage's upper half (expanded to bf16 by the cache writer)
+                    const int boxes = (min(kBlockN, s.P - kb) + br - 1) / br;
+                    if (gleader) mbar_arrive_expect_tx(&full[st], boxes * br * D);
+                    __syncwarp(gmask);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int box = gl + 16 * h;
+                        if (box < boxes)
+                            tma_load_3d(stage + C::kTileBytes / 2 + box * br * D, tm_cache, &full[st], 0,
+                                        (kb + box * br) & bmask, (h ? id1 : id0) * p.n_kv_heads + u.kvh);
+                    }
+                } else if (jj < ug.np) {
                     const int boxes = (min(kBlockN, s.P - kb) + br - 1) / br;
                     if (gleader) mbar_arrive_expect_tx(&full[st], boxes * br * C::kRowBytes * C::kChunks);
                     __syncwarp(gmask);
@@ -786,12 +803,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                         if (!v_ready) {
                             const int vst = tj % C::kStagesV;
                             bool got;
-                            if (kPaged && paged_tail_tile(ug.lo + j, s.P, ug.np)) {
-                                got = warp_wait(&ctl->v_fix[vst], (fixpar >> vst) & 1, ctl, hdr);
-                                fixpar ^= 1u << vst;
-                            } else if (kQuant && ug.lo + j < ug.np) {
+                            if (kQuant && ug.lo + j < ug.np) {
+                                // int8 prefix tile (a paged tail included: its rows past P
+                                // get scale 0 in the expansion)
                                 got = warp_wait(&ctl->v_conv[vst], (vcpar >> vst) & 1, ctl, hdr);
                                 vcpar ^= 1u << vst;
+                            } else if (kPaged && paged_tail_tile(ug.lo + j, s.P, ug.np)) {
+                                got = warp_wait(&ctl->v_fix[vst], (fixpar >> vst) & 1, ctl, hdr);
+                                fixpar ^= 1u << vst;
                             } else {
                                 got = warp_wait(&ctl->v_full[vst], (tj / C::kStagesV) & 1, ctl, hdr);
                             }
@@ -870,14 +889,32 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                     // int8 prefix tile: expand the codes for the MMA.  V rows
                     // become code * scale; K rows stay the (exact) codes and
                     // their scales go to the scale ring, folded into the scores.
-                    const int kb = tile_key_base<false>(j, us.s.P, np);
-                    const float* srow = (is_k ? p.scale_k : p.scale_v) +
-                                        ((size_t)us.u.b * p.n_kv_heads + us.u.kvh) * p.max_cache_len;
+                    const int kb = tile_key_base<kPaged>(j, us.s.P, np);
+                    const float* scales = is_k ? p.scale_k : p.scale_v;
                     float sc[4];
+                    if (kPaged) {
+                        // row scales through the block table; rows from P on (rest of the
+                        // last block, stale rows) get scale 0 and so expand to zeros
+                        const int32_t* tab = p.block_table + (size_t)us.u.b * p.max_blocks;
+                        const int bmask = (1 << p.block_log2) - 1;
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const int row = kb + 32 * q + lane;  // rows below 0 are zero-filled codes
-                        sc[q] = row >= 0 ? __ldg(srow + row) : 0.f;
+                        for (int q = 0; q < 4; ++q) {
+                            const int pos = kb + 32 * q + lane;
+                            sc[q] = 0.f;
+                            if (pos < us.s.P) {
+                                const int blk = __ldg(tab + (pos >> p.block_log2));
+                                if ((unsigned)blk < (unsigned)p.num_blocks)
+                                    sc[q] = __ldg(scales + ((((size_t)blk * p.n_kv_heads + us.u.kvh) << p.block_log2) +
+                                                            (pos & bmask)));
+                            }
+                        }
+                    } else {
+                        const float* srow = scales + ((size_t)us.u.b * p.n_kv_heads + us.u.kvh) * p.max_cache_len;
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const int row = kb + 32 * q + lane;  // rows below 0 are zero-filled codes
+                            sc[q] = row >= 0 ? __ldg(srow + row) : 0.f;
+                        }
                     }
                     if (!warp_wait(&full[st], (t / stages) & 1, ctl, hdr)) { ok = false; break; }
                     if (is_k) {
@@ -900,11 +937,25 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 int lo_row, nrows;
                 if (own_rows(j, np, us.u.q0, q_end, lo_row, nrows)) {
                     const int first_tok = (j - np) * kBlockN + lo_row;  // token index within the sequence
-                    if (kQuant) {
+                    if (kQuant && kPaged) {
+                        const int32_t* tab = p.block_table + (size_t)us.u.b * p.max_blocks;
+                        const int pos0 = us.s.P + first_tok, lg = p.block_log2, Hk = p.n_kv_heads, kvh = us.u.kvh;
+                        const int nb = p.num_blocks;
+                        quant_tile_rows<D>(ring + st * C::kTileBytes, reinterpret_cast<int8_t*>(cache),
+                                           is_k ? p.scale_k : p.scale_v,
+                                           [=](int i) -> size_t {
+                                               const int pos = pos0 + i;
+                                               const int blk = __ldg(tab + (pos >> lg));
+                                               if ((unsigned)blk >= (unsigned)nb) return ~size_t(0);
+                                               return (((size_t)blk * Hk + kvh) << lg) + (pos & ((1 << lg) - 1));
+                                           },
+                                           lo_row, nrows, lane);
+                    } else if (kQuant) {
                         const size_t row0 = ((size_t)us.u.b * p.n_kv_heads + us.u.kvh) * p.max_cache_len +
                                             us.s.P + first_tok;
-                        quant_tile_rows<D>(ring + st * C::kTileBytes, reinterpret_cast<int8_t*>(cache) + row0 * D,
-                                           (is_k ? p.scale_k : p.scale_v) + row0, lo_row, nrows, lane);
+                        quant_tile_rows<D>(ring + st * C::kTileBytes, reinterpret_cast<int8_t*>(cache),
+                                           is_k ? p.scale_k : p.scale_v, [=](int i) -> size_t { return row0 + i; },
+                                           lo_row, nrows, lane);
                     } else if (kPaged) {
                         copy_tile_rows_paged<D>(ring + st * C::kTileBytes, cache,
                                                 p.block_table + (size_t)us.u.b * p.max_blocks, p.block_log2,
@@ -1201,6 +1252,15 @@ cudaError_t encode_fwd_maps(FwdParams& p, const void* q, int total_q, int num_se
     if (e != cudaSuccess) return e;
     e = encode3d(&p.tm_v, p.v, D, Hk, T, D * 2, Hk * D * 2, cc, 1, kBlockN, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
     if (e != cudaSuccess) return e;
+    if (p.block_table && p.kv_quant) {
+        // int8 pools [num_blocks, Hk, bs, D] viewed (D, bs, num_blocks * Hk), box (D, min(bs, 128), 1)
+        const uint64_t bs = 1ull << p.block_log2, Z = (uint64_t)num_blocks * Hk;
+        e = encode3d(&p.tm_ck, p.cache_k, D, bs, Z, D, bs * D, (uint32_t)D, p.box_rows, 1, CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_DATA_TYPE_UINT8);
+        if (e != cudaSuccess) return e;
+        return encode3d(&p.tm_cv, p.cache_v, D, bs, Z, D, bs * D, (uint32_t)D, p.box_rows, 1, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_DATA_TYPE_UINT8);
+    }
     if (p.block_table) {
         // pool [num_blocks, Hk, bs, D] viewed (D, bs, num_blocks * Hk)
         const uint64_t bs = 1ull << p.block_log2, Z = (uint64_t)num_blocks * Hk;
@@ -1227,20 +1287,19 @@ cudaError_t encode_fwd_maps(FwdParams& p, const void* q, int total_q, int num_se
 
 cudaError_t launch_attn_fwd(const FwdParams& p, int head_dim, int grid, cudaStream_t st) {
     const bool paged = p.block_table != nullptr;
-    if (paged && p.kv_quant) return cudaErrorNotSupported;  // not built: the int8 cache is contiguous only
     if (p.wait_timeout_test) {  // the test hook exists for the plain d = 128 kernel only
         if (head_dim != 128 || paged || p.kv_quant) return cudaErrorNotSupported;
         return launch_d<128, false, false, true>(p, grid, st);
     }
     switch (head_dim) {
         case 32:
-            return paged ? launch_d<32, true, false>(p, grid, st)
+            return paged ? (p.kv_quant ? launch_d<32, true, true>(p, grid, st) : launch_d<32, true, false>(p, grid, st))
                          : (p.kv_quant ? launch_d<32, false, true>(p, grid, st) : launch_d<32, false, false>(p, grid, st));
         case 64:
-            return paged ? launch_d<64, true, false>(p, grid, st)
+            return paged ? (p.kv_quant ? launch_d<64, true, true>(p, grid, st) : launch_d<64, true, false>(p, grid, st))
                          : (p.kv_quant ? launch_d<64, false, true>(p, grid, st) : launch_d<64, false, false>(p, grid, st));
         case 128:
-            return paged ? launch_d<128, true, false>(p, grid, st)
+            return paged ? (p.kv_quant ? launch_d<128, true, true>(p, grid, st) : launch_d<128, true, false>(p, grid, st))
                          : (p.kv_quant ? launch_d<128, false, true>(p, grid, st)
                                        : launch_d<128, false, false>(p, grid, st));
         default: return cudaErrorInvalidValue;

@@ -264,6 +264,44 @@ def make_q8_cache(wl: Workload, g: torch.Generator, sentinel: bool = True):
     return tuple(out)
 
 
+def make_paged_q8_cache(wl: Workload, block_size: int, g: torch.Generator, extra_blocks: int = 3,
+                        sentinel: bool = True):
+    """A paged int8 cache: (block_table, codes_k, scales_k, codes_v, scales_v).
+
+    The table and block placement are drawn as in make_paged_cache; the pools
+    are int8 [num_blocks, n_kv_heads, block_size, head_dim] and fp32
+    [num_blocks, n_kv_heads, block_size], filled as make_q8_cache fills a slot:
+    prefilled positions hold N(0, 36^2)-like codes (one +-127 per row) and
+    scales in [0.02, 0.035], every other row random codes and a NaN scale.
+    """
+    B, Hk, d = wl.num_seqs, wl.n_kv_heads, wl.head_dim
+    max_blocks = -(-wl.max_cache_len // block_size)
+    num_blocks = B * max_blocks + extra_blocks
+    perm = torch.randperm(num_blocks, generator=g)[: B * max_blocks]
+    table = perm.to(torch.int32).reshape(B, max_blocks)
+    out = [table]
+    for _ in range(2):
+        codes = torch.randint(-127, 128, (num_blocks, Hk, block_size, d), generator=g, dtype=torch.int32).to(torch.int8)
+        scales = torch.full((num_blocks, Hk, block_size), float("nan") if sentinel else 0.0, dtype=torch.float32)
+        if not sentinel:
+            codes.zero_()
+        for b, p in enumerate(wl.prefilled):
+            if not p:
+                continue
+            c = (torch.randn((Hk, p, d), generator=g) * 36).round().clamp(-127, 127)
+            col = torch.randint(0, d, (Hk, p, 1), generator=g)
+            sign = torch.randint(0, 2, (Hk, p, 1), generator=g) * 2 - 1
+            c.scatter_(2, col, (127 * sign).to(c.dtype))
+            sc = torch.rand((Hk, p), generator=g) * 0.015 + 0.02
+            for L in range(-(-p // block_size)):
+                rows = min(block_size, p - L * block_size)
+                blk = int(table[b, L])
+                codes[blk, :, :rows] = c[:, L * block_size: L * block_size + rows].to(torch.int8)
+                scales[blk, :, :rows] = sc[:, L * block_size: L * block_size + rows]
+        out += [codes, scales]
+    return tuple(out)
+
+
 def make_step_inputs(wl: Workload, step: Step, g: torch.Generator):
     """q [T,H,d], k/v [T,Hk,d] bf16 and the int32 metadata of one launch (CPU)."""
     t = step.total_q

@@ -139,26 +139,36 @@ def compare_rotated_cache(got_bits, ref_bits, label=""):
     return int(diff.sum())
 
 
-def run_step_gpu_q8(wl, inp, ck, sk, cv, sv, window=0, rope_theta=0.0):
-    """One launch over an int8 cache (codes + fp32 row scales, CUDA tensors)."""
+def run_step_gpu_q8(wl, inp, ck, sk, cv, sv, window=0, rope_theta=0.0, block_table=None):
+    """One launch over an int8 cache (codes + fp32 row scales, CUDA tensors);
+    block_table (CUDA int32) selects paged pools."""
     dev = {k: v.cuda() for k, v in inp.items()}
     T = inp["q"].shape[0]
     out = Guarded((T, wl.n_heads, wl.head_dim), torch.bfloat16)
     lse = Guarded((T, wl.n_heads), torch.float32)
     binding.prefill_attn_varlen_ex(dev["q"], dev["k"], dev["v"], dev["cu_seqlens_q"], dev["cu_seqlens_k"],
                                    ck, cv, dev["cache_offsets"], out.t, lse.t, scale=wl.scale, causal=wl.causal,
-                                   window=window, rope_theta=rope_theta, cache_k_scale=sk, cache_v_scale=sv)
+                                   window=window, rope_theta=rope_theta, cache_k_scale=sk, cache_v_scale=sv,
+                                   block_table=block_table)
     torch.cuda.synchronize()
     assert out.guards_intact() and lse.guards_intact(), "write outside out/lse"
     assert binding.prefill_attn_device_status() == 0
     return out.t, lse.t
 
 
-def oracle_step_q8(wl, inp, ck, sk, cv, sv, rows=None, window=0, rope_theta=0.0, want_cache=True):
-    """The oracle over an int8 cache (numpy codes/scales); cache images are (codes, scales)."""
+def oracle_step_q8(wl, inp, ck, sk, cv, sv, rows=None, window=0, rope_theta=0.0, want_cache=True,
+                   block_table=None):
+    """The oracle over an int8 cache (numpy codes/scales); cache images are (codes, scales).
+    block_table (CPU int32 [B, max_blocks]): the codes/scales are paged pools."""
+    cap, bs = wl.max_cache_len, 0
+    if block_table is not None:
+        bs = ck.shape[2]
+        cap = block_table.shape[1] * bs
+        block_table = np.ascontiguousarray(block_table, np.int32)
     return oracle.prefill_attention(
         W.bf16_bits(inp["q"]), W.bf16_bits(inp["k"]), W.bf16_bits(inp["v"]),
         inp["cu_seqlens_q"].numpy(), inp["cu_seqlens_k"].numpy(), inp["cache_offsets"].numpy(),
         ck, cv, n_heads=wl.n_heads, n_kv_heads=wl.n_kv_heads, head_dim=wl.head_dim,
-        max_cache_len=wl.max_cache_len, scale=wl.scale, causal=wl.causal, window=window, rows=rows,
-        rope_theta=rope_theta, kv_quant=1, cache_k_scale=sk, cache_v_scale=sv, want_cache=want_cache)
+        max_cache_len=cap, scale=wl.scale, causal=wl.causal, window=window, rows=rows,
+        rope_theta=rope_theta, kv_quant=1, cache_k_scale=sk, cache_v_scale=sv, want_cache=want_cache,
+        block_table=block_table, block_size=bs)

@@ -116,7 +116,6 @@ _PAGED = dict(block_table=256, block_size=8, max_blocks=1, num_blocks=4)
     (dict(kv_quant=1, sk=514, sv=1024), 1, "aligned"),
     (dict(kv_quant=1, sk=512, sv=1024, reserved3=1), 1, "reserved3"),
     (dict(kv_quant=1, sk=512, sv=1024, struct_size=48), 1, "scale pointers"),
-    (dict(_PAGED, kv_quant=1, sk=512, sv=1024), 2, "paged"),
     (dict(wait_timeout_test=2), 1, "wait_timeout_test"),
     (dict(reserved4=5), 1, "reserved4"),
 ])

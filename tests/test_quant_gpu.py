@@ -128,3 +128,58 @@ def test_quant_codes_of_special_rows():
     assert np.array_equal(gk[0, 1, 1], exp) and gs[0, 1, 1] == np.float32(1 / 8)
     assert not gk[0, 1, 0].any() and gs[0, 1, 0] == 0.0 and not gk[0, :, 2].any()
     assert np.array_equal(cv.cpu().numpy()[0, 0, 0], exp) and sv.cpu().numpy()[0, 0, 0] == np.float32(0.25)
+
+
+
+def _paged_new_rows(shape, step, table, bs):
+    m = np.zeros(shape[:-1], dtype=bool)
+    for b, (n, P) in enumerate(zip(step.seqlens_q, step.cache_offsets)):
+        for pos in range(P, P + n):
+            m[int(table[b, pos // bs]), :, pos % bs] = True
+    return m
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_quant_paged_random_shapes(seed):
+    """The int8 cache in block pools (block sizes 8 .. 256, random placement):
+    partial last prefix blocks hold NaN-scaled rows that must expand to zeros."""
+    d = [32, 64, 128][seed % 3]
+    group = [1, 2, 4, 8][(seed // 3) % 4]
+    bs = [8, 16, 32, 64, 128, 256][(seed // 2) % 6]
+    window = 90 if seed % 5 == 3 else 0
+    rope = 10000.0 if seed % 6 == 5 else 0.0
+    wl = W.random_workload(1300 + seed, head_dim=d, group=group, n_kv_heads=2, max_prefix=500)
+    _, _, (inp,) = W.make_inputs(wl)
+    table, ck, sk, cv, sv = W.make_paged_q8_cache(wl, bs, torch.Generator().manual_seed(seed))
+    sk_d = PT.Guarded(sk.shape, torch.float32, fill=sk)
+    sv_d = PT.Guarded(sv.shape, torch.float32, fill=sv)
+    ck_d, cv_d = ck.cuda(), cv.cuda()
+    out, lse = PT.run_step_gpu_q8(wl, inp, ck_d, sk_d.t, cv_d, sv_d.t, window=window, rope_theta=rope,
+                                  block_table=table.cuda())
+    assert sk_d.guards_intact() and sv_d.guards_intact(), "write outside the scale pools"
+    ro, rl, (rk, rsk), (rv, rsv) = PT.oracle_step_q8(wl, inp, ck.numpy(), sk.numpy(), cv.numpy(), sv.numpy(),
+                                                     window=window, rope_theta=rope, block_table=table.numpy())
+    PT.compare(out, lse, ro, rl, label=f"{wl.name} int8 paged bs={bs}")
+    got = (ck_d.cpu().numpy(), sk_d.t.cpu().numpy(), cv_d.cpu().numpy(), sv_d.t.cpu().numpy())
+    _check_cache(got, (rk, rsk, rv, rsv), _paged_new_rows(ck.shape, wl.steps[0], table, bs), bool(rope), wl.name)
+
+
+def test_quant_paged_chunked_decode_sampled():
+    """chunked_decode over 16-token int8 blocks, 16 launches, sampled rows."""
+    wl = W.get("chunked_decode")
+    _, _, steps = W.make_inputs(wl)
+    bs = 16
+    table, ck, sk, cv, sv = W.make_paged_q8_cache(wl, bs, torch.Generator().manual_seed(6))
+    ck_d, sk_d, cv_d, sv_d, table_d = ck.cuda(), sk.cuda(), cv.cuda(), sv.cuda(), table.cuda()
+    rk, rsk, rv, rsv = ck.numpy(), sk.numpy(), cv.numpy(), sv.numpy()
+    for s, inp in enumerate(steps):
+        out, lse = PT.run_step_gpu_q8(wl, inp, ck_d, sk_d, cv_d, sv_d, block_table=table_d)
+        rows = PT.sample_rows(wl.steps[s], wl.n_heads, 12, seed=500 + s)
+        ro, rl, (rk, rsk), (rv, rsv) = PT.oracle_step_q8(wl, inp, rk, rsk, rv, rsv, rows=rows,
+                                                         block_table=table.numpy())
+        PT.compare(out, lse, ro, rl, rows=rows, label=f"int8 paged chunked step {s}")
+    got = (ck_d.cpu().numpy(), sk_d.cpu().numpy(), cv_d.cpu().numpy(), sv_d.cpu().numpy())
+    new = np.zeros(ck.shape[:-1], dtype=bool)
+    for st in wl.steps:
+        new |= _paged_new_rows(ck.shape, st, table, bs)
+    _check_cache(got, (rk, rsk, rv, rsv), new, False, "int8 paged chunked_decode")
