@@ -37,6 +37,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "causal varlen prefill attention TFLOP/s and tokens/s; % of GB300 BF16 peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_BYTES = 129e6  # GB300 L2
 
 
 # --------------------------------------------------------------------- utils --
@@ -280,10 +281,26 @@ def run_ours(args, ws, rank, local):
     if binding.prefill_attn_device_status() != 0:
         raise RuntimeError("device error word set during warm-up")
 
+    # L2: a working set larger than L2 needs no flush; a smaller one is timed
+    # cold (a 256 MB buffer written before every step, outside the timed spans)
+    ws_bytes = wl.tokens() * (wl.n_heads + 2 * wl.n_kv_heads) * wl.head_dim * 2
+    flush = None if ws_bytes > L2_BYTES else torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    hot_ms_step = None
+    if flush is not None:  # the same steps back to back with a warm L2, for reference
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        hot_ms_step = e0.elapsed_time(e1) / args.steps
+
     # timed region: K steps, per-launch events for the roofline
     n_launch = len(dev)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps * n_launch)]
+    step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
     e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
     sampler.start()
@@ -293,18 +310,23 @@ def run_ours(args, ws, rank, local):
     torch.cuda.synchronize()
     e_start.record(stream)
     k = 0
-    for _ in range(args.steps):
+    for si in range(args.steps):
+        if flush is not None:
+            flush.fill_(si & 0xFF)  # evict L2 (not inside the step's timed span)
+        step_ev[si][0].record(stream)
         for d, o, l in zip(dev, outs, lses):
             ev[k][0].record(stream)
             call(d, o, l)
             ev[k][1].record(stream)
             launches += binding.prefill_attn_last_launch_count()
             k += 1
+        step_ev[si][1].record(stream)
     e_end.record(stream)
     torch.cuda.synchronize()
     barrier(ws)
     clocks = sampler.stop()
-    ms_total = e_start.elapsed_time(e_end)
+    # cold L2: the sum of the steps' own spans; otherwise the whole region
+    ms_total = sum(a.elapsed_time(b) for a, b in step_ev) if flush is not None else e_start.elapsed_time(e_end)
     ms_total = max_over_ranks(ms_total, ws, device=torch.device("cuda", local))
     if binding.prefill_attn_device_status() != 0:
         raise RuntimeError("device error word set during the timed region")
@@ -325,6 +347,20 @@ def run_ours(args, ws, rank, local):
     fl_tot = sum(f for f, _ in per_launch)
     t_tot = sum(t for _, t in per_launch)
     achieved = fl_tot / (t_tot * 1e-3) / 1e12
+    # mixed roofline of a step: tensor time of its FLOPs vs HBM time of its
+    # algorithmic bytes (q, k, v read; out, lse, cache rows written; cached
+    # prefix read once), the larger of the two against the measured step time
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    kv_row = wl.n_kv_heads * wl.head_dim * (1 if args.kv_quant else 2) + (4 * wl.n_kv_heads if args.kv_quant else 0)
+    bytes_step = sum(st.total_q * (2 * wl.n_heads + 2 * wl.n_kv_heads) * wl.head_dim * 2 + 4 * st.total_q * wl.n_heads
+                     + 2 * st.total_q * kv_row + 2 * kv_row * sum(st.cache_offsets) for st in wl.steps)
+    t_tensor = flops_step / (peak * 1e12) * 1e3
+    t_hbm = bytes_step / (hbm_peak * 1e9) * 1e3
+    mixed = {"flops_per_step": flops_step, "bytes_per_step": int(bytes_step),
+             "t_tensor_ms": round(t_tensor, 4), "t_hbm_ms": round(t_hbm, 4),
+             "bound": "tensor" if t_tensor >= t_hbm else "hbm",
+             "frac": round(max(t_tensor, t_hbm) / ms_step, 4),
+             "peaks": f"{peak} TFLOP/s bf16 sustained, {hbm_peak} GB/s copy ({peak_src})"}
     traffic = None
     variant = (f"_window{args.window}" if args.window else "") + (f"_paged{args.paged}" if args.paged else "") \
         + ("_rope" if args.rope else "") + ("_int8kv" if args.kv_quant else "")
@@ -404,8 +440,10 @@ def run_ours(args, ws, rank, local):
                    "tokens_per_step": wl.tokens(), "n_heads": wl.n_heads, "n_kv_heads": wl.n_kv_heads,
                    "head_dim": wl.head_dim, "causal": wl.causal, "causal_flops_per_step": flops_step,
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
-                   "l2": "inputs larger than L2 (no flush)" if wl.tokens() * (wl.n_heads + 2 * wl.n_kv_heads)
-                         * wl.head_dim * 2 > 129e6 else "inputs smaller than L2 (hot L2)"},
+                   "l2": "inputs larger than L2 (no flush)" if flush is None else
+                         "inputs smaller than L2: a 256 MB buffer is written before every timed step (cold L2); "
+                         "value_hot_l2 is the same steps back to back"},
+        "roofline_mixed": mixed,
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside back-to-back steps)",
@@ -417,6 +455,7 @@ def run_ours(args, ws, rank, local):
                         "(wall clock over the steps); copies on two copy streams with a second buffer set, "
                         "overlapping the neighbouring steps' compute; KV cache stays device-resident"},
         "gpu_launches": launches,
+        "value_hot_l2": None if hot_ms_step is None else round(flops_step / (hot_ms_step * 1e-3) / 1e12 * ws, 2),
         "clocks": clocks,
     }
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
