@@ -323,10 +323,10 @@ def _sdpa_reference(wl, ck, cv, inp, causal, window=0):
     return out.numpy()
 
 
-@pytest.mark.parametrize("case", ["tiny_packed", "r1", "r2", "r3", "r4"])
+@pytest.mark.parametrize("case", ["tiny_packed", "layer512", "r1", "r2", "r3", "r4"])
 @pytest.mark.parametrize("causal", [True, False])
 def test_matches_torch_sdpa_float64(oracle_mod, case, causal):
-    if case == "tiny_packed":
+    if case in ("tiny_packed", "layer512"):  # the 3-prompt packing and the 7B-layer configs
         wl = W.get(case)
     else:
         i = int(case[1:])

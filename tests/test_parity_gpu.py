@@ -175,3 +175,33 @@ def test_query_block_edges():
     pref = [0, 127, 128, 129, 255, 256]
     wl = W.Workload("edges", 16, 4, 128, 600, [W.Step(lens, pref)], pref, seed=81)
     _run_single_step(wl)
+
+
+def test_prompt_16_chunks_equals_one_launch_on_gpu():
+    """The chunked workload's 8192-token prompt (GQA 32/8, d 128) as 16 launches of
+    512 tokens over the cache they fill == one 8192-token launch: outputs within
+    the tolerances of each other (and of the oracle on sampled rows), caches
+    bit-exact."""
+    H, Hk, d, n, c = 32, 8, 128, 8192, 512
+    one = W.Workload("prompt8k", H, Hk, d, n, [W.Step([n], [0])], [0], seed=4)
+    ck, cv, (inp,) = W.make_inputs(one)
+    ck1, cv1 = ck.cuda(), cv.cuda()
+    out1, lse1 = PT.run_step_gpu(one, inp, ck1, cv1)
+    ck2, cv2 = ck.cuda(), cv.cuda()
+    outs, lses = [], []
+    for s in range(n // c):
+        sl = slice(s * c, (s + 1) * c)
+        sub = dict(q=inp["q"][sl], k=inp["k"][sl], v=inp["v"][sl],
+                   cu_seqlens_q=torch.tensor([0, c], dtype=torch.int32),
+                   cu_seqlens_k=torch.tensor([0, s * c + c], dtype=torch.int32),
+                   cache_offsets=torch.tensor([s * c], dtype=torch.int32))
+        o, l = PT.run_step_gpu(one, sub, ck2, cv2)
+        outs.append(o.clone())
+        lses.append(l.clone())
+    out2, lse2 = torch.cat(outs), torch.cat(lses)
+    PT.compare(out2, lse2, out1.double().cpu().numpy(), lse1.double().cpu().numpy(), label="16 chunks vs one")
+    assert torch.equal(ck1.view(torch.int16), ck2.view(torch.int16))
+    assert torch.equal(cv1.view(torch.int16), cv2.view(torch.int16))
+    rows = PT.sample_rows(one.steps[0], H, 64, seed=11)
+    ref_out, ref_lse, _, _ = PT.oracle_step(one, inp, W.bf16_bits(ck), W.bf16_bits(cv), rows=rows, want_cache=False)
+    PT.compare(out2, lse2, ref_out, ref_lse, rows=rows, label="16 chunks vs oracle")
