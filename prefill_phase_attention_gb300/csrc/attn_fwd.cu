@@ -70,8 +70,8 @@ struct Cfg {
     static constexpr int kTileBytes = kChunks * kChunkBytes;  // 128 rows x D bf16
     static constexpr SmemSwizzle kSw = D >= 64 ? kSwizzle128B : kSwizzle64B;
     static constexpr int kSbo = 8 * kRowBytes;  // byte distance between 8-row groups
-    static constexpr int kStagesK = D == 128 ? 3 : 4;
-    static constexpr int kStagesV = D == 128 ? 2 : 4;
+    static constexpr int kStagesK = D == 128 ? 2 : 4;
+    static constexpr int kStagesV = D == 128 ? 3 : 4;
     static constexpr uint32_t kIdescS = idesc_bf16_f32(kBlockM, kBlockN, 0, 0);
     static constexpr uint32_t kIdescO = idesc_bf16_f32(kBlockM, D, 0, 1);
 };
