@@ -205,3 +205,30 @@ def test_prompt_16_chunks_equals_one_launch_on_gpu():
     rows = PT.sample_rows(one.steps[0], H, 64, seed=11)
     ref_out, ref_lse, _, _ = PT.oracle_step(one, inp, W.bf16_bits(ck), W.bf16_bits(cv), rows=rows, want_cache=False)
     PT.compare(out2, lse2, ref_out, ref_lse, rows=rows, label="16 chunks vs oracle")
+
+
+def test_two_streams_run_concurrently():
+    """Calls on two streams at once keep separate workspaces: both match the oracle."""
+    wa = W.random_workload(960, head_dim=128, group=4, n_kv_heads=2, max_prefix=400, allow_empty=False)
+    wb = W.random_workload(961, head_dim=64, group=2, n_kv_heads=2, max_prefix=400, allow_empty=False)
+    runs = []
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    for wl, st in zip((wa, wb), streams):
+        ck, cv, (inp,) = W.make_inputs(wl)
+        d = {k: v.cuda() for k, v in inp.items()}
+        ck_d, cv_d = ck.cuda(), cv.cuda()
+        out = torch.empty_like(d["q"])
+        lse = torch.empty(d["q"].shape[0], wl.n_heads, device="cuda")
+        runs.append((wl, inp, ck, cv, d, ck_d, cv_d, out, lse, st))
+    torch.cuda.synchronize()
+    for _ in range(5):  # several rounds so that the two streams' kernels overlap
+        for wl, inp, ck, cv, d, ck_d, cv_d, out, lse, st in runs:
+            with torch.cuda.stream(st):
+                binding.prefill_attn_varlen(d["q"], d["k"], d["v"], d["cu_seqlens_q"], d["cu_seqlens_k"], ck_d,
+                                            cv_d, d["cache_offsets"], out, lse, scale=wl.scale, stream=st)
+    torch.cuda.synchronize()
+    for wl, inp, ck, cv, d, ck_d, cv_d, out, lse, st in runs:
+        assert binding.prefill_attn_device_status(st) == 0
+        ref_out, ref_lse, ref_ck, ref_cv = PT.oracle_step(wl, inp, W.bf16_bits(ck), W.bf16_bits(cv))
+        PT.compare(out, lse, ref_out, ref_lse, label=f"{wl.name} on its own stream")
+        assert np.array_equal(W.bf16_bits(ck_d.cpu()), ref_ck) and np.array_equal(W.bf16_bits(cv_d.cpu()), ref_cv)
