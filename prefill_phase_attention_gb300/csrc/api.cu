@@ -321,6 +321,11 @@ pa_status enqueue(const void* q, const void* k, const void* v, const int32_t* cu
     p.num_blocks = o.num_blocks;
     p.kv_quant = o.kv_quant;
     p.wait_timeout_test = o.wait_timeout_test;
+    // alternating tiles pay off where most sequences are a few tokens over a long
+    // prefix (decode rows): one slot of such a unit would otherwise idle.  The
+    // kernel variant costs a little elsewhere (larger code), so it is taken only
+    // when the new tokens average under 64 per sequence.
+    p.alt = !o.kv_quant && (long long)total_q < 64LL * num_seqs;
     p.scale_k = o.scale_k;
     p.scale_v = o.scale_v;
     e = pa::encode_fwd_maps(p, q, total_q, num_seqs, head_dim, o.num_blocks);

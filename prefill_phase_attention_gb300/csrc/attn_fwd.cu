@@ -94,9 +94,15 @@ struct __align__(16) Ctrl {
     UnitSlot slot[2];
     uint32_t tmem_base;
     int abort;
-    // int8 cache: the row scales of K tile t (CTA tile counter) in slot t % 4,
-    // folded into the scores by the softmax warps (the K tile holds the codes)
-    alignas(16) float kscale[4][kBlockN];
+    union {
+        // int8 cache: the row scales of K tile t (CTA tile counter) in slot t % 4,
+        // folded into the scores by the softmax warps (the K tile holds the codes)
+        alignas(16) float kscale[4][kBlockN];
+        // alternating units (bf16 cache only): slot 1's running max and sum per
+        // query row, handed to slot 0's warp of the same rows for the merge
+        float2 xchg[4][32];
+    };
+    uint64_t xchg_full[4];  // alternating units: slot 1's (max, sum) of sub-partition sp written
 };
 
 // Tiles first (the dynamic shared window starts 1024-byte aligned, which the
@@ -193,12 +199,18 @@ __device__ __forceinline__ bool paged_tail_tile(int j, int P, int np) {
 // numbering, and the sub-range [a[s], b[s]) of that stream each slot visits
 // (a = b = 0 when the slot has no tokens).  With a sliding window the later
 // slot may start after the earlier one; the two ranges always touch.
+// alt: the unit's tokens fit in slot 0 (a decode row, a short sequence, the
+// last query block of a sequence) and it visits at least two KV tiles; then
+// both slots work on slot 0's query rows, slot 0 on the even tiles of the
+// stream and slot 1 on the odd ones, so that the two still ping-pong on the
+// tensor pipe, and the two partial results are merged in the epilogue.
 struct UnitGeo {
     int lo, ntiles, np;
     int a[kSlots], b[kSlots];
+    bool alt;
 };
 
-template <bool kPaged>
+template <bool kPaged, bool kAlt = false>
 __device__ __forceinline__ UnitGeo unit_geo(const Unit& u, const SeqInfo& s, int tps, int causal, int window) {
     UnitGeo g;
     g.np = prefix_tiles(s.P);
@@ -215,6 +227,7 @@ __device__ __forceinline__ UnitGeo unit_geo(const Unit& u, const SeqInfo& s, int
             g.b[i] = t.hi - g.lo;
         }
     }
+    g.alt = kAlt && u.q0 + tps >= s.n && g.ntiles >= 2;
     return g;
 }
 
@@ -432,9 +445,10 @@ __device__ __forceinline__ bool load_kv_tile(const FwdParams& p, Ctrl* ctl, Work
     return true;
 }
 
-template <int D, bool kPaged, bool kQuant, bool kHook = false>
+template <int D, bool kPaged, bool kQuant, bool kAlt = false, bool kHook = false>
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ FwdParams p) {
     using C = Cfg<D>;
+    static_assert(!(kAlt && kQuant), "the merge exchange shares storage with the int8 scale ring");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // launched with programmatic stream serialisation: wait for the scheduler
     // (and rotary) kernels of this call before anything else
@@ -480,6 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             mbar_init(&ctl->unit_empty[b], 12);  // MMA + V loader + 2 cache writers + 8 softmax warps
         }
         mbar_init(&ctl->mma_drain, 1);
+        for (int s = 0; s < 4; ++s) mbar_init(&ctl->xchg_full[s], 32);  // every lane of slot 1's warp
         mbar_init(&ctl->never, 1);
         ctl->abort = 0;
         fence_mbar_init();
@@ -745,10 +760,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             return warp_wait(&ctl->k_full[kst], (tt / C::kStagesK) & 1, ctl, hdr);
         };
         bool ok = true;
-        auto issue_s = [&](int i, uint32_t tt) {
+        auto issue_s = [&](int i, uint32_t tt, int qi) {  // S of slot i from Q tile qi and K tile tt
             if (leader) {
                 const uint32_t koff = (tt % C::kStagesK) * C::kTileBytes;
-                const uint32_t qoff = i * C::kTileBytes;
+                const uint32_t qoff = qi * C::kTileBytes;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = ((kk * 16) / C::kChunkCols) * C::kChunkBytes + ((kk * 16) % C::kChunkCols) * 2;
@@ -782,14 +797,60 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             __syncwarp();
             if (leader) mbar_arrive(&ctl->unit_empty[sl]);
             if (u.b < 0) break;
-            const UnitGeo ug = unit_geo<kPaged>(u, s, tps, p.causal, p.window);
+            const UnitGeo ug = unit_geo<kPaged, kAlt>(u, s, tps, p.causal, p.window);
             const int ntiles = ug.ntiles;
             if (!warp_wait(&ctl->q_full, u_it & 1, ctl, hdr)) break;
+            if constexpr (kAlt) if (ug.alt) {
+                // (bf16 cache only) V tile tj, index jt in the sequence, ready for PV
+                auto wait_v = [&](uint32_t tj, int jt) -> bool {
+                    const int vst = tj % C::kStagesV;
+                    if (kPaged && paged_tail_tile(jt, s.P, ug.np)) {
+                        const bool got = warp_wait(&ctl->v_fix[vst], (fixpar >> vst) & 1, ctl, hdr);
+                        fixpar ^= 1u << vst;
+                        return got;
+                    }
+                    return warp_wait(&ctl->v_full[vst], (tj / C::kStagesV) & 1, ctl, hdr);
+                };
+                // slot i takes the tiles j with j % 2 == i, both from Q tile 0:
+                // S_0(0), S_1(1), then per tile j: PV_i(j), S_i(j + 2)
+                if (!wait_k(t, ug.lo, ug.np)) break;
+                tc_fence_after();
+                issue_s(0, t, 0);
+                commit(&ctl->k_empty[t % C::kStagesK]);
+                if (!wait_k(t + 1, ug.lo + 1, ug.np)) break;
+                tc_fence_after();
+                issue_s(1, t + 1, 0);
+                commit(&ctl->k_empty[(t + 1) % C::kStagesK]);
+                if (ntiles == 2) commit(&ctl->q_empty);
+                for (int j = 0; j < ntiles && ok; ++j) {
+                    const uint32_t tj = t + j;
+                    const int i = j & 1, kth = j >> 1;
+                    if (!warp_wait(&ctl->p_full[i], (ns[i] + kth) & 1, ctl, hdr)) { ok = false; break; }
+                    if (kth == 0 && !warp_wait(&ctl->o_empty[i], (no[i] & 1) ^ 1, ctl, hdr)) { ok = false; break; }
+                    if (!wait_v(tj, ug.lo + j)) { ok = false; break; }
+                    tc_fence_after();
+                    issue_pv(i, tj, kth == 0);
+                    if (j + 2 < ntiles) {
+                        if (!wait_k(tj + 2, ug.lo + j + 2, ug.np)) { ok = false; break; }
+                        tc_fence_after();
+                        issue_s(i, tj + 2, 0);
+                        commit(&ctl->k_empty[(tj + 2) % C::kStagesK]);
+                        if (j + 3 == ntiles) commit(&ctl->q_empty);
+                    }
+                    commit(&ctl->v_empty[tj % C::kStagesV]);
+                }
+                ns[0] += (ntiles + 1) / 2;
+                ns[1] += ntiles / 2;
+                no[0] += 1;
+                no[1] += 1;
+                t += ntiles;
+                continue;
+            }
             // prologue: S of tile 0 for the slots that start there
             if (!wait_k(t, ug.lo, ug.np)) break;
             tc_fence_after();
             for (int i = 0; i < kSlots; ++i)
-                if (ug.a[i] == 0 && ug.b[i] > 0) issue_s(i, t);
+                if (ug.a[i] == 0 && ug.b[i] > 0) issue_s(i, t, i);
             commit(&ctl->k_empty[t % C::kStagesK]);
             if (ntiles == 1) commit(&ctl->q_empty);
             for (int j = 0; j < ntiles && ok; ++j) {
@@ -833,7 +894,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                             k_ready = true;
                             tc_fence_after();
                         }
-                        issue_s(i, tj + 1);
+                        issue_s(i, tj + 1, i);
                     }
                 }
                 if (!ok) break;
@@ -996,6 +1057,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         const uint32_t o_col = s_col + kColO;
         const float sl2 = p.scale_log2;
         uint32_t ns = 0;  // tiles this slot has processed
+        uint32_t na = 0;  // alternating units so far (parity of xchg_full)
         uint32_t tg = 0;  // CTA tiles before the current unit (int8 cache: scale ring index)
         for (int u_it = 0;; ++u_it) {
             const int sl = u_it & 1;
@@ -1006,12 +1068,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             if (us.u.b < 0) break;
             const Unit u = us.u;
             const SeqInfo s = us.s;
-            const UnitGeo ug = unit_geo<kPaged>(u, s, tps, p.causal, p.window);
-            const int nt = ug.b[slot] - ug.a[slot];
+            const UnitGeo ug = unit_geo<kPaged, kAlt>(u, s, tps, p.causal, p.window);
+            // tiles of this slot: [a, b) of the stream, or every other one from `slot` (alt).
+            // (if constexpr keeps the plain variant's code exactly as without alt)
+            int nt = ug.b[slot] - ug.a[slot];
+            if constexpr (kAlt) nt = ug.alt ? (ug.ntiles + 1 - slot) / 2 : nt;
             const uint32_t tg0 = tg;
             tg += ug.ntiles;
             if (nt == 0) continue;
-            const int qs = u.q0 + slot * tps;
+            int qs = u.q0 + slot * tps;
+            if constexpr (kAlt) qs = ug.alt ? u.q0 : qs;  // alt: both slots hold slot 0's rows
             const int qe = min(qs + tps, s.n);
             const int tok = qs + r / G;
             const int h = u.kvh * G + r % G;
@@ -1050,10 +1116,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                         sv[96 + i] = __uint_as_float(r3[i]);
                     }
                 }
-                const int jt = ug.lo + ug.a[slot] + j;  // tile index in the sequence
+                int jrel = ug.a[slot] + j;  // tile index in the unit's stream
+                if constexpr (kAlt) jrel = ug.alt ? slot + 2 * j : jrel;
+                const int jt = ug.lo + jrel;  // tile index in the sequence
                 if (kQuant && jt < np) {
                     // int8 prefix tile: S holds q . code; scale column c by its row's scale
-                    const uint32_t tc = tg0 + ug.a[slot] + j;
+                    const uint32_t tc = tg0 + jrel;
                     if (!warp_wait(&ctl->ks_full[tc & 3], (tc >> 2) & 1, ctl, hdr)) { ok = false; break; }
                     const float4* ksc = reinterpret_cast<const float4*>(ctl->kscale[tc & 3]);
 #pragma unroll
@@ -1146,6 +1214,28 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             // epilogue: O of the slot is final once the PV of its last tile is done
             if (!warp_wait(&ctl->pv_done[slot], (ns + nt - 1) & 1, ctl, hdr)) break;
             tc_fence_after();
+            if constexpr (kAlt) if (ug.alt && slot == 1) {
+                // alt unit: hand this row's max and sum to slot 0's warp of the same
+                // rows; slot 0 merges O_1 from TMEM, writes the row and frees both O
+                // regions.  The next write of xchg waits for that: slot 1's next PV
+                // needs o_empty[1], which slot 0 arrives on after reading.
+                ctl->xchg[sp][lane] = make_float2(m, l);
+                mbar_arrive(&ctl->xchg_full[sp]);
+                ns += nt;
+                continue;
+            }
+            float c0 = 1.f, c1 = 0.f;  // weights of O_0 and O_1 (alt merge)
+            if constexpr (kAlt) if (ug.alt) {
+                if (!warp_wait(&ctl->xchg_full[sp], na & 1, ctl, hdr)) break;
+                ++na;
+                tc_fence_after();  // slot 1 saw pv_done[1] before it arrived
+                const float2 ml = ctl->xchg[sp][lane];
+                const float mm = fmaxf(m, ml.x);
+                c0 = m == -INFINITY ? 0.f : ex2(m - mm);
+                c1 = ml.x == -INFINITY ? 0.f : ex2(ml.x - mm);
+                l = l * c0 + ml.y * c1;
+                m = mm;
+            }
             const float inv_l = 1.f / l;
             const size_t row = (size_t)(s.q_start + tok) * p.n_heads + h;
             uint4* dst = reinterpret_cast<uint4*>(p.out + row * D);
@@ -1155,6 +1245,21 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 tmem_ld32(o_col + c, o);
                 tmem_wait_ld();
                 reg_fence(o);
+                if constexpr (kAlt) if (ug.alt) {
+                    uint32_t o1[32];
+                    tmem_ld32(o_col + kColSlot + c, o1);  // slot 1's O, same TMEM lanes
+                    tmem_wait_ld();
+                    reg_fence(o1);
+#pragma unroll
+                    for (int i = 0; i < 32; i += 2) {
+                        const float2 a = __ffma2_rn(make_float2(__uint_as_float(o1[i]), __uint_as_float(o1[i + 1])),
+                                                    make_float2(c1, c1),
+                                                    __fmul2_rn(make_float2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])),
+                                                               make_float2(c0, c0)));
+                        o[i] = __float_as_uint(a.x);
+                        o[i + 1] = __float_as_uint(a.y);
+                    }
+                }
                 if (valid) {
 #pragma unroll
                     for (int v4 = 0; v4 < 4; ++v4) {
@@ -1170,7 +1275,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             if (valid && p.lse) p.lse[row] = (m + lg2(l)) * 0.69314718055994530942f;
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&ctl->o_empty[slot]);
+            if (lane == 0) {
+                mbar_arrive(&ctl->o_empty[slot]);
+                if constexpr (kAlt) if (ug.alt) mbar_arrive(&ctl->o_empty[1]);  // slot 1's O was read here too
+            }
             ns += nt;
         }
     }
@@ -1209,7 +1317,7 @@ cudaError_t encode3d(CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, 
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int D, bool kPaged, bool kQuant, bool kHook = false>
+template <int D, bool kPaged, bool kQuant, bool kAlt = false, bool kHook = false>
 cudaError_t launch_d(const FwdParams& p, int grid, cudaStream_t st) {
     constexpr int kSmem = smem_bytes<D>();
     static_assert(kSmem <= 232448, "shared memory budget");
@@ -1218,7 +1326,7 @@ cudaError_t launch_d(const FwdParams& p, int grid, cudaStream_t st) {
     cudaGetDevice(&dev);
     if (dev < 64 && !configured_for[dev]) {
         cudaError_t e =
-            cudaFuncSetAttribute(attn_fwd_kernel<D, kPaged, kQuant, kHook>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            cudaFuncSetAttribute(attn_fwd_kernel<D, kPaged, kQuant, kAlt, kHook>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kSmem);
         if (e != cudaSuccess) return e;
         configured_for[dev] = 1;
@@ -1235,7 +1343,7 @@ cudaError_t launch_d(const FwdParams& p, int grid, cudaStream_t st) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, attn_fwd_kernel<D, kPaged, kQuant, kHook>, p);
+    return cudaLaunchKernelEx(&cfg, attn_fwd_kernel<D, kPaged, kQuant, kAlt, kHook>, p);
 }
 
 }  // namespace
@@ -1285,23 +1393,26 @@ cudaError_t encode_fwd_maps(FwdParams& p, const void* q, int total_q, int num_se
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
 }
 
+template <int D>
+cudaError_t launch_dim(const FwdParams& p, int grid, cudaStream_t st) {
+    static_assert(D == 32 || D == 64 || D == 128, "head_dim");
+    if (p.block_table) {
+        if (p.kv_quant) return launch_d<D, true, true>(p, grid, st);
+        return p.alt ? launch_d<D, true, false, true>(p, grid, st) : launch_d<D, true, false>(p, grid, st);
+    }
+    if (p.kv_quant) return launch_d<D, false, true>(p, grid, st);
+    return p.alt ? launch_d<D, false, false, true>(p, grid, st) : launch_d<D, false, false>(p, grid, st);
+}
+
 cudaError_t launch_attn_fwd(const FwdParams& p, int head_dim, int grid, cudaStream_t st) {
-    const bool paged = p.block_table != nullptr;
     if (p.wait_timeout_test) {  // the test hook exists for the plain d = 128 kernel only
-        if (head_dim != 128 || paged || p.kv_quant) return cudaErrorNotSupported;
-        return launch_d<128, false, false, true>(p, grid, st);
+        if (head_dim != 128 || p.block_table || p.kv_quant) return cudaErrorNotSupported;
+        return launch_d<128, false, false, false, true>(p, grid, st);
     }
     switch (head_dim) {
-        case 32:
-            return paged ? (p.kv_quant ? launch_d<32, true, true>(p, grid, st) : launch_d<32, true, false>(p, grid, st))
-                         : (p.kv_quant ? launch_d<32, false, true>(p, grid, st) : launch_d<32, false, false>(p, grid, st));
-        case 64:
-            return paged ? (p.kv_quant ? launch_d<64, true, true>(p, grid, st) : launch_d<64, true, false>(p, grid, st))
-                         : (p.kv_quant ? launch_d<64, false, true>(p, grid, st) : launch_d<64, false, false>(p, grid, st));
-        case 128:
-            return paged ? (p.kv_quant ? launch_d<128, true, true>(p, grid, st) : launch_d<128, true, false>(p, grid, st))
-                         : (p.kv_quant ? launch_d<128, false, true>(p, grid, st)
-                                       : launch_d<128, false, false>(p, grid, st));
+        case 32: return launch_dim<32>(p, grid, st);
+        case 64: return launch_dim<64>(p, grid, st);
+        case 128: return launch_dim<128>(p, grid, st);
         default: return cudaErrorInvalidValue;
     }
 }

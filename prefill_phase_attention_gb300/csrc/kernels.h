@@ -66,6 +66,10 @@ struct FwdParams {
     float* scale_v;
     int kv_quant;
     int wait_timeout_test;  // test hook: CTA 0 waits on a barrier nothing completes
+    // bf16 cache: units whose query rows fit one slot split their key tiles
+    // between both slots (even / odd) and merge the two partial results; chosen
+    // by the host for launches made mostly of short (decode) sequences
+    int alt;
 };
 
 // Encodes the tensor maps of `p` (the pointer fields and sizes must be set).

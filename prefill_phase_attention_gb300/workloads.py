@@ -170,6 +170,29 @@ def random_workload(seed: int, *, head_dim: int, group: int, n_kv_heads: int = 2
                     [Step(lens, pref)], pref, seed=1000 + seed, causal=causal)
 
 
+def decode_workload(seed: int, *, head_dim: int, group: int, n_kv_heads: int = 2,
+                    max_seqs: int = 24, max_prefix: int = 3000, causal: bool = True) -> Workload:
+    """Decode-heavy random batch: mostly 1-4 new tokens over long cached
+    prefixes (some on a tile edge), a few short chunks; the new tokens average
+    well under 64 per sequence."""
+    rng = np.random.default_rng(seed)
+    b = int(rng.integers(4, max_seqs, endpoint=True))
+    lens = [int(rng.integers(1, 4, endpoint=True)) if rng.random() < 0.85 else int(rng.integers(5, 120))
+            for _ in range(b)]
+    pref = []
+    for _ in range(b):
+        r = rng.random()
+        if r < 0.1:
+            pref.append(0)
+        elif r < 0.25:
+            pref.append(128 * int(rng.integers(1, max(2, max_prefix // 128))))
+        else:
+            pref.append(int(rng.integers(1, max_prefix, endpoint=True)))
+    cap = max(p + n for p, n in zip(pref, lens)) + int(rng.integers(0, 8))
+    return Workload(f"decode{seed}", n_kv_heads * group, n_kv_heads, head_dim, cap,
+                    [Step(lens, pref)], pref, seed=2000 + seed, causal=causal)
+
+
 # ---------------------------------------------------------------------------
 # tensors
 # ---------------------------------------------------------------------------
