@@ -199,7 +199,25 @@ typedef struct pa_options {
      * a healthy GPU: the call returns normally, prefill_attn_device_status
      * reports PA_ERR_DEVICE_TIMEOUT, and the context stays usable. */
     int32_t wait_timeout_test;
-    int32_t reserved4;  /* must be 0 */
+    /* Work schedule.  A work unit is a block of query tokens of one sequence
+     * against one KV head, in Q tiles of 128 rows (128 / G tokens x the G
+     * query heads of that KV head); the kernel runs two Q tiles ("slots")
+     * against each K/V tile it loads.
+     * 0 = chosen by the library per call:
+     * 2 = units of two Q tiles sharing every K/V tile (quantised caches and
+     *     launches with many units);
+     * 3 = the same, but a unit whose rows fit one Q tile (a decode row, the
+     *     last block of a prompt) splits its KV tiles between the two slots
+     *     (even / odd tiles, partial results merged at the end), so that the
+     *     second slot does not idle (launches where the new tokens average
+     *     under 64 per sequence);
+     * 1 = units of one Q tile, each splitting its KV tiles that way (launches
+     *     with at most one two-tile unit per SM: twice the units).
+     * 1 and 3 need a bf16 cache and wait_timeout_test = 0 (else
+     * PA_ERR_INVALID_ARG).  Results agree within the stated tolerances
+     * whatever the schedule (not bitwise: the summation order differs); the
+     * cache contents are the same bits. */
+    int32_t schedule;
 } pa_options;
 
 /*

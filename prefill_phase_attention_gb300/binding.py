@@ -28,7 +28,7 @@ class PaOptions(ctypes.Structure):
                 ("reserved", ctypes.c_int32), ("rope_theta", ctypes.c_float), ("reserved2", ctypes.c_int32),
                 ("kv_quant", ctypes.c_int32), ("reserved3", ctypes.c_int32),
                 ("cache_k_scale", ctypes.c_void_p), ("cache_v_scale", ctypes.c_void_p),
-                ("wait_timeout_test", ctypes.c_int32), ("reserved4", ctypes.c_int32)]
+                ("wait_timeout_test", ctypes.c_int32), ("schedule", ctypes.c_int32)]
 
 
 # Entry points declared in include/prefill_attn.h: name -> (restype, argtypes)
@@ -129,12 +129,13 @@ def prefill_attn_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_k, cache_v, c
 
 def make_options(window: int = 0, block_table=None, block_size: int = 0, num_blocks: int = 0,
                  rope_theta: float = 0.0, cache_k_scale=None, cache_v_scale=None,
-                 wait_timeout_test: bool = False) -> PaOptions:
+                 wait_timeout_test: bool = False, schedule: int = 0) -> PaOptions:
     o = PaOptions()
     o.struct_size = ctypes.sizeof(PaOptions)
     o.window = int(window)
     o.rope_theta = float(rope_theta)
     o.wait_timeout_test = int(bool(wait_timeout_test))
+    o.schedule = int(schedule)
     if cache_k_scale is not None:
         o.kv_quant = 1
         o.cache_k_scale = cache_k_scale.data_ptr()
@@ -150,7 +151,7 @@ def make_options(window: int = 0, block_table=None, block_size: int = 0, num_blo
 def prefill_attn_varlen_ex(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_k, cache_v, cache_offsets, out, lse=None, *,
                            scale: Optional[float] = None, causal: bool = True, window: int = 0,
                            block_table=None, rope_theta: float = 0.0, cache_k_scale=None, cache_v_scale=None,
-                           wait_timeout_test: bool = False, stream=None) -> None:
+                           wait_timeout_test: bool = False, schedule: int = 0, stream=None) -> None:
     """prefill_attn_varlen with options.
 
     window > 0 restricts each query to its `window` most recent keys (causal only).
@@ -163,6 +164,9 @@ def prefill_attn_varlen_ex(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_k, cache_v
     cache_k_scale / cache_v_scale (fp32 CUDA [num_seqs, n_kv_heads, max_cache_len])
     select the int8 cache: cache_k/v are then int8 codes and row (b, h, p) stands
     for code * scale.
+    schedule fixes the work schedule (pa_options.schedule: 1 one-tile units
+    splitting their KV tiles between the two slots, 2 two-tile units, 3
+    two-tile units with single-tile ones split; 0 = the library's choice).
     """
     cap = None
     if block_table is not None:
@@ -180,7 +184,7 @@ def prefill_attn_varlen_ex(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_k, cache_v
                         scale, causal, stream, max_cache_len=cap,
                         cache_dtype=torch.int8 if quant else torch.bfloat16)
     opts = make_options(window, block_table, cache_k.shape[2], cache_k.shape[0], rope_theta,
-                        cache_k_scale, cache_v_scale, wait_timeout_test)
+                        cache_k_scale, cache_v_scale, wait_timeout_test, schedule)
     _check(load().prefill_attn_varlen_ex(*args[:-1], ctypes.byref(opts), args[-1]))
 
 

@@ -155,6 +155,7 @@ struct Options {
     float* scale_k = nullptr;
     float* scale_v = nullptr;
     int wait_timeout_test = 0;
+    int schedule = 0;  // pa_options.schedule (0: chosen per call)
 };
 
 // Reads the caller's options; fields past the caller's struct_size count as zero.
@@ -208,11 +209,16 @@ pa_status read_options(const pa_options* opts, int causal, Options* o) {
         o->scale_k = opts->cache_k_scale;
         o->scale_v = opts->cache_v_scale;
     }
-    if (have >= offsetof(pa_options, reserved4) + sizeof(int32_t)) {
+    if (have >= offsetof(pa_options, schedule) + sizeof(int32_t)) {
         if (opts->wait_timeout_test != 0 && opts->wait_timeout_test != 1)
             return fail(PA_ERR_INVALID_ARG, "wait_timeout_test must be 0 or 1");
-        if (opts->reserved4 != 0) return fail(PA_ERR_INVALID_ARG, "pa_options.reserved4 must be 0");
         o->wait_timeout_test = opts->wait_timeout_test;
+        if (opts->schedule < 0 || opts->schedule > 3)
+            return fail(PA_ERR_INVALID_ARG, "schedule must be 0 .. 3 (got %d)", opts->schedule);
+        if ((opts->schedule == 1 || opts->schedule == 3) && (o->kv_quant || o->wait_timeout_test))
+            return fail(PA_ERR_INVALID_ARG, "schedule %d needs a bf16 cache and wait_timeout_test = 0",
+                        opts->schedule);
+        o->schedule = opts->schedule;
     }
     return PA_OK;
 }
@@ -228,11 +234,37 @@ pa_status check_paged(const Options& o, int max_cache_len, int n_kv_heads) {
     return PA_OK;
 }
 
+// The schedule of a call (pa_options.schedule 1 .. 3).  Two-tile units
+// unless the launch is mostly decode rows (new tokens averaging under 64 per
+// sequence: a decode unit then splits its KV tiles between both softmax slots
+// so that the second does not idle) or is so small that two-tile units would
+// fill at most half of the SMs (then one-tile units, twice as many, each
+// splitting its tiles).  The splitting kernel variant runs other units a few
+// per cent slower and one K/V tile then feeds one Q tile instead of two, so
+// it is not taken for anything else.  Measured on GB300 (152 SMs): a 512-token
+// chunk over a 4096-token prefix, GQA 32/8, 64 two-tile units: 541 -> 840
+// TFLOP/s with one-tile units; 1024-token prompts (128 two-tile units): 300
+// with two-tile units against 282.  bf16 caches only.
+int auto_schedule(int total_q, int num_seqs, int n_heads, int n_kv_heads, bool kv_quant, int sms) {
+    if (kv_quant) return 2;
+    if ((long long)total_q < 64LL * num_seqs) return 3;
+    const int tpu = pa::kSlots * (pa::kBlockM / (n_heads / n_kv_heads));
+    const long long full_units = (long long)n_kv_heads * (total_q / tpu);
+    return 2 * full_units <= sms ? 1 : 2;
+}
+
 // Upper bound on the work units of a call (host-side; device metadata unread).
-long long unit_bound(int total_q, int num_seqs, int n_heads, int n_kv_heads) {
+long long unit_bound(int total_q, int num_seqs, int n_heads, int n_kv_heads, int slots) {
     const int group = n_heads / n_kv_heads;
-    const int tpu = pa::kSlots * (pa::kBlockM / group);  // query tokens per work unit
+    const int tpu = slots * (pa::kBlockM / group);  // query tokens per work unit
     return (long long)n_kv_heads * ((total_q + tpu - 1) / tpu + num_seqs);
+}
+
+int sm_count(int dev, pa_status* s) {
+    int sms = 0;
+    const cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    *s = e == cudaSuccess ? PA_OK : cuda_fail(e, "cudaDeviceGetAttribute");
+    return sms;
 }
 
 struct Scratch {
@@ -248,7 +280,8 @@ pa_status enqueue(const void* q, const void* k, const void* v, const int32_t* cu
                   const int32_t* cu_seqlens_k, void* cache_k, void* cache_v, const int32_t* cache_offsets, void* out,
                   float* lse, int num_seqs, int total_q, int max_cache_len, int n_heads, int n_kv_heads,
                   int head_dim, float scale, int causal, const Options& o, const Scratch& scr, long long units_bound,
-                  int dev, cudaStream_t stream) {
+                  int sched, int sms, cudaStream_t stream) {
+    const int slots = sched == 1 ? 1 : pa::kSlots;  // Q tiles per unit
     const int group = n_heads / n_kv_heads;
     pa::ScheduleArgs sa;
     sa.cu_seqlens_q = cu_seqlens_q;
@@ -265,6 +298,7 @@ pa_status enqueue(const void* q, const void* k, const void* v, const int32_t* cu
     sa.causal = causal;
     sa.window = o.window;
     sa.max_units = scr.max_units;
+    sa.unit_slots = slots;
     sa.block_table = o.block_table;
     sa.block_size = o.block_size;
     sa.max_blocks = o.max_blocks;
@@ -321,18 +355,12 @@ pa_status enqueue(const void* q, const void* k, const void* v, const int32_t* cu
     p.num_blocks = o.num_blocks;
     p.kv_quant = o.kv_quant;
     p.wait_timeout_test = o.wait_timeout_test;
-    // alternating tiles pay off where most sequences are a few tokens over a long
-    // prefix (decode rows): one slot of such a unit would otherwise idle.  The
-    // kernel variant costs a little elsewhere (larger code), so it is taken only
-    // when the new tokens average under 64 per sequence.
-    p.alt = !o.kv_quant && (long long)total_q < 64LL * num_seqs;
+    p.alt = sched != 2;
+    p.unit_slots = slots;
     p.scale_k = o.scale_k;
     p.scale_v = o.scale_v;
     e = pa::encode_fwd_maps(p, q, total_q, num_seqs, head_dim, o.num_blocks);
     if (e != cudaSuccess) return cuda_fail(e, "tensor map encoding");
-    int sms = 0;
-    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
     const int grid = (int)std::min<long long>(sms, units_bound);
     e = pa::launch_attn_fwd(p, head_dim, grid, stream);
     if (e != cudaSuccess) return cuda_fail(e, "attention launch");
@@ -391,7 +419,13 @@ pa_status prefill_attn_varlen_ex(const void* q, const void* k, const void* v, co
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-    const long long max_units_ll = unit_bound(total_q, num_seqs, n_heads, n_kv_heads);
+    const int sms = sm_count(dev, &s);
+    if (s != PA_OK) return s;
+    const int sched = o.schedule            ? o.schedule
+                      : o.wait_timeout_test ? 2  // the hook's kernel
+                                            : auto_schedule(total_q, num_seqs, n_heads, n_kv_heads, o.kv_quant != 0, sms);
+    const int slots = sched == 1 ? 1 : pa::kSlots;
+    const long long max_units_ll = unit_bound(total_q, num_seqs, n_heads, n_kv_heads, slots);
     if (max_units_ll >= (1LL << 31)) return fail(PA_ERR_UNSUPPORTED, "too many work units");
     Workspace* ws = nullptr;
     s = get_workspace(dev, stream, num_seqs, (int)max_units_ll, &ws);
@@ -402,7 +436,8 @@ pa_status prefill_attn_varlen_ex(const void* q, const void* k, const void* v, co
         if (s != PA_OK) return s;
     }
     return enqueue(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_k, cache_v, cache_offsets, out, lse, num_seqs, total_q,
-                   max_cache_len, n_heads, n_kv_heads, head_dim, scale, causal, o, scr, max_units_ll, dev, stream);
+                   max_cache_len, n_heads, n_kv_heads, head_dim, scale, causal, o, scr, max_units_ll, sched, sms,
+                   stream);
 }
 
 pa_status prefill_attn_varlen_validate(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q,
@@ -529,16 +564,19 @@ extern "C" pa_status prefill_attn_varlen_noalloc(const void* q, const void* k, c
                              num_seqs, total_q, max_cache_len, n_heads, n_kv_heads, head_dim, scale, causal);
     if (s != PA_OK) return s;
     if (num_seqs == 0 || total_q == 0) return PA_OK;
-    const long long units = unit_bound(total_q, num_seqs, n_heads, n_kv_heads);
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    const int sms = sm_count(dev, &s);
+    if (s != PA_OK) return s;
+    const int sched = auto_schedule(total_q, num_seqs, n_heads, n_kv_heads, false, sms);
+    const long long units = unit_bound(total_q, num_seqs, n_heads, n_kv_heads, sched == 1 ? 1 : pa::kSlots);
     if (num_seqs > kNoAllocMaxSeqs)
         return fail(PA_ERR_UNSUPPORTED, "num_seqs %d exceeds the allocation-free limit %d", num_seqs, kNoAllocMaxSeqs);
     if (units > kNoAllocMaxUnits)
         return fail(PA_ERR_UNSUPPORTED, "up to %lld work units exceed the allocation-free limit %d", units,
                     kNoAllocMaxUnits);
-    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
     void* scratch = nullptr;
     s = noalloc_scratch(dev, &scratch);
     if (s != PA_OK) return s;
@@ -549,5 +587,6 @@ extern "C" pa_status prefill_attn_varlen_noalloc(const void* q, const void* k, c
     Scratch scr{static_cast<pa::WorkspaceHeader*>(scratch), seqs, reinterpret_cast<pa::Unit*>(seqs + kNoAllocMaxSeqs),
                 kNoAllocMaxUnits};
     return enqueue(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_k, cache_v, cache_offsets, out, lse, num_seqs, total_q,
-                   max_cache_len, n_heads, n_kv_heads, head_dim, scale, causal, Options(), scr, units, dev, stream);
+                   max_cache_len, n_heads, n_kv_heads, head_dim, scale, causal, Options(), scr, units, sched, sms,
+                   stream);
 }

@@ -110,8 +110,9 @@ struct __align__(16) Ctrl {
 // CTA never lands on an SM (each CTA holds all 512 TMEM columns).
 template <int D>
 constexpr int smem_bytes() {
-    return (Cfg<D>::kTileBytes * (kSlots + Cfg<D>::kStagesK + Cfg<D>::kStagesV) + (int)sizeof(Ctrl)) > 120 * 1024
-               ? Cfg<D>::kTileBytes * (kSlots + Cfg<D>::kStagesK + Cfg<D>::kStagesV) + (int)sizeof(Ctrl)
+    using C = Cfg<D>;
+    return (C::kTileBytes * (kSlots + C::kStagesK + C::kStagesV) + (int)sizeof(Ctrl)) > 120 * 1024
+               ? C::kTileBytes * (kSlots + C::kStagesK + C::kStagesV) + (int)sizeof(Ctrl)
                : 120 * 1024;
 }
 
@@ -199,35 +200,39 @@ __device__ __forceinline__ bool paged_tail_tile(int j, int P, int np) {
 // numbering, and the sub-range [a[s], b[s]) of that stream each slot visits
 // (a = b = 0 when the slot has no tokens).  With a sliding window the later
 // slot may start after the earlier one; the two ranges always touch.
-// alt: the unit's tokens fit in slot 0 (a decode row, a short sequence, the
-// last query block of a sequence) and it visits at least two KV tiles; then
-// both slots work on slot 0's query rows, slot 0 on the even tiles of the
-// stream and slot 1 on the odd ones, so that the two still ping-pong on the
-// tensor pipe, and the two partial results are merged in the epilogue.
+// kAlt (the variant for decode-heavy or small launches): units hold
+// unit_slots Q tiles (1 or 2, FwdParams::unit_slots); a unit whose rows fit
+// ONE Q tile (a decode row, the last block of a prompt, every unit when
+// unit_slots = 1) and that visits at least two KV tiles is "alt": both slots
+// work on its rows, slot 0 on the even tiles of the stream and slot 1 on the
+// odd ones, so that the two still ping-pong on the tensor pipe, and the two
+// partial results are merged in the epilogue.
 struct UnitGeo {
     int lo, ntiles, np;
     int a[kSlots], b[kSlots];
     bool alt;
 };
 
-template <bool kPaged, bool kAlt = false>
-__device__ __forceinline__ UnitGeo unit_geo(const Unit& u, const SeqInfo& s, int tps, int causal, int window) {
+template <bool kPaged, bool kAlt>
+__device__ __forceinline__ UnitGeo unit_geo(const Unit& u, const SeqInfo& s, int tps, int causal, int window,
+                                            int unit_slots) {
+    const int nslots = kAlt ? unit_slots : kSlots;  // Q tiles of a unit
     UnitGeo g;
     g.np = prefix_tiles(s.P);
-    const TileSpan all = query_tiles(s.n, s.P, u.q0, min(u.q0 + kSlots * tps, s.n), causal, window, kPaged);
+    const TileSpan all = query_tiles(s.n, s.P, u.q0, min(u.q0 + nslots * tps, s.n), causal, window, kPaged);
     g.lo = all.lo;
     g.ntiles = all.hi - all.lo;
 #pragma unroll
     for (int i = 0; i < kSlots; ++i) {
         const int qs = u.q0 + i * tps;
         g.a[i] = g.b[i] = 0;
-        if (qs < s.n) {
+        if (i < nslots && qs < s.n) {
             const TileSpan t = query_tiles(s.n, s.P, qs, min(qs + tps, s.n), causal, window, kPaged);
             g.a[i] = t.lo - g.lo;
             g.b[i] = t.hi - g.lo;
         }
     }
-    g.alt = kAlt && u.q0 + tps >= s.n && g.ntiles >= 2;
+    g.alt = kAlt && u.q0 + tps >= min(u.q0 + nslots * tps, s.n) && g.ntiles >= 2;
     return g;
 }
 
@@ -449,6 +454,7 @@ template <int D, bool kPaged, bool kQuant, bool kAlt = false, bool kHook = false
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ FwdParams p) {
     using C = Cfg<D>;
     static_assert(!(kAlt && kQuant), "the merge exchange shares storage with the int8 scale ring");
+    const int unit_slots = kAlt ? p.unit_slots : kSlots;  // Q tiles of a unit
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // launched with programmatic stream serialisation: wait for the scheduler
     // (and rotary) kernels of this call before anything else
@@ -588,7 +594,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 // both Q tiles: rows (token, head-in-group) of each slot
                 ok = wait_bar(&ctl->q_empty, (u_it & 1) ^ 1, ctl, hdr);
                 if (ok) {
-                    const int nq = u.q0 + tps < s.n ? 2 : 1;
+                    const int nq = unit_slots == 2 && u.q0 + tps < s.n ? 2 : 1;
                     mbar_arrive_expect_tx(&ctl->q_full, nq * G * tps * C::kRowBytes * C::kChunks);
                     for (int i = 0; i < nq; ++i)
                         for (int c = 0; c < C::kChunks; ++c)
@@ -598,7 +604,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 }
             }
             if (!is_v && !__shfl_sync(gmask, ok, src)) break;
-            const UnitGeo ug = unit_geo<true>(u, s, tps, p.causal, p.window);
+            const UnitGeo ug = unit_geo<true, kAlt>(u, s, tps, p.causal, p.window, unit_slots);
             const int32_t* tab = p.block_table + (size_t)u.b * p.max_blocks;
             // this lane's boxes of tile jj: box (pair / kChunks), chunk (pair % kChunks)
             // for pair = gl and gl + 16; returns the block id of each (prefix tiles)
@@ -692,14 +698,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 const SeqInfo s = us.s;
                 // both Q tiles: rows (token, head-in-group) of each slot
                 if (!wait_bar(&ctl->q_empty, (u_it & 1) ^ 1, ctl, hdr)) break;
-                const int nq = u.q0 + tps < s.n ? 2 : 1;
+                const int nq = unit_slots == 2 && u.q0 + tps < s.n ? 2 : 1;
                 mbar_arrive_expect_tx(&ctl->q_full, nq * G * tps * C::kRowBytes * C::kChunks);
                 for (int i = 0; i < nq; ++i)
                     for (int c = 0; c < C::kChunks; ++c)
                         tma_load_3d(q_smem + i * C::kTileBytes + c * C::kChunkBytes, &p.tm_q, &ctl->q_full,
                                     c * C::kChunkCols, u.kvh * G, s.q_start + u.q0 + i * tps);
                 last_q_parity[0] = u_it & 1;
-                const UnitGeo ug = unit_geo<kPaged>(u, s, tps, p.causal, p.window);
+                const UnitGeo ug = unit_geo<kPaged, kAlt>(u, s, tps, p.causal, p.window, unit_slots);
                 bool ok = true;
                 for (int j = 0; j < ug.ntiles && ok; ++j, ++t)
                     ok = load_kv_tile<D, kQuant>(p, ctl, hdr, k_smem, C::kStagesK, ctl->k_full, ctl->k_empty, &p.tm_ck,
@@ -721,7 +727,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 const UnitSlot us = ctl->slot[sl];
                 mbar_arrive(&ctl->unit_empty[sl]);
                 if (us.u.b < 0) break;
-                const UnitGeo ug = unit_geo<kPaged>(us.u, us.s, tps, p.causal, p.window);
+                const UnitGeo ug = unit_geo<kPaged, kAlt>(us.u, us.s, tps, p.causal, p.window, unit_slots);
                 bool ok = true;
                 for (int j = 0; j < ug.ntiles && ok; ++j, ++t)
                     ok = load_kv_tile<D, kQuant>(p, ctl, hdr, v_smem, C::kStagesV, ctl->v_full, ctl->v_empty, &p.tm_cv,
@@ -797,7 +803,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             __syncwarp();
             if (leader) mbar_arrive(&ctl->unit_empty[sl]);
             if (u.b < 0) break;
-            const UnitGeo ug = unit_geo<kPaged, kAlt>(u, s, tps, p.causal, p.window);
+            const UnitGeo ug = unit_geo<kPaged, kAlt>(u, s, tps, p.causal, p.window, unit_slots);
             const int ntiles = ug.ntiles;
             if (!warp_wait(&ctl->q_full, u_it & 1, ctl, hdr)) break;
             if constexpr (kAlt) if (ug.alt) {
@@ -939,9 +945,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             __syncwarp();
             if (lane == 0) mbar_arrive(&ctl->unit_empty[sl]);
             if (us.u.b < 0) break;
-            const UnitGeo ug = unit_geo<kPaged>(us.u, us.s, tps, p.causal, p.window);
+            const UnitGeo ug = unit_geo<kPaged, kAlt>(us.u, us.s, tps, p.causal, p.window, unit_slots);
             const int np = ug.np;
-            const int q_end = min(us.u.q0 + kSlots * tps, us.s.n);
+            const int q_end = min(us.u.q0 + unit_slots * tps, us.s.n);
             bool ok = true;
             for (int jr = 0; jr < ug.ntiles; ++jr, ++t) {
                 const int j = ug.lo + jr;  // tile index in the sequence
@@ -1068,7 +1074,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             if (us.u.b < 0) break;
             const Unit u = us.u;
             const SeqInfo s = us.s;
-            const UnitGeo ug = unit_geo<kPaged, kAlt>(u, s, tps, p.causal, p.window);
+            const UnitGeo ug = unit_geo<kPaged, kAlt>(u, s, tps, p.causal, p.window, unit_slots);
             // tiles of this slot: [a, b) of the stream, or every other one from `slot` (alt).
             // (if constexpr keeps the plain variant's code exactly as without alt)
             int nt = ug.b[slot] - ug.a[slot];

@@ -26,7 +26,8 @@ struct SeqInfo {
 // One work unit: query block [q0, q0 + 2 * (128/G)) of sequence b against KV
 // head kvh, split into two Q tiles ("slots") of 128/G tokens; in each tile the
 // G query heads of that KV head are packed into the 128 rows
-// (row r <-> token q0 + slot * 128/G + r / G, head kvh * G + r % G).
+// (row r <-> token q0 + slot * 128/G + r / G, head kvh * G + r % G).  In the
+// kernel's alternating variant a unit is one Q tile, [q0, q0 + 128/G).
 struct Unit {
     int b;
     int kvh;
@@ -57,6 +58,7 @@ struct ScheduleArgs {
     int causal;
     int window;     // sliding window (0: none)
     int max_units;  // capacity of the unit list
+    int unit_slots; // Q tiles per unit: 2 (plain kernel) or 1 (alternating variant)
     // paged cache (block_table == nullptr: contiguous slots)
     const int32_t* block_table;  // [num_seqs][max_blocks]
     int block_size, max_blocks, num_blocks;

@@ -66,10 +66,11 @@ struct FwdParams {
     float* scale_v;
     int kv_quant;
     int wait_timeout_test;  // test hook: CTA 0 waits on a barrier nothing completes
-    // bf16 cache: units whose query rows fit one slot split their key tiles
-    // between both slots (even / odd) and merge the two partial results; chosen
-    // by the host for launches made mostly of short (decode) sequences
+    // alternating variant (bf16 cache): units whose rows fit one Q tile split
+    // their KV tiles between both softmax slots (even / odd) and merge the two
+    // partial results; the host picks it for decode-heavy or small launches
     int alt;
+    int unit_slots;  // Q tiles per unit the scheduler cut (2, or 1 in the alternating variant)
 };
 
 // Encodes the tensor maps of `p` (the pointer fields and sizes must be set).

@@ -65,7 +65,7 @@ __global__ void __launch_bounds__(1024) build_schedule_kernel(ScheduleArgs a) {
     __shared__ int warp_sums[32];
     const int tid = threadIdx.x;
     const int nthr = blockDim.x;
-    const int tpu = kSlots * (kBlockM / a.group);  // query tokens per unit
+    const int tpu = a.unit_slots * (kBlockM / a.group);  // query tokens per unit
     // the next kernel (launched with programmatic stream serialisation) may
     // start its prologue now; it waits for this kernel before reading the list
     griddep_launch();

@@ -43,18 +43,20 @@ class Guarded:
         return bool((g == GUARD_F32).all())
 
 
-def run_step_gpu(wl, inp, cache_k_dev, cache_v_dev, guarded=True, window=0, block_table=None, rope_theta=0.0):
+def run_step_gpu(wl, inp, cache_k_dev, cache_v_dev, guarded=True, window=0, block_table=None, rope_theta=0.0,
+                 schedule=0):
     """One launch on the GPU; returns (out, lse) CUDA tensors (and checks guards).
-    block_table (CUDA int32) selects the paged cache: the caches are then pools."""
+    block_table (CUDA int32) selects the paged cache: the caches are then pools.
+    schedule 1 .. 3 fixes the work schedule (pa_options.schedule; 0: the library's choice)."""
     dev = {k: v.cuda() for k, v in inp.items()}
     T = inp["q"].shape[0]
     out = Guarded((T, wl.n_heads, wl.head_dim), torch.bfloat16)
     lse = Guarded((T, wl.n_heads), torch.float32)
-    if window or block_table is not None or rope_theta:
+    if window or block_table is not None or rope_theta or schedule:
         binding.prefill_attn_varlen_ex(dev["q"], dev["k"], dev["v"], dev["cu_seqlens_q"], dev["cu_seqlens_k"],
                                        cache_k_dev, cache_v_dev, dev["cache_offsets"], out.t, lse.t,
                                        scale=wl.scale, causal=wl.causal, window=window, block_table=block_table,
-                                       rope_theta=rope_theta)
+                                       rope_theta=rope_theta, schedule=schedule)
     else:
         binding.prefill_attn_varlen(dev["q"], dev["k"], dev["v"], dev["cu_seqlens_q"], dev["cu_seqlens_k"],
                                     cache_k_dev, cache_v_dev, dev["cache_offsets"], out.t, lse.t,

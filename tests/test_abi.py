@@ -84,10 +84,10 @@ def test_python_binding_refuses_cpu_tensors(lib):
 
 def _call_ex(lib, window=0, causal=1, struct_size=None, block_table=None, block_size=0, max_blocks=0,
              num_blocks=0, reserved=0, rope_theta=0.0, reserved2=0, kv_quant=0, reserved3=0, sk=None, sv=None,
-             wait_timeout_test=0, reserved4=0):
+             wait_timeout_test=0, schedule=0):
     opts = binding.PaOptions(ctypes.sizeof(binding.PaOptions) if struct_size is None else struct_size, window,
                              block_table, block_size, max_blocks, num_blocks, reserved, rope_theta, reserved2,
-                             kv_quant, reserved3, sk, sv, wait_timeout_test, reserved4)
+                             kv_quant, reserved3, sk, sv, wait_timeout_test, schedule)
     return lib.prefill_attn_varlen_ex(16, 32, 48, 64, 80, 96, 112, 128, 144, None, 1, 4, 8, 4, 2, 64,
                                       0.125, causal, ctypes.byref(opts), None)
 
@@ -117,7 +117,11 @@ _PAGED = dict(block_table=256, block_size=8, max_blocks=1, num_blocks=4)
     (dict(kv_quant=1, sk=512, sv=1024, reserved3=1), 1, "reserved3"),
     (dict(kv_quant=1, sk=512, sv=1024, struct_size=48), 1, "scale pointers"),
     (dict(wait_timeout_test=2), 1, "wait_timeout_test"),
-    (dict(reserved4=5), 1, "reserved4"),
+    (dict(schedule=4), 1, "schedule"),
+    (dict(schedule=-1), 1, "schedule"),
+    (dict(schedule=1, kv_quant=1, sk=512, sv=1024), 1, "schedule 1 needs"),
+    (dict(schedule=3, kv_quant=1, sk=512, sv=1024), 1, "schedule 3 needs"),
+    (dict(schedule=1, wait_timeout_test=1), 1, "schedule 1 needs"),
 ])
 def test_options_are_checked_before_launch(lib, kw, status, msg):
     assert _call_ex(lib, **kw) == status
@@ -131,5 +135,5 @@ def test_options_layout_matches_header():
         ("struct_size", 0), ("window", 4), ("block_table", 8), ("block_size", 16),
         ("max_blocks_per_seq", 20), ("num_blocks", 24), ("reserved", 28), ("rope_theta", 32),
         ("reserved2", 36), ("kv_quant", 40), ("reserved3", 44), ("cache_k_scale", 48), ("cache_v_scale", 56),
-        ("wait_timeout_test", 64), ("reserved4", 68)]
+        ("wait_timeout_test", 64), ("schedule", 68)]
     assert ctypes.sizeof(P) == 72

@@ -30,7 +30,7 @@ def _lib(oracle_mod):
         pytest.fail("GPU tests need CUDA")
 
 
-def _run_paged(wl, bs, seed, window=0, rows=None, table=None, pools=None):
+def _run_paged(wl, bs, seed, window=0, rows=None, table=None, pools=None, schedule=0):
     g = torch.Generator().manual_seed(seed)
     _, _, (inp,) = W.make_inputs(wl)
     if table is None:
@@ -39,7 +39,8 @@ def _run_paged(wl, bs, seed, window=0, rows=None, table=None, pools=None):
         pk, pv = pools
     pk_d = PT.Guarded(pk.shape, torch.bfloat16, fill=pk)
     pv_d = PT.Guarded(pv.shape, torch.bfloat16, fill=pv)
-    out, lse = PT.run_step_gpu(wl, inp, pk_d.t, pv_d.t, window=window, block_table=table.cuda())
+    out, lse = PT.run_step_gpu(wl, inp, pk_d.t, pv_d.t, window=window, block_table=table.cuda(),
+                               schedule=schedule)
     assert pk_d.guards_intact() and pv_d.guards_intact(), "write outside the pool"
     ref_out, ref_lse, ref_pk, ref_pv = PT.oracle_step(wl, inp, W.bf16_bits(pk), W.bf16_bits(pv), rows=rows,
                                                       window=window, block_table=table.numpy())
@@ -62,7 +63,7 @@ def test_paged_random_shapes(seed):
         window = int(np.random.default_rng(seed).integers(1, 400))
     wl = W.random_workload(500 + seed, head_dim=d, group=group, n_kv_heads=2, causal=causal,
                            max_prefix=[300, 700][seed % 2])
-    _run_paged(wl, bs, seed, window=window)
+    _run_paged(wl, bs, seed, window=window, schedule=(seed // 5) % 4)
 
 
 @pytest.mark.parametrize("bs", [16, 128])
@@ -72,7 +73,8 @@ def test_paged_long_prefix_sampled(bs):
     wl = W.Workload("paged_long", 32, 8, 128, 8192, [W.Step([1024, 1, 37, 300], [7000, 4000, 129, 0])],
                     [7000, 4000, 129, 0], seed=31)
     rows = PT.sample_rows(wl.steps[0], wl.n_heads, 64, seed=bs)
-    _run_paged(wl, bs, 40 + bs, rows=rows)
+    for sched in (1, 2):
+        _run_paged(wl, bs, 40 + bs, rows=rows, schedule=sched)
 
 
 def test_paged_chunked_decode_all_steps():

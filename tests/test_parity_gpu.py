@@ -21,11 +21,11 @@ def _lib(oracle_mod):
         pytest.fail("GPU tests need CUDA")
 
 
-def _run_single_step(wl, rows=None, window=0):
+def _run_single_step(wl, rows=None, window=0, schedule=0):
     ck, cv, (inp,) = W.make_inputs(wl)
     ck_d = PT.Guarded(ck.shape, torch.bfloat16, fill=ck)
     cv_d = PT.Guarded(cv.shape, torch.bfloat16, fill=cv)
-    out, lse = PT.run_step_gpu(wl, inp, ck_d.t, cv_d.t, window=window)
+    out, lse = PT.run_step_gpu(wl, inp, ck_d.t, cv_d.t, window=window, schedule=schedule)
     assert ck_d.guards_intact() and cv_d.guards_intact(), "write outside the cache"
     ref_out, ref_lse, ref_ck, ref_cv = PT.oracle_step(wl, inp, W.bf16_bits(ck), W.bf16_bits(cv), rows=rows,
                                                       window=window)
@@ -35,9 +35,13 @@ def _run_single_step(wl, rows=None, window=0):
     return stats
 
 
+@pytest.mark.parametrize("sched", [0, 1, 2, 3])
 @pytest.mark.parametrize("name", ["tiny_packed", "layer512", "varlen16"])
-def test_named_workload_full(name):
-    _run_single_step(W.get(name))
+def test_named_workload_full(name, sched):
+    """Every schedule (one-tile units splitting their KV tiles between the two
+    slots; two-tile units; two-tile units with single-tile ones split) and
+    the library's own choice."""
+    _run_single_step(W.get(name), schedule=sched)
 
 
 def test_long32k_sampled():
@@ -66,13 +70,14 @@ def test_chunked_decode_all_steps():
     assert np.array_equal(W.bf16_bits(cv_d.cpu()), ov)
 
 
+@pytest.mark.parametrize("sched", [1, 2, 3])
 @pytest.mark.parametrize("seed", range(12))
 @pytest.mark.parametrize("d", [32, 64, 128])
 @pytest.mark.parametrize("group", [1, 2, 4, 8])
-def test_random_shapes(seed, d, group):
+def test_random_shapes(seed, d, group, sched):
     wl = W.random_workload(seed * 31 + d + group, head_dim=d, group=group, n_kv_heads=2,
                            causal=(seed % 4 != 3))
-    _run_single_step(wl)
+    _run_single_step(wl, schedule=sched)
 
 
 def test_length_one_is_bit_exact():
@@ -130,7 +135,7 @@ def test_inconsistent_device_metadata_is_flagged_and_skipped():
 @pytest.mark.parametrize("window", [1, 17, 128, 200, 1000])
 def test_sliding_window_random_shapes(seed, d, group, window):
     wl = W.random_workload(seed * 7 + d + group + window, head_dim=d, group=group, n_kv_heads=2)
-    _run_single_step(wl, window=window)
+    _run_single_step(wl, window=window, schedule=1 + seed % 3)
 
 
 def test_sliding_window_long_prompt_sampled():
@@ -145,7 +150,8 @@ def test_sliding_window_chunk_over_cached_prefix():
     wl = W.Workload("winchunk", 16, 4, 128, 3000, [W.Step([300, 1, 700], [2000, 1500, 600])], [2000, 1500, 600],
                     seed=31)
     for window in (64, 333, 1024):
-        _run_single_step(wl, window=window)
+        for sched in (1, 2, 3):
+            _run_single_step(wl, window=window, schedule=sched)
 
 
 def test_many_sequences_sampled():
@@ -174,7 +180,8 @@ def test_query_block_edges():
     lens = [127, 128, 129, 255, 256, 257]
     pref = [0, 127, 128, 129, 255, 256]
     wl = W.Workload("edges", 16, 4, 128, 600, [W.Step(lens, pref)], pref, seed=81)
-    _run_single_step(wl)
+    for sched in (1, 2, 3):
+        _run_single_step(wl, schedule=sched)
 
 
 def test_prompt_16_chunks_equals_one_launch_on_gpu():

@@ -42,7 +42,7 @@ def _check_caches(got_k, got_v, ref_k, ref_v, mask, label):
     PT.compare_rotated_cache(got_k[mask], ref_k[mask], label)
 
 
-def _run(wl, theta, window=0, bs=0, rows=None, seed=0):
+def _run(wl, theta, window=0, bs=0, rows=None, seed=0, schedule=0):
     _, _, (inp,) = W.make_inputs(wl)
     table = None
     if bs:
@@ -54,7 +54,8 @@ def _run(wl, theta, window=0, bs=0, rows=None, seed=0):
     q0, k0 = inp["q"].clone(), inp["k"].clone()
     dev_inp = {kk: vv for kk, vv in inp.items()}
     out, lse = PT.run_step_gpu(wl, dev_inp, ck_d.t, cv_d.t, window=window,
-                               block_table=None if table is None else table.cuda(), rope_theta=theta)
+                               block_table=None if table is None else table.cuda(), rope_theta=theta,
+                               schedule=schedule)
     assert ck_d.guards_intact() and cv_d.guards_intact(), "write outside the cache"
     ref_out, ref_lse, ref_ck, ref_cv = PT.oracle_step(wl, inp, W.bf16_bits(ck), W.bf16_bits(cv), rows=rows,
                                                       window=window,
@@ -77,7 +78,7 @@ def test_rope_random_shapes(seed):
     window = 150 if (causal and seed % 5 == 2) else 0
     bs = [0, 0, 16, 64][seed % 4]
     wl = W.random_workload(700 + seed, head_dim=d, group=group, n_kv_heads=2, causal=causal, max_prefix=500)
-    _run(wl, theta, window=window, bs=bs, seed=seed)
+    _run(wl, theta, window=window, bs=bs, seed=seed, schedule=seed // 12)
 
 
 def test_rope_long_prompt_sampled():
