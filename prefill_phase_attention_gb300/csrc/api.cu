@@ -50,9 +50,10 @@ std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// header | SeqInfo[max_seqs] | Unit[max_units] | int[max_seqs] (scheduler scratch)
 size_t ws_bytes(int max_seqs, int max_units) {
     return align_up(sizeof(pa::WorkspaceHeader), 16) + (size_t)max_seqs * sizeof(pa::SeqInfo) +
-           (size_t)max_units * sizeof(pa::Unit);
+           (size_t)max_units * sizeof(pa::Unit) + (size_t)max_seqs * sizeof(int);
 }
 
 pa::SeqInfo* ws_seqs(const Workspace& w) {
@@ -60,6 +61,8 @@ pa::SeqInfo* ws_seqs(const Workspace& w) {
 }
 
 pa::Unit* ws_units(const Workspace& w) { return reinterpret_cast<pa::Unit*>(ws_seqs(w) + w.max_seqs); }
+
+int* ws_seq_scratch(const Workspace& w) { return reinterpret_cast<int*>(ws_units(w) + w.max_units); }
 
 // Returns the workspace of (device, stream), growing it (stream-ordered) when needed.
 pa_status get_workspace(int dev, cudaStream_t st, int num_seqs, int max_units, Workspace** out) {
@@ -272,6 +275,7 @@ struct Scratch {
     pa::SeqInfo* seqs;
     pa::Unit* units;
     int max_units;
+    int* seq_scratch;      // int[num_seqs] for the scheduler
     void* rope = nullptr;  // room for the rotated q and k when the rotary embedding is on
 };
 
@@ -290,6 +294,7 @@ pa_status enqueue(const void* q, const void* k, const void* v, const int32_t* cu
     sa.hdr = scr.hdr;
     sa.seqs = scr.seqs;
     sa.units = scr.units;
+    sa.seq_scratch = scr.seq_scratch;
     sa.num_seqs = num_seqs;
     sa.total_q = total_q;
     sa.max_cache_len = max_cache_len;
@@ -430,7 +435,8 @@ pa_status prefill_attn_varlen_ex(const void* q, const void* k, const void* v, co
     Workspace* ws = nullptr;
     s = get_workspace(dev, stream, num_seqs, (int)max_units_ll, &ws);
     if (s != PA_OK) return s;
-    Scratch scr{static_cast<pa::WorkspaceHeader*>(ws->ptr), ws_seqs(*ws), ws_units(*ws), ws->max_units};
+    Scratch scr{static_cast<pa::WorkspaceHeader*>(ws->ptr), ws_seqs(*ws), ws_units(*ws), ws->max_units,
+                ws_seq_scratch(*ws)};
     if (o.rope_theta > 0.f) {
         s = get_rope_scratch(ws, stream, (size_t)total_q * (n_heads + n_kv_heads) * head_dim * 2, &scr.rope);
         if (s != PA_OK) return s;
@@ -525,7 +531,7 @@ constexpr int kNoAllocMaxSeqs = 4096;
 constexpr int kNoAllocMaxUnits = 61440;
 constexpr size_t kNoAllocHeaderBytes = 16;
 constexpr size_t kNoAllocBytes = kNoAllocHeaderBytes + (size_t)kNoAllocMaxSeqs * sizeof(pa::SeqInfo) +
-                                 (size_t)kNoAllocMaxUnits * sizeof(pa::Unit);
+                                 (size_t)kNoAllocMaxUnits * sizeof(pa::Unit) + (size_t)kNoAllocMaxSeqs * sizeof(int);
 static_assert(sizeof(pa::WorkspaceHeader) <= kNoAllocHeaderBytes, "header size");
 
 // In host code this name is only a stand-in for the array; its device address
@@ -584,8 +590,9 @@ extern "C" pa_status prefill_attn_varlen_noalloc(const void* q, const void* k, c
     e = cudaMemsetAsync(scratch, 0, kNoAllocHeaderBytes, stream);
     if (e != cudaSuccess) return cuda_fail(e, "clearing the scratch header");
     pa::SeqInfo* seqs = reinterpret_cast<pa::SeqInfo*>(static_cast<unsigned char*>(scratch) + kNoAllocHeaderBytes);
-    Scratch scr{static_cast<pa::WorkspaceHeader*>(scratch), seqs, reinterpret_cast<pa::Unit*>(seqs + kNoAllocMaxSeqs),
-                kNoAllocMaxUnits};
+    pa::Unit* units_ws = reinterpret_cast<pa::Unit*>(seqs + kNoAllocMaxSeqs);
+    Scratch scr{static_cast<pa::WorkspaceHeader*>(scratch), seqs, units_ws, kNoAllocMaxUnits,
+                reinterpret_cast<int*>(units_ws + kNoAllocMaxUnits)};
     return enqueue(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_k, cache_v, cache_offsets, out, lse, num_seqs, total_q,
                    max_cache_len, n_heads, n_kv_heads, head_dim, scale, causal, Options(), scr, units, sched, sms,
                    stream);

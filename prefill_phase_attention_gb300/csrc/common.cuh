@@ -50,6 +50,7 @@ struct ScheduleArgs {
     WorkspaceHeader* hdr;
     SeqInfo* seqs;
     Unit* units;
+    int* seq_scratch;  // [num_seqs] scheduler scratch (cost bin, then first unit of the sequence)
     int num_seqs;
     int total_q;
     int max_cache_len;

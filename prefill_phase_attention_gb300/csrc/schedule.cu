@@ -3,9 +3,16 @@
 // Reads cu_seqlens_q / cu_seqlens_k / cache_offsets on the device (the varlen
 // kernel "reads cu_seqlens" itself, "大模型 Prompt Prefill 阶段的高效 Batching 与算子排布",
 // §2), sanitises each sequence, cuts it into work units (query block x KV head)
-// and lays the units out by descending cost (KV tiles visited) with a counting
-// sort, so that the persistent attention kernel starts the longest units first
-// (LPT order).  It also resets the attention kernel's work counter.
+// and lays them out for the persistent attention kernel, which claims them in
+// list order: sequences by descending total cost (KV tiles visited, counting
+// sort over log-spaced cost bins), within a sequence the query blocks last to
+// first (for a causal mask, the most expensive first) with the KV heads of a
+// block adjacent.  The longest work still starts first (LPT order within a
+// sequence and across sequences; the last units claimed are the cheapest
+// blocks of the cheapest sequences), and the CTAs running at any moment work
+// on one or two sequences, whose K/V then stay in L2 (ordering by unit cost
+// alone interleaves every sequence of a varlen batch and re-reads their K/V
+// from HBM).  It also resets the attention kernel's work counter.
 //
 // One CTA of 1024 threads; its cost is a few microseconds and it keeps the whole
 // launch free of host synchronisation.
@@ -18,7 +25,14 @@
 
 namespace pa {
 
-__device__ __forceinline__ int clamp_bin(int c) { return c < kCostBins - 1 ? c : kCostBins - 1; }
+// Sort key of a sequence: its total cost in log-spaced bins (exact below 64,
+// then 64 bins per power of two), clamped to the histogram.
+__device__ __forceinline__ int cost_bin(long long c) {
+    if (c < 64) return (int)c;
+    const int e = 63 - __clzll(c);  // >= 6
+    const long long bin = 64 + (long long)(e - 6) * 64 + ((c >> (e - 6)) & 63);
+    return bin < kCostBins - 1 ? (int)bin : kCostBins - 1;
+}
 
 // Block-wide exclusive scan of one int per thread (1024 threads); returns the
 // exclusive prefix and writes the block total to *total.
@@ -125,13 +139,24 @@ __global__ void __launch_bounds__(1024) build_schedule_kernel(ScheduleArgs a) {
     __threadfence_block();
     __syncthreads();
 
-    // Pass 2: histogram of unit costs (each query block gives n_kv_heads units).
-    for (int i = tid; i < total_blocks; i += nthr) {
-        const int b = block_owner(a.seqs, a.num_seqs, i);
-        const SeqInfo si = a.seqs[b];
-        const int q0 = (i - si.pad) * tpu;
-        atomicAdd(&hist[clamp_bin(unit_tiles(si.n, si.P, q0, tpu, a.causal, a.window, paged))], a.n_kv_heads);
+    // Pass 2 (one warp per sequence): total cost of the sequence's units; the
+    // histogram counts units per cost bin, the bin waits in seq_scratch.
+    {
+        const int lane = tid & 31, nwarps = nthr >> 5;
+        for (int b = tid >> 5; b < a.num_seqs; b += nwarps) {
+            const SeqInfo si = a.seqs[b];
+            const int nblk = (si.n + tpu - 1) / tpu;
+            long long c = 0;
+            for (int i = lane; i < nblk; i += 32) c += unit_tiles(si.n, si.P, i * tpu, tpu, a.causal, a.window, paged);
+            for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+            if (lane == 0 && nblk > 0) {
+                const int bin = cost_bin(c * a.n_kv_heads);
+                a.seq_scratch[b] = bin;
+                atomicAdd(&hist[bin], nblk * a.n_kv_heads);
+            }
+        }
     }
+    __threadfence_block();
     __syncthreads();
 
     // Exclusive scan in DESCENDING cost order: start[c] = sum of hist[c'] for c' > c.
@@ -150,14 +175,23 @@ __global__ void __launch_bounds__(1024) build_schedule_kernel(ScheduleArgs a) {
     }
     __syncthreads();
 
-    // Pass 3: scatter the units to their sorted positions (the KV heads of one
-    // query block stay adjacent).
+    // Pass 3: each sequence claims its range of the list from its bin ...
+    for (int b = tid; b < a.num_seqs; b += nthr) {
+        const int nblk = (a.seqs[b].n + tpu - 1) / tpu;
+        if (nblk > 0) a.seq_scratch[b] = atomicAdd(&hist[a.seq_scratch[b]], nblk * a.n_kv_heads);
+    }
+    __threadfence_block();
+    __syncthreads();
+
+    // ... and its units go there: query blocks last to first, KV heads adjacent.
     for (int i = tid; i < total_blocks; i += nthr) {
         const int b = block_owner(a.seqs, a.num_seqs, i);
         const SeqInfo si = a.seqs[b];
-        const int q0 = (i - si.pad) * tpu;
+        const int blk = i - si.pad;
+        const int nblk = (si.n + tpu - 1) / tpu;
+        const int q0 = blk * tpu;
         const int cost = unit_tiles(si.n, si.P, q0, tpu, a.causal, a.window, paged);
-        const int base = atomicAdd(&hist[clamp_bin(cost)], a.n_kv_heads);
+        const int base = a.seq_scratch[b] + (nblk - 1 - blk) * a.n_kv_heads;
         for (int kvh = 0; kvh < a.n_kv_heads; ++kvh) {
             const int pos = base + kvh;
             if (pos < a.max_units) {
