@@ -36,6 +36,11 @@
 //                   (its TMEM lane), fp32 running max/sum in registers, exp2
 //                   on the MUFU, lazy O rescale, epilogue out = O / l (bf16)
 //                   and LSE.
+// Variants (template arguments): a paged cache (block table), an int8 cache
+// (codes expanded in shared memory), and the tile-splitting schedule, in which
+// a unit whose rows fit one Q tile gives its even KV tiles to slot 0 and its
+// odd ones to slot 1 and merges the two partial results (decode rows, short
+// launches of one-tile units).
 // Every wait is bounded in time; on timeout the CTA records PA_DEVERR_TIMEOUT,
 // drains its in-flight copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
@@ -591,7 +596,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             if (is_v && gleader) mbar_arrive(&ctl->unit_empty[sl]);
             if (u.b < 0) break;
             if (!is_v && gleader) {
-                // both Q tiles: rows (token, head-in-group) of each slot
+                // the unit's Q tiles (one or two): rows (token, head-in-group) of each slot
                 ok = wait_bar(&ctl->q_empty, (u_it & 1) ^ 1, ctl, hdr);
                 if (ok) {
                     const int nq = unit_slots == 2 && u.q0 + tps < s.n ? 2 : 1;
@@ -696,7 +701,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 if (us.u.b < 0) break;
                 const Unit u = us.u;
                 const SeqInfo s = us.s;
-                // both Q tiles: rows (token, head-in-group) of each slot
+                // the unit's Q tiles (one or two): rows (token, head-in-group) of each slot
                 if (!wait_bar(&ctl->q_empty, (u_it & 1) ^ 1, ctl, hdr)) break;
                 const int nq = unit_slots == 2 && u.q0 + tps < s.n ? 2 : 1;
                 mbar_arrive_expect_tx(&ctl->q_full, nq * G * tps * C::kRowBytes * C::kChunks);

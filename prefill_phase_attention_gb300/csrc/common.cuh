@@ -26,8 +26,9 @@ struct SeqInfo {
 // One work unit: query block [q0, q0 + 2 * (128/G)) of sequence b against KV
 // head kvh, split into two Q tiles ("slots") of 128/G tokens; in each tile the
 // G query heads of that KV head are packed into the 128 rows
-// (row r <-> token q0 + slot * 128/G + r / G, head kvh * G + r % G).  In the
-// kernel's alternating variant a unit is one Q tile, [q0, q0 + 128/G).
+// (row r <-> token q0 + slot * 128/G + r / G, head kvh * G + r % G).  With
+// ScheduleArgs::unit_slots = 1 (the one-tile schedule) a unit is one Q tile,
+// [q0, q0 + 128/G).
 struct Unit {
     int b;
     int kvh;
