@@ -351,21 +351,27 @@ __device__ __noinline__ void dequant_tile(uint8_t* stage, const float (&sc)[4], 
             for (int b = 0; b < kGroup; ++b) {
                 const int r = r0 + b * kRows + lane / kGran;
                 // code + 128 as the low mantissa byte of 2^23, minus 2^23 + 128: exact
+                // (pairs of columns on packed fp32 ops)
                 const uint32_t x = w[b].x ^ 0x80808080u, y = w[b].y ^ 0x80808080u;
-                float f[8];
+                const float2 off = make_float2(-8388736.0f, -8388736.0f);
+                float2 f[4];  // columns (0,1), (2,3) of x, then of y
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    f[e] = __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7540u + e)) - 8388736.0f;
-                    f[e + 4] = __uint_as_float(__byte_perm(y, 0x4B000000u, 0x7540u + e)) - 8388736.0f;
+                for (int e = 0; e < 2; ++e) {
+                    f[e] = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(x, 0x4B000000u, 0x7540u + 2 * e)),
+                                                  __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7541u + 2 * e))),
+                                      off);
+                    f[e + 2] = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(y, 0x4B000000u, 0x7540u + 2 * e)),
+                                                      __uint_as_float(__byte_perm(y, 0x4B000000u, 0x7541u + 2 * e))),
+                                          off);
                     if (kScale) {
-                        f[e] *= s[b];
-                        f[e + 4] *= s[b];
+                        f[e] = __fmul2_rn(f[e], make_float2(s[b], s[b]));
+                        f[e + 2] = __fmul2_rn(f[e + 2], make_float2(s[b], s[b]));
                     }
                 }
                 const int phys = D >= 64 ? (gg ^ (r & 7)) : (gg ^ ((r >> 1) & 3));
                 *reinterpret_cast<uint4*>(stage + c * C::kChunkBytes + r * C::kRowBytes + phys * 16) =
-                    make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]),
-                               pack_bf16(f[6], f[7]));
+                    make_uint4(pack_bf16(f[0].x, f[0].y), pack_bf16(f[1].x, f[1].y), pack_bf16(f[2].x, f[2].y),
+                               pack_bf16(f[3].x, f[3].y));
             }
         }
     }
