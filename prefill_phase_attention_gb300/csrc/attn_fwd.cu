@@ -465,6 +465,14 @@ template <int D, bool kPaged, bool kQuant, bool kAlt = false, bool kHook = false
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ FwdParams p) {
     using C = Cfg<D>;
     static_assert(!(kAlt && kQuant), "the merge exchange shares storage with the int8 scale ring");
+    // K stages in use.  With an int8 cache the K writer publishes each tile's row
+    // scales in a 4-deep ring (Ctrl::kscale) that the softmax warps read after
+    // S; it writes the scales of tile t + 4 only once that tile has landed, i.e.
+    // once its stage was released by the S of tile t + 4 - kStK, which the MMA
+    // warp issues after the PV of tile t + 3 - kStK of every slot.  With at most
+    // 3 stages that PV follows every slot's softmax of tile t: the ring slot is
+    // free.  (bf16 caches use no scale ring.)
+    constexpr int kStK = kQuant && C::kStagesK > 3 ? 3 : C::kStagesK;
     const int unit_slots = kAlt ? p.unit_slots : kSlots;  // Q tiles of a unit
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // launched with programmatic stream serialisation: wait for the scheduler
@@ -488,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     if (threadIdx.x == 0) {
         mbar_init(&ctl->q_full, 1);
         mbar_init(&ctl->q_empty, 1);
-        for (int s = 0; s < C::kStagesK; ++s) {
+        for (int s = 0; s < kStK; ++s) {
             mbar_init(&ctl->k_full[s], 1);
             mbar_init(&ctl->k_empty[s], 2);  // MMA commit + cache writer
         }
@@ -498,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             mbar_init(&ctl->v_fix[s], 1);  // V cache writer
             mbar_init(&ctl->v_conv[s], 1);
         }
-        for (int s = 0; s < C::kStagesK; ++s) mbar_init(&ctl->k_conv[s], 1);  // K cache writer
+        for (int s = 0; s < kStK; ++s) mbar_init(&ctl->k_conv[s], 1);  // K cache writer
         for (int s = 0; s < 4; ++s) mbar_init(&ctl->ks_full[s], 1);          // K cache writer
         for (int i = 0; i < kSlots; ++i) {
             mbar_init(&ctl->s_full[i], 1);
@@ -559,7 +567,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         const int src = lane & 16;  // the group's leader lane
         const bool gleader = gl == 0;
         uint8_t* ring = is_v ? v_smem : k_smem;
-        const int stages = is_v ? C::kStagesV : C::kStagesK;
+        const int stages = is_v ? C::kStagesV : kStK;
         uint64_t* full = is_v ? ctl->v_full : ctl->k_full;
         uint64_t* empty = is_v ? ctl->v_empty : ctl->k_empty;
         const CUtensorMap* tm_cache = is_v ? &p.tm_cv : &p.tm_ck;
@@ -719,13 +727,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 const UnitGeo ug = unit_geo<kPaged, kAlt>(u, s, tps, p.causal, p.window, unit_slots);
                 bool ok = true;
                 for (int j = 0; j < ug.ntiles && ok; ++j, ++t)
-                    ok = load_kv_tile<D, kQuant>(p, ctl, hdr, k_smem, C::kStagesK, ctl->k_full, ctl->k_empty, &p.tm_ck,
+                    ok = load_kv_tile<D, kQuant>(p, ctl, hdr, k_smem, kStK, ctl->k_full, ctl->k_empty, &p.tm_ck,
                                                  &p.tm_k, last_k_parity, t, ug.lo + j, u, s, ug.np);
                 if (!ok) break;
             }
             if (aborted(ctl)) {
                 drain(&ctl->q_full, last_q_parity, 1);
-                drain(ctl->k_full, last_k_parity, C::kStagesK);
+                drain(ctl->k_full, last_k_parity, kStK);
             }
         } else if (lane == 1) {
             // ------------------------------------------------------- V loads
@@ -768,18 +776,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         // K tile tt (index jt in the sequence) ready for S: a prefix tile of an
         // int8 cache once the K writer has expanded it, else once TMA landed
         auto wait_k = [&](uint32_t tt, int jt, int np) -> bool {
-            const int kst = tt % C::kStagesK;
+            const int kst = tt % kStK;
             if (kQuant && jt < np) {
                 const bool got = warp_wait(&ctl->k_conv[kst], (kcpar >> kst) & 1, ctl, hdr);
                 kcpar ^= 1u << kst;
                 return got;
             }
-            return warp_wait(&ctl->k_full[kst], (tt / C::kStagesK) & 1, ctl, hdr);
+            return warp_wait(&ctl->k_full[kst], (tt / kStK) & 1, ctl, hdr);
         };
         bool ok = true;
         auto issue_s = [&](int i, uint32_t tt, int qi) {  // S of slot i from Q tile qi and K tile tt
             if (leader) {
-                const uint32_t koff = (tt % C::kStagesK) * C::kTileBytes;
+                const uint32_t koff = (tt % kStK) * C::kTileBytes;
                 const uint32_t qoff = qi * C::kTileBytes;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
@@ -833,11 +841,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 if (!wait_k(t, ug.lo, ug.np)) break;
                 tc_fence_after();
                 issue_s(0, t, 0);
-                commit(&ctl->k_empty[t % C::kStagesK]);
+                commit(&ctl->k_empty[t % kStK]);
                 if (!wait_k(t + 1, ug.lo + 1, ug.np)) break;
                 tc_fence_after();
                 issue_s(1, t + 1, 0);
-                commit(&ctl->k_empty[(t + 1) % C::kStagesK]);
+                commit(&ctl->k_empty[(t + 1) % kStK]);
                 if (ntiles == 2) commit(&ctl->q_empty);
                 for (int j = 0; j < ntiles && ok; ++j) {
                     const uint32_t tj = t + j;
@@ -851,7 +859,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                         if (!wait_k(tj + 2, ug.lo + j + 2, ug.np)) { ok = false; break; }
                         tc_fence_after();
                         issue_s(i, tj + 2, 0);
-                        commit(&ctl->k_empty[(tj + 2) % C::kStagesK]);
+                        commit(&ctl->k_empty[(tj + 2) % kStK]);
                         if (j + 3 == ntiles) commit(&ctl->q_empty);
                     }
                     commit(&ctl->v_empty[tj % C::kStagesV]);
@@ -868,7 +876,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             tc_fence_after();
             for (int i = 0; i < kSlots; ++i)
                 if (ug.a[i] == 0 && ug.b[i] > 0) issue_s(i, t, i);
-            commit(&ctl->k_empty[t % C::kStagesK]);
+            commit(&ctl->k_empty[t % kStK]);
             if (ntiles == 1) commit(&ctl->q_empty);
             for (int j = 0; j < ntiles && ok; ++j) {
                 const uint32_t tj = t + j;
@@ -916,7 +924,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 }
                 if (!ok) break;
                 if (j + 1 < ntiles) {
-                    commit(&ctl->k_empty[(tj + 1) % C::kStagesK]);
+                    commit(&ctl->k_empty[(tj + 1) % kStK]);
                     if (j + 2 == ntiles) commit(&ctl->q_empty);
                 }
                 commit(&ctl->v_empty[tj % C::kStagesV]);
@@ -943,7 +951,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         // behind; on the tiles holding the unit's own tokens it first copies
         // those rows from shared memory into the cache.
         const bool is_k = warp == 3;
-        const int stages = is_k ? C::kStagesK : C::kStagesV;
+        const int stages = is_k ? kStK : C::kStagesV;
         uint8_t* ring = is_k ? k_smem : v_smem;
         uint64_t* full = is_k ? ctl->k_full : ctl->v_full;
         uint64_t* empty = is_k ? ctl->k_empty : ctl->v_empty;
