@@ -362,6 +362,7 @@ pa_status enqueue(const void* q, const void* k, const void* v, const int32_t* cu
     p.wait_timeout_test = o.wait_timeout_test;
     p.alt = sched != 2;
     p.unit_slots = slots;
+    p.out_align32 = (reinterpret_cast<uintptr_t>(out) & 31u) == 0;
     p.scale_k = o.scale_k;
     p.scale_v = o.scale_v;
     e = pa::encode_fwd_maps(p, q, total_q, num_seqs, head_dim, o.num_blocks);

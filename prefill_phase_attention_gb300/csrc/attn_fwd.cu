@@ -168,6 +168,13 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// 32-byte store (sm_100+); p 32-byte aligned
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t (&w)[8]) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]), "r"(w[1]), "r"(w[2]),
+                 "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+}
+
 // max of three (one instruction on sm_100+)
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
     float d;
@@ -1286,14 +1293,21 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                     }
                 }
                 if (valid) {
+                    // whole 32-byte sectors per store when out allows it: the lanes
+                    // of a warp write 32 different rows, so each store is 32 pieces
 #pragma unroll
-                    for (int v4 = 0; v4 < 4; ++v4) {
-                        uint4 w;
-                        w.x = pack_bf16(__uint_as_float(o[v4 * 8 + 0]) * inv_l, __uint_as_float(o[v4 * 8 + 1]) * inv_l);
-                        w.y = pack_bf16(__uint_as_float(o[v4 * 8 + 2]) * inv_l, __uint_as_float(o[v4 * 8 + 3]) * inv_l);
-                        w.z = pack_bf16(__uint_as_float(o[v4 * 8 + 4]) * inv_l, __uint_as_float(o[v4 * 8 + 5]) * inv_l);
-                        w.w = pack_bf16(__uint_as_float(o[v4 * 8 + 6]) * inv_l, __uint_as_float(o[v4 * 8 + 7]) * inv_l);
-                        dst[c / 8 + v4] = w;
+                    for (int h = 0; h < 2; ++h) {
+                        uint32_t w[8];
+#pragma unroll
+                        for (int k = 0; k < 8; ++k)
+                            w[k] = pack_bf16(__uint_as_float(o[h * 16 + 2 * k]) * inv_l,
+                                             __uint_as_float(o[h * 16 + 2 * k + 1]) * inv_l);
+                        if (p.out_align32) {
+                            st_global_v8(dst + c / 8 + 2 * h, w);
+                        } else {
+                            dst[c / 8 + 2 * h] = make_uint4(w[0], w[1], w[2], w[3]);
+                            dst[c / 8 + 2 * h + 1] = make_uint4(w[4], w[5], w[6], w[7]);
+                        }
                     }
                 }
             }

@@ -71,6 +71,7 @@ struct FwdParams {
     // partial results; the host picks it for decode-heavy or small launches
     int alt;
     int unit_slots;  // Q tiles per unit the scheduler cut (2, or 1 in the alternating variant)
+    int out_align32;  // out is 32-byte aligned: the epilogue stores whole 32-byte sectors
 };
 
 // Encodes the tensor maps of `p` (the pointer fields and sizes must be set).

@@ -239,3 +239,26 @@ def test_two_streams_run_concurrently():
         ref_out, ref_lse, ref_ck, ref_cv = PT.oracle_step(wl, inp, W.bf16_bits(ck), W.bf16_bits(cv))
         PT.compare(out, lse, ref_out, ref_lse, label=f"{wl.name} on its own stream")
         assert np.array_equal(W.bf16_bits(ck_d.cpu()), ref_ck) and np.array_equal(W.bf16_bits(cv_d.cpu()), ref_cv)
+
+
+@pytest.mark.parametrize("d", [32, 64, 128])
+def test_out_16_byte_aligned(d):
+    """out at a 16-byte (not 32-byte) aligned address, the API's minimum: the
+    epilogue then stores 16-byte pieces; results and guard bands as usual."""
+    wl = W.random_workload(960 + d, head_dim=d, group=2, n_kv_heads=2, allow_empty=False)
+    ck, cv, (inp,) = W.make_inputs(wl)
+    dev = {k: v.cuda() for k, v in inp.items()}
+    T = inp["q"].shape[0]
+    n = T * wl.n_heads * d
+    buf = torch.full((n + 64,), 7.0, dtype=torch.bfloat16, device="cuda")
+    out = buf[8:8 + n].view(T, wl.n_heads, d)  # 16 bytes past a 256-byte aligned base
+    assert out.data_ptr() % 32 == 16
+    lse = torch.empty(T, wl.n_heads, device="cuda")
+    ck_d, cv_d = ck.cuda(), cv.cuda()
+    binding.prefill_attn_varlen(dev["q"], dev["k"], dev["v"], dev["cu_seqlens_q"], dev["cu_seqlens_k"], ck_d, cv_d,
+                                dev["cache_offsets"], out, lse, scale=wl.scale, causal=wl.causal)
+    torch.cuda.synchronize()
+    assert binding.prefill_attn_device_status() == 0
+    assert bool((buf[:8] == 7.0).all()) and bool((buf[8 + n:] == 7.0).all()), "write outside out"
+    ref_out, ref_lse, _, _ = PT.oracle_step(wl, inp, W.bf16_bits(ck), W.bf16_bits(cv), want_cache=False)
+    PT.compare(out, lse, ref_out, ref_lse, label=f"out +16 B d={d}")
