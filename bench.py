@@ -275,7 +275,11 @@ def run_ours(args, ws, rank, local):
         for d, o, l in zip(dev, outs, lses):
             call(d, o, l)
 
-    for _ in range(args.warmup):
+    schedules = set()  # the work schedule each call of a step ran (pa_options.schedule)
+    for d, o, l in zip(dev, outs, lses):
+        call(d, o, l)
+        schedules.add(binding.prefill_attn_last_schedule())
+    for _ in range(args.warmup - 1):
         step()
     torch.cuda.synchronize()
     if binding.prefill_attn_device_status() != 0:
@@ -434,6 +438,7 @@ def run_ours(args, ws, rank, local):
                    + (f"+paged{args.paged}" if args.paged else "") + (f"+rope{args.rope:g}" if args.rope else "")
                    + ("+int8kv" if args.kv_quant else ""),
                    "launches_per_step": n_launch, "window": args.window, "num_seqs": wl.num_seqs,
+                   "schedule": sorted(schedules)[0] if len(schedules) == 1 else sorted(schedules),
                    "kv_cache": (f"paged, {args.paged}-token blocks" if args.paged else "contiguous per sequence")
                    + (", int8 codes + fp32 row scales" if args.kv_quant else ", bf16"),
                    "rope_theta": args.rope,

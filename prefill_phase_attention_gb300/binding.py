@@ -45,6 +45,8 @@ SIGNATURES = {
     "prefill_attn_status_string": (ctypes.c_char_p, [_I]),
     "prefill_attn_last_error": (ctypes.c_char_p, []),
     "prefill_attn_last_launch_count": (_I, []),
+    "prefill_attn_last_schedule": (_I, []),
+    "prefill_attn_auto_schedule": (_I, [_I, _I, _I, _I, _I, _I]),
 }
 
 _lib = None
@@ -222,3 +224,14 @@ def prefill_attn_release() -> None:
 
 def prefill_attn_last_launch_count() -> int:
     return load().prefill_attn_last_launch_count()
+
+
+def prefill_attn_last_schedule() -> int:
+    """The schedule (pa_options.schedule 1, 2 or 3) the last call on this thread ran."""
+    return load().prefill_attn_last_schedule()
+
+
+def prefill_attn_auto_schedule(total_q: int, num_seqs: int, n_heads: int, n_kv_heads: int, kv_quant: bool,
+                               num_sms: int) -> int:
+    """The schedule the library picks for these sizes (host-only; -1 for rejected sizes)."""
+    return load().prefill_attn_auto_schedule(total_q, num_seqs, n_heads, n_kv_heads, int(bool(kv_quant)), num_sms)

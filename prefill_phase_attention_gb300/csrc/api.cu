@@ -21,6 +21,7 @@ namespace {
 
 thread_local std::string g_last_error;
 thread_local int g_last_launches = 0;
+thread_local int g_last_schedule = 0;
 
 pa_status fail(pa_status s, const char* fmt, ...) {
     char buf[512];
@@ -371,6 +372,7 @@ pa_status enqueue(const void* q, const void* k, const void* v, const int32_t* cu
     e = pa::launch_attn_fwd(p, head_dim, grid, stream);
     if (e != cudaSuccess) return cuda_fail(e, "attention launch");
     g_last_launches = launches;
+    g_last_schedule = sched;
     return PA_OK;
 }
 
@@ -395,6 +397,15 @@ const char* prefill_attn_last_error(void) { return g_last_error.c_str(); }
 
 int prefill_attn_last_launch_count(void) { return g_last_launches; }
 
+int prefill_attn_last_schedule(void) { return g_last_schedule; }
+
+int prefill_attn_auto_schedule(int total_q, int num_seqs, int n_heads, int n_kv_heads, int kv_quant, int num_sms) {
+    if (total_q <= 0 || num_seqs <= 0 || n_heads <= 0 || n_kv_heads <= 0 || num_sms <= 0 ||
+        n_heads % n_kv_heads != 0 || n_heads / n_kv_heads > pa::kBlockM)
+        return -1;
+    return auto_schedule(total_q, num_seqs, n_heads, n_kv_heads, kv_quant != 0, num_sms);
+}
+
 pa_status prefill_attn_varlen(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q,
                               const int32_t* cu_seqlens_k, void* cache_k, void* cache_v,
                               const int32_t* cache_offsets, void* out, float* lse, int num_seqs, int total_q,
@@ -412,6 +423,7 @@ pa_status prefill_attn_varlen_ex(const void* q, const void* k, const void* v, co
                                  int causal, const pa_options* opts, pa_stream_t stream_) {
     g_last_error.clear();
     g_last_launches = 0;
+    g_last_schedule = 0;
     Options o;
     pa_status s = read_options(opts, causal, &o);
     if (s != PA_OK) return s;
@@ -567,6 +579,7 @@ extern "C" pa_status prefill_attn_varlen_noalloc(const void* q, const void* k, c
                                                  float scale, int causal, pa_stream_t stream_) {
     g_last_error.clear();
     g_last_launches = 0;
+    g_last_schedule = 0;
     pa_status s = check_args(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_k, cache_v, cache_offsets, out, lse,
                              num_seqs, total_q, max_cache_len, n_heads, n_kv_heads, head_dim, scale, causal);
     if (s != PA_OK) return s;

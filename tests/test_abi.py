@@ -137,3 +137,31 @@ def test_options_layout_matches_header():
         ("reserved2", 36), ("kv_quant", 40), ("reserved3", 44), ("cache_k_scale", 48), ("cache_v_scale", 56),
         ("wait_timeout_test", 64), ("schedule", 68)]
     assert ctypes.sizeof(P) == 72
+
+
+@pytest.mark.parametrize("args,expect", [
+    # (total_q, num_seqs, n_heads, n_kv_heads, kv_quant, num_sms) -> schedule
+    ((32768, 1, 32, 32, 0, 152), 2),   # one long prompt: 4096 two-tile units
+    ((512, 1, 32, 32, 0, 152), 1),     # a 512-token MHA prompt: 64 two-tile units <= 152 / 2
+    ((1024, 1, 32, 32, 0, 152), 2),    # 128 two-tile units > 76
+    ((512, 1, 32, 8, 0, 152), 1),      # GQA-4: 64-token units, 8 x 8 = 64 units
+    ((576, 65, 32, 8, 0, 152), 3),     # a chunk and 64 decode rows: 8.9 new tokens per sequence
+    ((64, 64, 32, 8, 0, 152), 3),      # decode rows only
+    ((64, 64, 32, 8, 1, 152), 2),      # int8 cache: always two-tile units, no splitting
+    ((4096, 64, 32, 8, 0, 152), 2),    # exactly 64 tokens per sequence is not decode-heavy
+    ((4095, 64, 32, 8, 0, 152), 3),
+    ((0, 1, 32, 32, 0, 152), -1),
+    ((512, 1, 30, 8, 0, 152), -1),     # n_heads not a multiple of n_kv_heads
+    ((512, 1, 32, 32, 0, 0), -1),
+])
+def test_auto_schedule_policy(lib, args, expect):
+    """The schedule the library picks when pa_options.schedule is 0 (host-only)."""
+    assert binding.prefill_attn_auto_schedule(*args) == expect
+
+
+def test_last_schedule_is_zero_without_a_launch(lib):
+    # an empty batch returns PA_OK without launching anything
+    assert lib.prefill_attn_varlen(16, 32, 48, 64, 80, 96, 112, 128, 144, None, 0, 0, 8, 4, 2, 64, 0.125, 1,
+                                   None) == 0
+    assert lib.prefill_attn_last_launch_count() == 0
+    assert lib.prefill_attn_last_schedule() == 0
