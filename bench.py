@@ -434,16 +434,9 @@ def run_ours(args, ws, rank, local):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "tokens_per_s": round(tokens_s, 1),
         "pct_of_bf16_peak": round(100 * value / ws / peak, 2),
-        "config": {"workload": wl.name + (f"+window{args.window}" if args.window else "")
-                   + (f"+paged{args.paged}" if args.paged else "") + (f"+rope{args.rope:g}" if args.rope else "")
-                   + ("+int8kv" if args.kv_quant else ""),
-                   "launches_per_step": n_launch, "window": args.window, "num_seqs": wl.num_seqs,
+        "config": {**workload_config(args, wl),
+                   "launches_per_step": n_launch,
                    "schedule": sorted(schedules)[0] if len(schedules) == 1 else sorted(schedules),
-                   "kv_cache": (f"paged, {args.paged}-token blocks" if args.paged else "contiguous per sequence")
-                   + (", int8 codes + fp32 row scales" if args.kv_quant else ", bf16"),
-                   "rope_theta": args.rope,
-                   "tokens_per_step": wl.tokens(), "n_heads": wl.n_heads, "n_kv_heads": wl.n_kv_heads,
-                   "head_dim": wl.head_dim, "causal": wl.causal, "causal_flops_per_step": flops_step,
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
                    "l2": "inputs larger than L2 (no flush)" if flush is None else
                          "inputs smaller than L2: a 256 MB buffer is written before every timed step (cold L2); "
@@ -473,6 +466,19 @@ def run_ours(args, ws, rank, local):
         dist.destroy_process_group()
 
 
+def workload_config(args, wl):
+    """The workload part of the JSON line's config (the same in both arms)."""
+    return {"workload": wl.name + (f"+window{args.window}" if args.window else "")
+            + (f"+paged{args.paged}" if args.paged else "") + (f"+rope{args.rope:g}" if args.rope else "")
+            + ("+int8kv" if args.kv_quant else ""),
+            "window": args.window, "num_seqs": wl.num_seqs,
+            "kv_cache": (f"paged, {args.paged}-token blocks" if args.paged else "contiguous per sequence")
+            + (", int8 codes + fp32 row scales" if args.kv_quant else ", bf16"),
+            "rope_theta": args.rope,
+            "tokens_per_step": wl.tokens(), "n_heads": wl.n_heads, "n_kv_heads": wl.n_kv_heads,
+            "head_dim": wl.head_dim, "causal": wl.causal, "causal_flops_per_step": wl.flops(args.window)}
+
+
 # ----------------------------------------------------------- reference arm --
 
 def run_reference(args, ws, rank):
@@ -499,7 +505,7 @@ def run_reference(args, ws, rank):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": wl.name, "parallelism": "host cores"},
+        "config": {**workload_config(args, wl), "parallelism": "host cores"},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
