@@ -103,11 +103,11 @@ struct __align__(16) Ctrl {
         // int8 cache: the row scales of K tile t (CTA tile counter) in slot t % 4,
         // folded into the scores by the softmax warps (the K tile holds the codes)
         alignas(16) float kscale[4][kBlockN];
-        // alternating units (bf16 cache only): slot 1's running max and sum per
-        // query row, handed to slot 0's warp of the same rows for the merge
-        float2 xchg[4][32];
+        // tile-splitting variant: the column-split softmax's pair exchange,
+        // per sub-partition [phase parity][warp half][lane]
+        alignas(16) float xsplit[4][2 * 2 * 32];
     };
-    uint64_t xchg_full[4];  // alternating units: slot 1's (max, sum) of sub-partition sp written
+    uint64_t xs_full[4];  // column-split softmax: both warps of sub-partition sp wrote their value
 };
 
 // Tiles first (the dynamic shared window starts 1024-byte aligned, which the
@@ -517,16 +517,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         for (int s = 0; s < 4; ++s) mbar_init(&ctl->ks_full[s], 1);          // K cache writer
         for (int i = 0; i < kSlots; ++i) {
             mbar_init(&ctl->s_full[i], 1);
-            mbar_init(&ctl->p_full[i], 4);  // the slot's 4 softmax warps
+            mbar_init(&ctl->p_full[i], kAlt ? 8 : 4);  // the slot's 4 softmax warps (all 8: column split)
             mbar_init(&ctl->pv_done[i], 1);
-            mbar_init(&ctl->o_empty[i], 4);
+            mbar_init(&ctl->o_empty[i], kAlt ? 8 : 4);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&ctl->unit_full[b], 1);
             mbar_init(&ctl->unit_empty[b], 12);  // MMA + V loader + 2 cache writers + 8 softmax warps
         }
         mbar_init(&ctl->mma_drain, 1);
-        for (int s = 0; s < 4; ++s) mbar_init(&ctl->xchg_full[s], 32);  // every lane of slot 1's warp
+        for (int s = 0; s < 4; ++s) mbar_init(&ctl->xs_full[s], 64);  // every lane of the pair
         mbar_init(&ctl->never, 1);
         ctl->abort = 0;
         fence_mbar_init();
@@ -1077,20 +1077,43 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             }
             if (!ok) break;
         }
-    } else {
-        // ------------------------------------------------------------- softmax
-        // Warps 4-7 serve slot 0, warps 8-11 slot 1.  Sub-partition sp = warp % 4
-        // owns TMEM lanes (= query rows) [32 sp, 32 sp + 32).
-        const int slot = (warp - 4) >> 2;
+    } else if constexpr (kAlt) {
+        // ------------------------------------------------- softmax, column split
+        // The two warps of sub-partition sp (warps 4 + sp and 8 + sp) share the
+        // TMEM lanes (= query rows) [32 sp, 32 sp + 32) of BOTH slots: warp half
+        // h takes the score columns [64 h, 64 h + 64) of every tile and the O
+        // columns [h D/2, (h + 1) D/2).  Per tile the pair combines its row
+        // maxima through shared memory (so both use the same running max, and
+        // half 1 writes P over S columns 32-63 only after half 0 has read them);
+        // each warp keeps the sum of its own columns, combined at the end of the
+        // unit.  Both slots' tiles go through the same warps in the MMA warp's
+        // order (slot 0's tile j, then slot 1's), so a tile's exponentials take
+        // half the time of a one-warp-per-row softmax and the two slots'
+        // softmaxes no longer share a sub-partition at the same time.
+        constexpr int kHalfCols = kBlockN / 2;  // score columns per warp
+        constexpr int kHalfD = D / 2;           // O columns per warp
+        const int half = (warp - 4) >> 2;
         const int sp = warp & 3;
         const int r = sp * 32 + lane;  // query row of the tile == TMEM lane
         const uint32_t lane_off = (uint32_t)(sp * 32) << 16;
-        const uint32_t s_col = tmem + lane_off + slot * kColSlot;
-        const uint32_t o_col = s_col + kColO;
         const float sl2 = p.scale_log2;
-        uint32_t ns = 0;  // tiles this slot has processed
-        uint32_t na = 0;  // alternating units so far (parity of xchg_full)
-        uint32_t tg = 0;  // CTA tiles before the current unit (int8 cache: scale ring index)
+        uint32_t ns[kSlots] = {0, 0};  // tiles each slot has processed (s_full / pv_done phases)
+        uint32_t nx = 0;               // pair exchanges so far (xs_full phase, buffer parity)
+        float* xbuf = ctl->xsplit[sp];
+        // write this warp's value, wait for the partner's, read it (bounded wait)
+        auto exchange = [&](float v, float& other) -> bool {
+            const int par = nx & 1;
+            xbuf[(par * 2 + half) * 32 + lane] = v;
+            tc_fence_before();  // this warp's TMEM loads are ordered before the partner's stores
+            mbar_arrive(&ctl->xs_full[sp]);
+            const bool got = warp_wait(&ctl->xs_full[sp], par, ctl, hdr);
+            tc_fence_after();
+            other = xbuf[(par * 2 + (half ^ 1)) * 32 + lane];
+            ++nx;
+            return got;
+        };
+        // the warp's O columns of slot i: 32 at a time (16 at d = 32)
+        auto o_cols = [&](int i) -> uint32_t { return tmem + lane_off + i * kColSlot + kColO + half * kHalfD; };
         for (int u_it = 0;; ++u_it) {
             const int sl = u_it & 1;
             if (!warp_wait(&ctl->unit_full[sl], (u_it >> 1) & 1, ctl, hdr)) break;
@@ -1101,15 +1124,264 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             const Unit u = us.u;
             const SeqInfo s = us.s;
             const UnitGeo ug = unit_geo<kPaged, kAlt>(u, s, tps, p.causal, p.window, unit_slots);
-            // tiles of this slot: [a, b) of the stream, or every other one from `slot` (alt).
-            // (if constexpr keeps the plain variant's code exactly as without alt)
-            int nt = ug.b[slot] - ug.a[slot];
-            if constexpr (kAlt) nt = ug.alt ? (ug.ntiles + 1 - slot) / 2 : nt;
+            bool alt = false;
+            if constexpr (kAlt) alt = ug.alt;
+            const int np = ug.np;
+            const int Lk = s.P + s.n;
+            // rows of each slot (alt: both slots hold slot 0's rows)
+            int tok[kSlots], row_hi[kSlots], slot_hi[kSlots], row_lo[kSlots], slot_lo[kSlots];
+            bool valid[kSlots];
+#pragma unroll
+            for (int i = 0; i < kSlots; ++i) {
+                const int qs = u.q0 + (alt ? 0 : i) * tps;
+                const int qe = min(qs + tps, s.n);
+                tok[i] = qs + r / G;
+                valid[i] = r < tps * G && tok[i] < s.n;
+                row_hi[i] = p.causal ? min(s.P + tok[i] + 1, Lk) : Lk;  // keys [0, row_hi) visible
+                slot_hi[i] = p.causal ? min(s.P + qs + 1, Lk) : Lk;    // smallest row_hi of the slot
+                // sliding window: keys [row_lo, row_hi); slot_lo = largest row_lo of the slot
+                row_lo[i] = (p.causal && p.window > 0) ? s.P + tok[i] - p.window + 1 : INT_MIN / 2;
+                slot_lo[i] = (p.causal && p.window > 0) ? s.P + qe - p.window : INT_MIN / 2;
+            }
+            const int hrow = u.kvh * G + r % G;
+            float m[kSlots] = {-INFINITY, -INFINITY}, l[kSlots] = {0.f, 0.f};
+            int cnt[kSlots] = {0, 0};  // this unit's tiles per slot
+            bool ok = true;
+            for (int j = 0; j < ug.ntiles && ok; ++j) {
+#pragma unroll
+                for (int i = 0; i < kSlots; ++i) {
+                    const bool in = alt ? (j & 1) == i : (j >= ug.a[i] && j < ug.b[i]);
+                    if (!in) continue;
+                    if (!warp_wait(&ctl->s_full[i], ns[i] & 1, ctl, hdr)) { ok = false; break; }
+                    tc_fence_after();
+                    // S_i(j) is complete, and with it every earlier MMA of slot i
+                    // (its previous PV included): O may be rescaled below.
+                    const uint32_t s_col = tmem + lane_off + i * kColSlot;
+                    float sv[kHalfCols];
+                    {
+                        uint32_t r0[32], r1[32];
+                        tmem_ld32(s_col + half * kHalfCols, r0);
+                        tmem_ld32(s_col + half * kHalfCols + 32, r1);
+                        tmem_wait_ld();
+                        reg_fence(r0);
+                        reg_fence(r1);
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) {
+                            sv[c] = __uint_as_float(r0[c]);
+                            sv[32 + c] = __uint_as_float(r1[c]);
+                        }
+                    }
+                    const int jt = ug.lo + j;  // tile index in the sequence
+                    const int kb = tile_key_base<kPaged>(jt, s.P, np);
+                    // paged: the last prefix tile holds prefix keys only below P
+                    const bool tail = kPaged && jt < np && kb + kBlockN > s.P;
+                    if (kb < 0 || kb + kBlockN > slot_hi[i] || kb < slot_lo[i] || tail) {
+                        const int lo = max(-kb, row_lo[i] - kb) - half * kHalfCols;
+                        const int hi = (tail ? min(row_hi[i], s.P) : row_hi[i]) - kb - half * kHalfCols;
+#pragma unroll
+                        for (int c = 0; c < kHalfCols; ++c)
+                            if (c < lo || c >= hi) sv[c] = -INFINITY;
+                    }
+                    // row max of the warp's columns: four chains of three-input maxima
+                    float mx0 = fmaxf(sv[0], sv[1]), mx1 = fmaxf(sv[2], sv[3]);
+                    float mx2 = fmaxf(sv[4], sv[5]), mx3 = fmaxf(sv[6], sv[7]);
+#pragma unroll
+                    for (int c = 8; c < kHalfCols; c += 8) {
+                        mx0 = fmax3(mx0, sv[c], sv[c + 1]);
+                        mx1 = fmax3(mx1, sv[c + 2], sv[c + 3]);
+                        mx2 = fmax3(mx2, sv[c + 4], sv[c + 5]);
+                        mx3 = fmax3(mx3, sv[c + 6], sv[c + 7]);
+                    }
+                    const float mh = fmaxf(fmax3(mx0, mx1, mx2), mx3);
+                    float mo;
+                    if (!exchange(mh, mo)) { ok = false; break; }
+                    // the same in both warps: max of (half 0, half 1) in a fixed order
+                    const float m_tile = (half == 0 ? fmaxf(mh, mo) : fmaxf(mo, mh)) * sl2;
+                    const float m_new = fmaxf(m[i], m_tile);
+                    float alpha = 1.f;
+                    bool rescale = false;
+                    if (cnt[i] == 0) {
+                        m[i] = m_new;
+                    } else {
+                        const bool need = m_new > m[i] + 8.f;
+                        rescale = __any_sync(0xffffffffu, need);
+                        if (need) {
+                            alpha = ex2(m[i] - m_new);
+                            m[i] = m_new;
+                        }
+                    }
+                    const float m_use = m[i] == -INFINITY ? 0.f : m[i];
+                    // P as bf16 pairs: the warp's 64 scores go to the 32 TMEM
+                    // columns at 32 h (over S columns the pair has read)
+                    const float2 sl2v = make_float2(sl2, sl2), negm = make_float2(-m_use, -m_use);
+                    float2 sum2 = make_float2(0.f, 0.f);
+#pragma unroll
+                    for (int c4 = 0; c4 < 2; ++c4) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int q = 0; q < 16; ++q) {
+                            const float2 a =
+                                __ffma2_rn(make_float2(sv[c4 * 32 + 2 * q], sv[c4 * 32 + 2 * q + 1]), sl2v, negm);
+                            const float p0 = ex2(a.x);
+                            const float p1 = ex2(a.y);
+                            sum2 = __fadd2_rn(sum2, make_float2(p0, p1));
+                            pk[q] = pack_bf16(p0, p1);
+                        }
+                        tmem_st16(s_col + half * (kHalfCols / 2) + c4 * 16, pk);
+                    }
+                    l[i] = l[i] * alpha + (sum2.x + sum2.y);
+                    if (rescale) {
+                        if constexpr (kHalfD >= 32) {
+#pragma unroll
+                            for (int c = 0; c < kHalfD; c += 32) {
+                                uint32_t o[32];
+                                tmem_ld32(o_cols(i) + c, o);
+                                tmem_wait_ld();
+                                reg_fence(o);
+#pragma unroll
+                                for (int q = 0; q < 32; q += 2) {
+                                    const float2 v = __fmul2_rn(make_float2(__uint_as_float(o[q]), __uint_as_float(o[q + 1])),
+                                                                make_float2(alpha, alpha));
+                                    o[q] = __float_as_uint(v.x);
+                                    o[q + 1] = __float_as_uint(v.y);
+                                }
+                                tmem_st32(o_cols(i) + c, o);
+                            }
+                        } else {
+                            uint32_t o[16];
+                            tmem_ld16(o_cols(i), o);
+                            tmem_wait_ld();
+                            reg_fence(o);
+#pragma unroll
+                            for (int q = 0; q < 16; q += 2) {
+                                const float2 v = __fmul2_rn(make_float2(__uint_as_float(o[q]), __uint_as_float(o[q + 1])),
+                                                            make_float2(alpha, alpha));
+                                o[q] = __float_as_uint(v.x);
+                                o[q + 1] = __float_as_uint(v.y);
+                            }
+                            tmem_st16(o_cols(i), o);
+                        }
+                    }
+                    tmem_wait_st();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&ctl->p_full[i]);
+                    ++ns[i];
+                    ++cnt[i];
+                }
+            }
+            if (!ok) break;
+            // epilogue: a slot's O is final once the PV of its last tile is done.
+            // The pair adds its partial sums (in a fixed order, so both get the
+            // same l); each warp normalises and writes its half of every row.
+            // An alt unit merges the two slots' partial results of the same rows.
+            float w[kSlots] = {0.f, 0.f};  // weight of each slot's O in the output row
+            bool done = false;
+            for (int e = 0; e < kSlots && !done; ++e) {
+                // alt: one merged output (e = 0 only); else slot e, if it had tiles
+                if (alt ? e > 0 : cnt[e] == 0) continue;
+                float lt[kSlots], mm = -INFINITY;
+#pragma unroll
+                for (int i = 0; i < kSlots; ++i) {
+                    lt[i] = 0.f;
+                    const bool use = alt ? cnt[i] > 0 : i == e;
+                    if (!use) continue;
+                    if (!warp_wait(&ctl->pv_done[i], (ns[i] - 1) & 1, ctl, hdr)) { ok = false; break; }
+                    float lo_;
+                    if (!exchange(l[i], lo_)) { ok = false; break; }
+                    lt[i] = half == 0 ? l[i] + lo_ : lo_ + l[i];
+                    mm = fmaxf(mm, m[i]);
+                }
+                if (!ok) break;
+                tc_fence_after();
+                float lsum = 0.f;
+#pragma unroll
+                for (int i = 0; i < kSlots; ++i) {
+                    const bool use = alt ? cnt[i] > 0 : i == e;
+                    w[i] = 0.f;
+                    if (!use) continue;
+                    const float c = (m[i] == -INFINITY) ? 0.f : ex2(m[i] - mm);  // 1 for a single slot
+                    w[i] = c;
+                    lsum += lt[i] * c;
+                }
+                const float inv_l = 1.f / lsum;
+                const int orow_slot = alt ? 0 : e;
+                const bool v_ok = valid[orow_slot];
+                const size_t row = (size_t)(s.q_start + tok[orow_slot]) * p.n_heads + hrow;
+                uint4* dst = reinterpret_cast<uint4*>(p.out + row * D + half * kHalfD);
+#pragma unroll
+                for (int c = 0; c < kHalfD; c += (kHalfD >= 32 ? 32 : 16)) {
+                    constexpr int kW = kHalfD >= 32 ? 32 : 16;
+                    float o[kW];
+#pragma unroll
+                    for (int q = 0; q < kW; ++q) o[q] = 0.f;
+#pragma unroll
+                    for (int i = 0; i < kSlots; ++i) {
+                        const bool use = alt ? cnt[i] > 0 : i == e;
+                        if (!use) continue;
+                        uint32_t ob[kW];
+                        if constexpr (kW == 32) tmem_ld32(o_cols(i) + c, ob); else tmem_ld16(o_cols(i) + c, ob);
+                        tmem_wait_ld();
+                        reg_fence(ob);
+                        const float wi = w[i] * inv_l;
+#pragma unroll
+                        for (int q = 0; q < kW; ++q) o[q] = fmaf(__uint_as_float(ob[q]), wi, o[q]);
+                    }
+                    if (v_ok) {
+#pragma unroll
+                        for (int g = 0; g < kW / 16; ++g) {
+                            uint32_t pw[8];
+#pragma unroll
+                            for (int k = 0; k < 8; ++k) pw[k] = pack_bf16(o[g * 16 + 2 * k], o[g * 16 + 2 * k + 1]);
+                            if (p.out_align32) {
+                                st_global_v8(dst + c / 8 + 2 * g, pw);
+                            } else {
+                                dst[c / 8 + 2 * g] = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+                                dst[c / 8 + 2 * g + 1] = make_uint4(pw[4], pw[5], pw[6], pw[7]);
+                            }
+                        }
+                    }
+                }
+                if (v_ok && half == 0 && p.lse) p.lse[row] = (mm + lg2(lsum)) * 0.69314718055994530942f;
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+#pragma unroll
+                    for (int i = 0; i < kSlots; ++i)
+                        if (alt ? cnt[i] > 0 : i == e) mbar_arrive(&ctl->o_empty[i]);
+                }
+                if (alt) done = true;
+            }
+            if (!ok) break;
+        }
+    } else {
+        // ------------------------------------------------------------- softmax
+        // (plain schedule) Warps 4-7 serve slot 0, warps 8-11 slot 1.  Sub-partition sp = warp % 4
+        // owns TMEM lanes (= query rows) [32 sp, 32 sp + 32).
+        const int slot = (warp - 4) >> 2;
+        const int sp = warp & 3;
+        const int r = sp * 32 + lane;  // query row of the tile == TMEM lane
+        const uint32_t lane_off = (uint32_t)(sp * 32) << 16;
+        const uint32_t s_col = tmem + lane_off + slot * kColSlot;
+        const uint32_t o_col = s_col + kColO;
+        const float sl2 = p.scale_log2;
+        uint32_t ns = 0;  // tiles this slot has processed
+        uint32_t tg = 0;  // CTA tiles before the current unit (int8 cache: scale ring index)
+        for (int u_it = 0;; ++u_it) {
+            const int sl = u_it & 1;
+            if (!warp_wait(&ctl->unit_full[sl], (u_it >> 1) & 1, ctl, hdr)) break;
+            const UnitSlot us = ctl->slot[sl];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl->unit_empty[sl]);
+            if (us.u.b < 0) break;
+            const Unit u = us.u;
+            const SeqInfo s = us.s;
+            const UnitGeo ug = unit_geo<kPaged, false>(u, s, tps, p.causal, p.window, unit_slots);
+            const int nt = ug.b[slot] - ug.a[slot];  // tiles of this slot: [a, b) of the stream
             const uint32_t tg0 = tg;
             tg += ug.ntiles;
             if (nt == 0) continue;
-            int qs = u.q0 + slot * tps;
-            if constexpr (kAlt) qs = ug.alt ? u.q0 : qs;  // alt: both slots hold slot 0's rows
+            const int qs = u.q0 + slot * tps;
             const int qe = min(qs + tps, s.n);
             const int tok = qs + r / G;
             const int h = u.kvh * G + r % G;
@@ -1148,8 +1420,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                         sv[96 + i] = __uint_as_float(r3[i]);
                     }
                 }
-                int jrel = ug.a[slot] + j;  // tile index in the unit's stream
-                if constexpr (kAlt) jrel = ug.alt ? slot + 2 * j : jrel;
+                const int jrel = ug.a[slot] + j;  // tile index in the unit's stream
                 const int jt = ug.lo + jrel;  // tile index in the sequence
                 if (kQuant && jt < np) {
                     // int8 prefix tile: S holds q . code; scale column c by its row's scale
@@ -1246,28 +1517,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             // epilogue: O of the slot is final once the PV of its last tile is done
             if (!warp_wait(&ctl->pv_done[slot], (ns + nt - 1) & 1, ctl, hdr)) break;
             tc_fence_after();
-            if constexpr (kAlt) if (ug.alt && slot == 1) {
-                // alt unit: hand this row's max and sum to slot 0's warp of the same
-                // rows; slot 0 merges O_1 from TMEM, writes the row and frees both O
-                // regions.  The next write of xchg waits for that: slot 1's next PV
-                // needs o_empty[1], which slot 0 arrives on after reading.
-                ctl->xchg[sp][lane] = make_float2(m, l);
-                mbar_arrive(&ctl->xchg_full[sp]);
-                ns += nt;
-                continue;
-            }
-            float c0 = 1.f, c1 = 0.f;  // weights of O_0 and O_1 (alt merge)
-            if constexpr (kAlt) if (ug.alt) {
-                if (!warp_wait(&ctl->xchg_full[sp], na & 1, ctl, hdr)) break;
-                ++na;
-                tc_fence_after();  // slot 1 saw pv_done[1] before it arrived
-                const float2 ml = ctl->xchg[sp][lane];
-                const float mm = fmaxf(m, ml.x);
-                c0 = m == -INFINITY ? 0.f : ex2(m - mm);
-                c1 = ml.x == -INFINITY ? 0.f : ex2(ml.x - mm);
-                l = l * c0 + ml.y * c1;
-                m = mm;
-            }
             const float inv_l = 1.f / l;
             const size_t row = (size_t)(s.q_start + tok) * p.n_heads + h;
             uint4* dst = reinterpret_cast<uint4*>(p.out + row * D);
@@ -1277,21 +1526,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 tmem_ld32(o_col + c, o);
                 tmem_wait_ld();
                 reg_fence(o);
-                if constexpr (kAlt) if (ug.alt) {
-                    uint32_t o1[32];
-                    tmem_ld32(o_col + kColSlot + c, o1);  // slot 1's O, same TMEM lanes
-                    tmem_wait_ld();
-                    reg_fence(o1);
-#pragma unroll
-                    for (int i = 0; i < 32; i += 2) {
-                        const float2 a = __ffma2_rn(make_float2(__uint_as_float(o1[i]), __uint_as_float(o1[i + 1])),
-                                                    make_float2(c1, c1),
-                                                    __fmul2_rn(make_float2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])),
-                                                               make_float2(c0, c0)));
-                        o[i] = __float_as_uint(a.x);
-                        o[i + 1] = __float_as_uint(a.y);
-                    }
-                }
                 if (valid) {
                     // whole 32-byte sectors per store when out allows it: the lanes
                     // of a warp write 32 different rows, so each store is 32 pieces
@@ -1314,10 +1548,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             if (valid && p.lse) p.lse[row] = (m + lg2(l)) * 0.69314718055994530942f;
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&ctl->o_empty[slot]);
-                if constexpr (kAlt) if (ug.alt) mbar_arrive(&ctl->o_empty[1]);  // slot 1's O was read here too
-            }
+            if (lane == 0) mbar_arrive(&ctl->o_empty[slot]);
             ns += nt;
         }
     }
