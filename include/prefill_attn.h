@@ -318,7 +318,7 @@ int prefill_attn_last_schedule(void);
  * with these sizes on a GPU with num_sms SMs (kv_quant as in pa_options):
  * 2 for int8 caches; else 3 when total_q < 64 * num_seqs (decode rows); else
  * 1 when n_kv_heads * (total_q / (256 / G)) two-tile units, G = n_heads /
- * n_kv_heads, would fill at most half the SMs; else 2.  Host-only (no CUDA
+ * n_kv_heads, would not exceed the SMs; else 2.  Host-only (no CUDA
  * call); -1 for sizes a call rejects (a non-positive size or n_heads not a
  * multiple of n_kv_heads). */
 int prefill_attn_auto_schedule(int total_q, int num_seqs, int n_heads, int n_kv_heads, int kv_quant, int num_sms);

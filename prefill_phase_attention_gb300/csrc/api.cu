@@ -242,19 +242,20 @@ pa_status check_paged(const Options& o, int max_cache_len, int n_kv_heads) {
 // unless the launch is mostly decode rows (new tokens averaging under 64 per
 // sequence: a decode unit then splits its KV tiles between both softmax slots
 // so that the second does not idle) or is so small that two-tile units would
-// fill at most half of the SMs (then one-tile units, twice as many, each
-// splitting its tiles).  The splitting kernel variant runs other units a few
-// per cent slower and one K/V tile then feeds one Q tile instead of two, so
-// it is not taken for anything else.  Measured on GB300 (152 SMs): a 512-token
-// chunk over a 4096-token prefix, GQA 32/8, 64 two-tile units: 541 -> 840
-// TFLOP/s with one-tile units; 1024-token prompts (128 two-tile units): 300
-// with two-tile units against 282.  bf16 caches only.
+// not give every SM one (then one-tile units, twice as many, each splitting
+// its tiles).  The splitting kernel variant runs other units a few per cent
+// slower and one K/V tile then feeds one Q tile instead of two, so it is not
+// taken for anything else.  Measured on GB300 (152 SMs), TFLOP/s with
+// one-tile / two-tile units: a 512-token chunk over a 4096-token prefix, GQA
+// 32/8 (64 two-tile units) 819 / 540; 1024-token prompts (128 units) 315 /
+// 296 (MHA) and 318 / 309 (GQA-4); a 1536-token MHA prompt (192 units) 490 /
+// 531.  bf16 caches only.
 int auto_schedule(int total_q, int num_seqs, int n_heads, int n_kv_heads, bool kv_quant, int sms) {
     if (kv_quant) return 2;
     if ((long long)total_q < 64LL * num_seqs) return 3;
     const int tpu = pa::kSlots * (pa::kBlockM / (n_heads / n_kv_heads));
     const long long full_units = (long long)n_kv_heads * (total_q / tpu);
-    return 2 * full_units <= sms ? 1 : 2;
+    return full_units <= sms ? 1 : 2;
 }
 
 // Upper bound on the work units of a call (host-side; device metadata unread).

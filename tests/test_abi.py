@@ -142,8 +142,9 @@ def test_options_layout_matches_header():
 @pytest.mark.parametrize("args,expect", [
     # (total_q, num_seqs, n_heads, n_kv_heads, kv_quant, num_sms) -> schedule
     ((32768, 1, 32, 32, 0, 152), 2),   # one long prompt: 4096 two-tile units
-    ((512, 1, 32, 32, 0, 152), 1),     # a 512-token MHA prompt: 64 two-tile units <= 152 / 2
-    ((1024, 1, 32, 32, 0, 152), 2),    # 128 two-tile units > 76
+    ((512, 1, 32, 32, 0, 152), 1),     # a 512-token MHA prompt: 64 two-tile units <= 152
+    ((1024, 1, 32, 32, 0, 152), 1),    # 128 two-tile units <= 152
+    ((1536, 1, 32, 32, 0, 152), 2),    # 192 two-tile units > 152
     ((512, 1, 32, 8, 0, 152), 1),      # GQA-4: 64-token units, 8 x 8 = 64 units
     ((576, 65, 32, 8, 0, 152), 3),     # a chunk and 64 decode rows: 8.9 new tokens per sequence
     ((64, 64, 32, 8, 0, 152), 3),      # decode rows only
