@@ -241,10 +241,12 @@ def test_two_streams_run_concurrently():
         assert np.array_equal(W.bf16_bits(ck_d.cpu()), ref_ck) and np.array_equal(W.bf16_bits(cv_d.cpu()), ref_cv)
 
 
+@pytest.mark.parametrize("sched", [1, 2])
 @pytest.mark.parametrize("d", [32, 64, 128])
-def test_out_16_byte_aligned(d):
+def test_out_16_byte_aligned(d, sched):
     """out at a 16-byte (not 32-byte) aligned address, the API's minimum: the
-    epilogue then stores 16-byte pieces; results and guard bands as usual."""
+    epilogue then stores 16-byte pieces (in both softmax layouts: the plain
+    schedule's and the splitting one's); results and guard bands as usual."""
     wl = W.random_workload(960 + d, head_dim=d, group=2, n_kv_heads=2, allow_empty=False)
     ck, cv, (inp,) = W.make_inputs(wl)
     dev = {k: v.cuda() for k, v in inp.items()}
@@ -255,10 +257,11 @@ def test_out_16_byte_aligned(d):
     assert out.data_ptr() % 32 == 16
     lse = torch.empty(T, wl.n_heads, device="cuda")
     ck_d, cv_d = ck.cuda(), cv.cuda()
-    binding.prefill_attn_varlen(dev["q"], dev["k"], dev["v"], dev["cu_seqlens_q"], dev["cu_seqlens_k"], ck_d, cv_d,
-                                dev["cache_offsets"], out, lse, scale=wl.scale, causal=wl.causal)
+    binding.prefill_attn_varlen_ex(dev["q"], dev["k"], dev["v"], dev["cu_seqlens_q"], dev["cu_seqlens_k"], ck_d, cv_d,
+                                   dev["cache_offsets"], out, lse, scale=wl.scale, causal=wl.causal, schedule=sched)
     torch.cuda.synchronize()
     assert binding.prefill_attn_device_status() == 0
+    assert binding.prefill_attn_last_schedule() == sched
     assert bool((buf[:8] == 7.0).all()) and bool((buf[8 + n:] == 7.0).all()), "write outside out"
     ref_out, ref_lse, _, _ = PT.oracle_step(wl, inp, W.bf16_bits(ck), W.bf16_bits(cv), want_cache=False)
-    PT.compare(out, lse, ref_out, ref_lse, label=f"out +16 B d={d}")
+    PT.compare(out, lse, ref_out, ref_lse, label=f"out +16 B d={d} schedule {sched}")
