@@ -40,7 +40,8 @@
 // (codes expanded in shared memory), and the tile-splitting schedule, in which
 // a unit whose rows fit one Q tile gives its even KV tiles to slot 0 and its
 // odd ones to slot 1 and merges the two partial results (decode rows, short
-// launches of one-tile units).
+// launches of one-tile units); there the softmax is column-split: the two
+// warps of a sub-partition take half of every row's columns for both slots.
 // Every wait is bounded in time; on timeout the CTA records PA_DEVERR_TIMEOUT,
 // drains its in-flight copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
