@@ -58,6 +58,9 @@ def load_library(path: str):
     f.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, I,
                   ctypes.c_double, I, I, P, I, I, I, ctypes.c_double, I, P, P, P, P, P, ctypes.c_int64, I]
     f.restype = I
+    g = lib.oracle_rope_rotate
+    g.argtypes = [P, ctypes.c_int64, I, P, I, ctypes.c_double, P]
+    g.restype = I
     return lib
 
 
@@ -141,3 +144,23 @@ def prefill_attention(q, k, v, cu_seqlens_q, cu_seqlens_k, cache_offsets, cache_
         if kv_quant:
             ck, cv = (ck, sk_out), (cv, sv_out)
     return out, lse, ck, cv
+
+
+def rope_rotate(x, positions, *, rope_theta: float, max_pos: Optional[int] = None, lib=None):
+    """The oracle's rotary rotation alone, before any rounding.
+
+    x [n, d]: uint16 bf16 bit patterns; positions [n]: int32 absolute positions.
+    Returns float64 [n, d]: each vector rotated to its position (rotate-half
+    pairing, fp32 inv_freq and angles, fp64 cos/sin and rotation).
+    """
+    lib = lib or _load()
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    pos = np.ascontiguousarray(positions, dtype=np.int32)
+    n, d = x.shape
+    assert pos.shape == (n,)
+    mp = int(max_pos if max_pos is not None else (int(pos.max()) + 1 if n else 1))
+    out = np.empty((n, d), dtype=np.float64)
+    rc = lib.oracle_rope_rotate(_ptr(x), n, d, _ptr(pos), mp, float(rope_theta), _ptr(out))
+    if rc != 0:
+        raise ValueError(f"oracle: {ERRORS.get(rc, rc)}")
+    return out

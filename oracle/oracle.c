@@ -246,6 +246,59 @@ static int owner(const int32_t *cu_q, int num_seqs, int64_t t)
     return lo; /* the last sequence starting at or before t owns it */
 }
 
+/* cos and sin of every position's rotary angles, [n_pos][d/2] each (cos
+ * first, then sin): inv_freq[i] = 1 / theta^(2i / d) and the angle
+ * pos * inv_freq[i] in fp32, as the page's formula computes them
+ * ([mhpn] §5.1), then cos/sin in fp64.  NULL when out of memory. */
+static double *rope_table(double rope_theta, int head_dim, int n_pos)
+{
+    const int half = head_dim / 2;
+    const size_t n_tab = (size_t)(n_pos > 0 ? n_pos : 1) * half;
+    double *tab = (double *)malloc(2 * n_tab * sizeof(double));
+    if (!tab)
+        return NULL;
+    for (int i = 0; i < half; ++i) {
+        const float inv_freq = 1.0f / powf((float)rope_theta, (float)(2 * i) / (float)head_dim);
+        for (int pos = 0; pos < n_pos; ++pos) {
+            const float angle = (float)pos * inv_freq;
+            tab[(size_t)pos * half + i] = cos((double)angle);
+            tab[n_tab + (size_t)pos * half + i] = sin((double)angle);
+        }
+    }
+    return tab;
+}
+
+/* The rotation alone, before the bf16 rounding that the attention above
+ * applies: head vectors x (bf16 bit patterns, [n_vec][head_dim]) rotated to
+ * the positions pos[n_vec] (each in [0, max_pos)), widened exactly and
+ * written to out ([n_vec][head_dim], fp64).  Returns 0, -1 on bad sizes, -6
+ * when out of memory. */
+int oracle_rope_rotate(const uint16_t *x, int64_t n_vec, int head_dim, const int32_t *pos, int max_pos,
+                       double rope_theta, double *out)
+{
+    if (n_vec < 0 || head_dim <= 0 || head_dim % 2 != 0 || max_pos <= 0 || !(rope_theta > 0))
+        return -1;
+    for (int64_t r = 0; r < n_vec; ++r)
+        if (pos[r] < 0 || pos[r] >= max_pos)
+            return -1;
+    double *tab = rope_table(rope_theta, head_dim, max_pos);
+    if (!tab)
+        return -6;
+    problem pb;
+    memset(&pb, 0, sizeof pb);
+    pb.d = head_dim;
+    pb.rope_cos = tab;
+    pb.rope_sin = tab + (size_t)max_pos * (head_dim / 2);
+    for (int64_t r = 0; r < n_vec; ++r) {
+        double *o = out + (size_t)r * head_dim;
+        for (int e = 0; e < head_dim; ++e)
+            o[e] = bf16_to_double(x[(size_t)r * head_dim + e]);
+        rope_rotate(&pb, pos[r], o);
+    }
+    free(tab);
+    return 0;
+}
+
 /*
  * Returns 0 on success, a negative code for inconsistent metadata:
  *  -1 bad sizes, -2 cu_seqlens_q not starting at 0 or decreasing,
@@ -311,24 +364,13 @@ int oracle_prefill_attention(
                   num_seqs, max_cache_len, n_heads, n_kv_heads, head_dim, scale, causal, window,
                   block_table, block_size, max_blocks, num_blocks, NULL, NULL, kv_quant, scale_k, scale_v};
 
-    /* cos/sin of every position's angles: inv_freq and m * inv_freq in fp32 */
     double *rope_tab = NULL;
     if (rope_theta > 0) {
-        const int half = head_dim / 2;
-        const size_t n_tab = (size_t)(max_cache_len > 0 ? max_cache_len : 1) * half;
-        rope_tab = (double *)malloc(2 * n_tab * sizeof(double));
+        rope_tab = rope_table(rope_theta, head_dim, max_cache_len);
         if (!rope_tab)
             return -6;
-        for (int i = 0; i < half; ++i) {
-            const float inv_freq = 1.0f / powf((float)rope_theta, (float)(2 * i) / (float)head_dim);
-            for (int pos = 0; pos < max_cache_len; ++pos) {
-                const float angle = (float)pos * inv_freq;
-                rope_tab[(size_t)pos * half + i] = cos((double)angle);
-                rope_tab[n_tab + (size_t)pos * half + i] = sin((double)angle);
-            }
-        }
         pb.rope_cos = rope_tab;
-        pb.rope_sin = rope_tab + n_tab;
+        pb.rope_sin = rope_tab + (size_t)(max_cache_len > 0 ? max_cache_len : 1) * (head_dim / 2);
     }
 
     const int64_t n_all = total_q * n_heads;

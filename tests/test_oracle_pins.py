@@ -766,3 +766,73 @@ def test_quant_zero_cache_rows_read_as_zero(oracle_mod):
     assert lse[0, 0] == pytest.approx(math.log(5 + math.exp(s_new)), abs=1e-12)
     w = math.exp(s_new) / (5 + math.exp(s_new))
     assert np.allclose(out[0, 0], w * f64(inp["v"][0, 0]), atol=1e-12)
+
+
+# ------------------------------------------------- rotation before rounding ---
+
+def _libm_inv_freq(theta, d):
+    """inv_freq[i] = 1 / theta^(2i/d) in fp32 through the C library's powf (the
+    same routine the oracle's C code calls), so the angles agree bit for bit."""
+    import ctypes
+    import ctypes.util
+    libm = ctypes.CDLL(ctypes.util.find_library("m"))
+    libm.powf.restype = ctypes.c_float
+    libm.powf.argtypes = [ctypes.c_float, ctypes.c_float]
+    return np.array([np.float32(1.0) / np.float32(libm.powf(np.float32(theta), np.float32(2 * i) / np.float32(d)))
+                     for i in range(d // 2)], dtype=np.float32)
+
+
+@pytest.mark.parametrize("d,theta", [(32, 10000.0), (64, 500000.0), (128, 10000.0)])
+def test_rope_rotation_before_rounding_matches_complex_exponential(oracle_mod, d, theta):
+    """[mhpn] §5.1 restated independently: the pair (x_i, x_{i+d/2}) is the
+    complex number x_i + j x_{i+d/2}, turned by exp(j m inv_freq[i]).  The
+    oracle's fp64 rotation, before its bf16 rounding, equals it to 1e-12 at
+    positions up to 40000 (angles taken in fp32 as the page's formula does)."""
+    rng = np.random.default_rng(d)
+    n = 300
+    x = torch.randn(n, d, generator=torch.Generator().manual_seed(d)).to(torch.bfloat16)
+    pos = np.concatenate([[0, 1, 2, 127, 128, 4095, 32767, 40000],
+                          rng.integers(0, 40001, size=n - 8)]).astype(np.int32)
+    got = oracle_mod.rope_rotate(W.bf16_bits(x), pos, rope_theta=theta, max_pos=40001)
+    inv = _libm_inv_freq(theta, d)
+    ang = (pos.astype(np.float32)[:, None] * inv[None, :]).astype(np.float32).astype(np.float64)
+    xf = x.double().numpy()
+    z = (xf[:, : d // 2] + 1j * xf[:, d // 2:]) * np.exp(1j * ang)
+    ref = np.concatenate([z.real, z.imag], axis=1)
+    assert np.abs(got - ref).max() < 1e-12
+    # position 0 is the identity, exactly
+    assert np.array_equal(got[0], xf[0])
+    # and a rotation keeps every pair's length
+    assert np.allclose(np.hypot(got[:, : d // 2], got[:, d // 2:]), np.hypot(xf[:, : d // 2], xf[:, d // 2:]),
+                       rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("m", [3, 100, 1000, 9999])
+def test_quant_of_rotated_unit_key_closed_form(oracle_mod, m):
+    """int8 x RoPE: a unit key e_i at position m is rotated onto (cos a, sin a)
+    at dimensions (i, i + d/2), a = m * inv_freq[i], then rounded to bf16 (the
+    model dtype, [mhpn] §5.1) and quantised per row ([zskr] §4.3): the larger of
+    the two magnitudes becomes code +-127 with scale = that magnitude / 127, the
+    other code is 127 times the ratio rounded to the nearest integer, and every
+    other code is 0."""
+    d = 32
+    wl = _custom("q8rope", 2, 2, d, [m + 1], [0], cap=m + 1)
+    _, _, (inp,) = W.make_inputs(wl)
+    k = inp["k"].clone()
+    k[m] = 0
+    k[m, 0, 0] = 1.0          # head 0: e_0, inv_freq 1
+    k[m, 1, d // 4] = 1.0     # head 1: e_{d/4}, inv_freq 1/100
+    _, _, (ck, sk), _ = _q8_case(oracle_mod, wl, dict(inp, k=k), rope_theta=10000.0)
+    inv = _libm_inv_freq(10000.0, d)
+    bf = lambda x: float(torch.tensor(x, dtype=torch.float64).to(torch.bfloat16).double())
+    for h, i in ((0, 0), (1, d // 4)):
+        a = float(np.float32(np.float32(m) * inv[i]))
+        x, y = bf(math.cos(a)), bf(math.sin(a))
+        big = max(abs(x), abs(y))
+        exp_codes = np.zeros(d, np.int64)
+        for e, val in ((i, x), (i + d // 2, y)):
+            r = 127 * abs(val) / big
+            assert abs(r - math.floor(r) - 0.5) > 1e-4, "a tie would make the closed form ambiguous"
+            exp_codes[e] = int(math.copysign(round(r), val))
+        assert np.array_equal(ck[0, h, m].astype(np.int64), exp_codes), (h, ck[0, h, m], exp_codes)
+        assert sk[0, h, m] == np.float32(np.float32(big) / np.float32(127.0))
