@@ -15,6 +15,15 @@ For N > 1 (torchrun, one process per GPU) every rank runs its own replica of
 the workload: the units of attention are independent, no collective is on
 the data path (weak scaling).  Timing is max over ranks.
 
+The line's roofline fraction divides by the measured burst bf16 peak when the
+timed region is shorter than 3 s (the sustained, power-capped figure from 3 s
+on); the fractions against the other references are reported beside it.  The
+default run (long32k) also carries a "per_config" block: the other measured
+configurations (tiny_packed, layer512, varlen16, chunked_decode) and
+chunked_decode's two parts alone (chunk512: its 512-token chunk over a
+4096-token prefix; decode64: its 64 decode rows), each with its time per step,
+TFLOP/s, fraction of the burst peak and of its mixed tensor/HBM roofline.
+
 --impl reference times the fp64 CPU oracle on this host's cores on a bounded
 sample of the same workload (the baseline this library is compared with).
 """
@@ -220,6 +229,200 @@ def cpu_baseline(wl, inputs, budget_s: float = 15.0, window: int = 0, rope: floa
 
 # ----------------------------------------------------------------- our arm --
 
+DATASHEET_BF16_TFLOPS = 2250.0  # GB300 dense bf16, NVIDIA's figure without 2:4 sparsity
+SUSTAINED_AFTER_S = 3.0         # timed regions at least this long are compared with the sustained peak
+
+
+class Runner:
+    """A workload's inputs resident on the device and the call that runs one step."""
+
+    def __init__(self, wl, args, binding, W):
+        import torch
+        self.wl, self.args, self.binding = wl, args, binding
+        self.inputs = W.make_inputs(wl, sentinel=False)
+        cache_k, cache_v, steps = self.inputs
+        self.table_d = self.sk_d = self.sv_d = None
+        if args.kv_quant and args.paged:
+            # int8 codes + fp32 row scales in block pools
+            table, codes_k, scales_k, codes_v, scales_v = W.make_paged_q8_cache(
+                wl, args.paged, torch.Generator().manual_seed(wl.seed), sentinel=False)
+            self.ck, self.sk_d, self.cv, self.sv_d = codes_k.cuda(), scales_k.cuda(), codes_v.cuda(), scales_v.cuda()
+            self.table_d = table.cuda()
+        elif args.kv_quant:
+            # the same workload over an int8 cache (codes + fp32 row scales)
+            codes_k, scales_k, codes_v, scales_v = W.make_q8_cache(wl, torch.Generator().manual_seed(wl.seed),
+                                                                   sentinel=False)
+            self.ck, self.sk_d, self.cv, self.sv_d = codes_k.cuda(), scales_k.cuda(), codes_v.cuda(), scales_v.cuda()
+        elif args.paged:
+            # the same workload over a paged cache: a block pool + per-sequence block table
+            table, pool_k, pool_v = W.make_paged_cache(wl, args.paged, torch.Generator().manual_seed(wl.seed),
+                                                       sentinel=False)
+            self.ck, self.cv, self.table_d = pool_k.cuda(), pool_v.cuda(), table.cuda()
+        else:
+            self.ck, self.cv = cache_k.cuda(), cache_v.cuda()
+        self.dev = [{k: v.cuda() for k, v in s.items()} for s in steps]
+        self.outs = [torch.empty_like(d["q"]) for d in self.dev]
+        self.lses = [torch.empty(d["q"].shape[0], wl.n_heads, device="cuda", dtype=torch.float32) for d in self.dev]
+        self.schedules = set()  # the work schedule each call of a step ran (pa_options.schedule)
+
+    def call(self, d, o, l):
+        a, b = self.args, self.binding
+        if a.window or a.paged or a.rope or a.kv_quant:
+            b.prefill_attn_varlen_ex(d["q"], d["k"], d["v"], d["cu_seqlens_q"], d["cu_seqlens_k"], self.ck, self.cv,
+                                     d["cache_offsets"], o, l, scale=self.wl.scale, causal=self.wl.causal,
+                                     window=a.window, block_table=self.table_d, rope_theta=a.rope,
+                                     cache_k_scale=self.sk_d, cache_v_scale=self.sv_d)
+        else:
+            b.prefill_attn_varlen(d["q"], d["k"], d["v"], d["cu_seqlens_q"], d["cu_seqlens_k"], self.ck, self.cv,
+                                  d["cache_offsets"], o, l, scale=self.wl.scale, causal=self.wl.causal)
+
+    def step(self):
+        for d, o, l in zip(self.dev, self.outs, self.lses):
+            self.call(d, o, l)
+
+    def warm(self, warmup):
+        import torch
+        for d, o, l in zip(self.dev, self.outs, self.lses):
+            self.call(d, o, l)
+            self.schedules.add(self.binding.prefill_attn_last_schedule())
+        for _ in range(warmup - 1):
+            self.step()
+        torch.cuda.synchronize()
+        if self.binding.prefill_attn_device_status() != 0:
+            raise RuntimeError(f"device error word set during warm-up of {self.wl.name}")
+
+    def working_set_bytes(self):
+        wl = self.wl
+        return wl.tokens() * (wl.n_heads + 2 * wl.n_kv_heads) * wl.head_dim * 2
+
+    def schedule(self):
+        s = sorted(self.schedules)
+        return s[0] if len(s) == 1 else s
+
+
+def measure(runner, steps, ws=1, local=0, sampler=None):
+    """K timed steps with CUDA events on the launching stream.  A working set
+    larger than L2 runs back to back (the region between the first and the last
+    event); a smaller one is timed cold: a 256 MB buffer is written before
+    every step, outside the step's span, and the spans are summed."""
+    import torch
+    stream = torch.cuda.current_stream()
+    flush = None
+    if runner.working_set_bytes() <= L2_BYTES:
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    hot_ms_step = None
+    if flush is not None:  # the same steps back to back with a warm L2, for reference
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            runner.step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        hot_ms_step = e0.elapsed_time(e1) / steps
+    n_launch = len(runner.dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps * n_launch)]
+    step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if sampler is not None:
+        sampler.start()
+        time.sleep(0.3)
+    launches = 0
+    barrier(ws)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    e_start.record(stream)
+    k = 0
+    for si in range(steps):
+        if flush is not None:
+            flush.fill_(si & 0xFF)  # evict L2 (not inside the step's timed span)
+        step_ev[si][0].record(stream)
+        for d, o, l in zip(runner.dev, runner.outs, runner.lses):
+            ev[k][0].record(stream)
+            runner.call(d, o, l)
+            ev[k][1].record(stream)
+            launches += runner.binding.prefill_attn_last_launch_count()
+            k += 1
+        step_ev[si][1].record(stream)
+    e_end.record(stream)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    barrier(ws)
+    clocks = sampler.stop() if sampler is not None else None
+    ms_total = sum(a.elapsed_time(b) for a, b in step_ev) if flush is not None else e_start.elapsed_time(e_end)
+    ms_total = max_over_ranks(ms_total, ws, device=torch.device("cuda", local))
+    if runner.binding.prefill_attn_device_status() != 0:
+        raise RuntimeError(f"device error word set during the timed region of {runner.wl.name}")
+    per_call_ms = [a.elapsed_time(b) for a, b in ev]
+    return {"ms_total": ms_total, "ms_step": ms_total / steps, "per_call_ms": per_call_ms, "launches": launches,
+            "cold_l2": flush is not None, "hot_ms_step": hot_ms_step, "clocks": clocks,
+            "region_s": ms_total * 1e-3 if flush is not None else t_wall}
+
+
+def algorithmic_bytes(wl, kv_quant=False):
+    """q, k, v read; out, lse and the new cache rows written; the cached prefix read once."""
+    kv_row = wl.n_kv_heads * wl.head_dim * (1 if kv_quant else 2) + (4 * wl.n_kv_heads if kv_quant else 0)
+    return sum(st.total_q * (2 * wl.n_heads + 2 * wl.n_kv_heads) * wl.head_dim * 2 + 4 * st.total_q * wl.n_heads
+               + 2 * st.total_q * kv_row + 2 * kv_row * sum(st.cache_offsets) for st in wl.steps)
+
+
+def peak_for(region_s, peaks):
+    """The measured bf16 peak that applies to a timed region: the burst figure
+    unless the region runs for seconds (then the power-capped sustained one)."""
+    if region_s >= SUSTAINED_AFTER_S:
+        return float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])), \
+            "bf16_tflops_sustained"
+    return float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])), "bf16_tflops"
+
+
+def mixed_roofline(wl, ms_step, tensor_peak, hbm_peak, kv_quant=False):
+    """A step bounded by max(FLOPs / tensor peak, algorithmic bytes / HBM copy bandwidth)."""
+    flops = wl.flops()
+    byt = algorithmic_bytes(wl, kv_quant)
+    t_tensor = flops / (tensor_peak * 1e12) * 1e3
+    t_hbm = byt / (hbm_peak * 1e9) * 1e3
+    return {"flops_per_step": flops, "bytes_per_step": int(byt), "t_tensor_ms": round(t_tensor, 4),
+            "t_hbm_ms": round(t_hbm, 4), "bound": "tensor" if t_tensor >= t_hbm else "hbm",
+            "frac": round(max(t_tensor, t_hbm) / ms_step, 4)}
+
+
+# The configurations the library is measured on besides the headline one, and
+# chunked_decode's two parts alone (its 512-token chunk over a 4096-token
+# prefix, and its 64 decode rows).
+PER_CONFIG = ["tiny_packed", "layer512", "varlen16", "chunked_decode", "chunk512", "decode64"]
+
+
+def per_config_lines(args, binding, W, peaks, steps):
+    import torch
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    lines = {}
+    for name in PER_CONFIG:
+        wl = W.get(name)
+        r = Runner(wl, args, binding, W)
+        r.warm(3)
+        n = steps if len(wl.steps) == 1 else max(3, steps // 4)
+        m = measure(r, n)
+        ms = m["ms_step"]
+        tflops = wl.flops() / (ms * 1e-3) / 1e12
+        byt = algorithmic_bytes(wl)
+        lines[name] = {
+            "ms_per_step": round(ms, 5), "tflops": round(tflops, 2),
+            "tokens_per_s": round(wl.tokens() / (ms * 1e-3), 1), "launches_per_step": len(wl.steps),
+            "frac_of_burst_bf16": round(tflops / burst, 4),
+            "algorithmic_gbs": round(byt / (ms * 1e-3) / 1e9, 1),
+            "frac_of_hbm_copy": round(byt / (ms * 1e-3) / 1e9 / hbm_peak, 4),
+            "roofline_mixed": mixed_roofline(wl, ms, burst, hbm_peak),
+            "schedule": r.schedule(), "steps": n,
+            "l2": "cold (256 MB written before every step)" if m["cold_l2"] else "inputs larger than L2",
+            "value_hot_l2": None if m["hot_ms_step"] is None else
+            round(wl.flops() / (m["hot_ms_step"] * 1e-3) / 1e12, 2)}
+        del r
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    return lines
+
+
 def run_ours(args, ws, rank, local):
     import torch
     from prefill_phase_attention_gb300 import binding, build
@@ -232,116 +435,21 @@ def run_ours(args, ws, rank, local):
     build.build()
     binding.load()
     wl = W.get(args.workload)
-    inputs = W.make_inputs(wl, sentinel=False)
-    cache_k, cache_v, steps = inputs
-    table_d = None
-    sk_d = sv_d = None
-    if args.kv_quant and args.paged:
-        # int8 codes + fp32 row scales in block pools
-        table, codes_k, scales_k, codes_v, scales_v = W.make_paged_q8_cache(
-            wl, args.paged, torch.Generator().manual_seed(wl.seed), sentinel=False)
-        ck, sk_d, cv, sv_d, table_d = codes_k.cuda(), scales_k.cuda(), codes_v.cuda(), scales_v.cuda(), table.cuda()
-        del codes_k, codes_v
-    elif args.kv_quant:
-        # the same workload over an int8 cache (codes + fp32 row scales)
-        codes_k, scales_k, codes_v, scales_v = W.make_q8_cache(wl, torch.Generator().manual_seed(wl.seed),
-                                                               sentinel=False)
-        ck, sk_d, cv, sv_d = codes_k.cuda(), scales_k.cuda(), codes_v.cuda(), scales_v.cuda()
-        del codes_k, codes_v
-    elif args.paged:
-        # the same workload over a paged cache: a block pool + per-sequence block table
-        table, pool_k, pool_v = W.make_paged_cache(wl, args.paged, torch.Generator().manual_seed(wl.seed),
-                                                   sentinel=False)
-        ck, cv, table_d = pool_k.cuda(), pool_v.cuda(), table.cuda()
-        del pool_k, pool_v
-    else:
-        ck, cv = cache_k.cuda(), cache_v.cuda()
-    dev = [{k: v.cuda() for k, v in s.items()} for s in steps]
-    outs = [torch.empty_like(d["q"]) for d in dev]
-    lses = [torch.empty(d["q"].shape[0], wl.n_heads, device="cuda", dtype=torch.float32) for d in dev]
-    stream = torch.cuda.current_stream()
-
-    def call(d, o, l):
-        if args.window or args.paged or args.rope or args.kv_quant:
-            binding.prefill_attn_varlen_ex(d["q"], d["k"], d["v"], d["cu_seqlens_q"], d["cu_seqlens_k"], ck, cv,
-                                           d["cache_offsets"], o, l, scale=wl.scale, causal=wl.causal,
-                                           window=args.window, block_table=table_d, rope_theta=args.rope,
-                                           cache_k_scale=sk_d, cache_v_scale=sv_d)
-        else:
-            binding.prefill_attn_varlen(d["q"], d["k"], d["v"], d["cu_seqlens_q"], d["cu_seqlens_k"], ck, cv,
-                                        d["cache_offsets"], o, l, scale=wl.scale, causal=wl.causal)
-
-    def step():
-        for d, o, l in zip(dev, outs, lses):
-            call(d, o, l)
-
-    schedules = set()  # the work schedule each call of a step ran (pa_options.schedule)
-    for d, o, l in zip(dev, outs, lses):
-        call(d, o, l)
-        schedules.add(binding.prefill_attn_last_schedule())
-    for _ in range(args.warmup - 1):
-        step()
-    torch.cuda.synchronize()
-    if binding.prefill_attn_device_status() != 0:
-        raise RuntimeError("device error word set during warm-up")
-
-    # L2: a working set larger than L2 needs no flush; a smaller one is timed
-    # cold (a 256 MB buffer written before every step, outside the timed spans)
-    ws_bytes = wl.tokens() * (wl.n_heads + 2 * wl.n_kv_heads) * wl.head_dim * 2
-    flush = None if ws_bytes > L2_BYTES else torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
-    hot_ms_step = None
-    if flush is not None:  # the same steps back to back with a warm L2, for reference
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(args.steps):
-            step()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        hot_ms_step = e0.elapsed_time(e1) / args.steps
-
-    # timed region: K steps, per-launch events for the roofline
-    n_launch = len(dev)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps * n_launch)]
-    step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.steps)]
-    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    runner = Runner(wl, args, binding, W)
+    runner.warm(args.warmup)
     sampler = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
-    sampler.start()
-    time.sleep(0.3)
-    launches = 0
-    barrier(ws)
-    torch.cuda.synchronize()
-    e_start.record(stream)
-    k = 0
-    for si in range(args.steps):
-        if flush is not None:
-            flush.fill_(si & 0xFF)  # evict L2 (not inside the step's timed span)
-        step_ev[si][0].record(stream)
-        for d, o, l in zip(dev, outs, lses):
-            ev[k][0].record(stream)
-            call(d, o, l)
-            ev[k][1].record(stream)
-            launches += binding.prefill_attn_last_launch_count()
-            k += 1
-        step_ev[si][1].record(stream)
-    e_end.record(stream)
-    torch.cuda.synchronize()
-    barrier(ws)
-    clocks = sampler.stop()
-    # cold L2: the sum of the steps' own spans; otherwise the whole region
-    ms_total = sum(a.elapsed_time(b) for a, b in step_ev) if flush is not None else e_start.elapsed_time(e_end)
-    ms_total = max_over_ranks(ms_total, ws, device=torch.device("cuda", local))
-    if binding.prefill_attn_device_status() != 0:
-        raise RuntimeError("device error word set during the timed region")
-    per_call_ms = [a.elapsed_time(b) for a, b in ev]
-    ms_step = ms_total / args.steps
+    m = measure(runner, args.steps, ws, local, sampler)
+    clocks = m["clocks"]
+    ms_total, ms_step, per_call_ms = m["ms_total"], m["ms_step"], m["per_call_ms"]
+    n_launch = len(runner.dev)
     flops_step = wl.flops(args.window)
     value = weak_scaling_value(flops_step, ms_total, args.steps, ws)
     tokens_s = ws * wl.tokens() / (ms_step * 1e-3)
 
     peaks, peak_src = load_peaks()
-    peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    peak, peak_key = peak_for(m["region_s"], peaks)
+    burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    sustained = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     # roofline of the dominant kernel: algorithmic causal FLOPs per call / mean call time
     per_launch = []
     for li, s in enumerate(wl.steps):
@@ -351,20 +459,9 @@ def run_ours(args, ws, rank, local):
     fl_tot = sum(f for f, _ in per_launch)
     t_tot = sum(t for _, t in per_launch)
     achieved = fl_tot / (t_tot * 1e-3) / 1e12
-    # mixed roofline of a step: tensor time of its FLOPs vs HBM time of its
-    # algorithmic bytes (q, k, v read; out, lse, cache rows written; cached
-    # prefix read once), the larger of the two against the measured step time
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
-    kv_row = wl.n_kv_heads * wl.head_dim * (1 if args.kv_quant else 2) + (4 * wl.n_kv_heads if args.kv_quant else 0)
-    bytes_step = sum(st.total_q * (2 * wl.n_heads + 2 * wl.n_kv_heads) * wl.head_dim * 2 + 4 * st.total_q * wl.n_heads
-                     + 2 * st.total_q * kv_row + 2 * kv_row * sum(st.cache_offsets) for st in wl.steps)
-    t_tensor = flops_step / (peak * 1e12) * 1e3
-    t_hbm = bytes_step / (hbm_peak * 1e9) * 1e3
-    mixed = {"flops_per_step": flops_step, "bytes_per_step": int(bytes_step),
-             "t_tensor_ms": round(t_tensor, 4), "t_hbm_ms": round(t_hbm, 4),
-             "bound": "tensor" if t_tensor >= t_hbm else "hbm",
-             "frac": round(max(t_tensor, t_hbm) / ms_step, 4),
-             "peaks": f"{peak} TFLOP/s bf16 sustained, {hbm_peak} GB/s copy ({peak_src})"}
+    mixed = mixed_roofline(wl, ms_step, peak, hbm_peak, args.kv_quant)
+    mixed["peaks"] = f"{peak} TFLOP/s {peak_key}, {hbm_peak} GB/s copy ({peak_src})"
     traffic = None
     variant = (f"_window{args.window}" if args.window else "") + (f"_paged{args.paged}" if args.paged else "") \
         + ("_rope" if args.rope else "") + ("_int8kv" if args.kv_quant else "")
@@ -378,6 +475,8 @@ def run_ours(args, ws, rank, local):
     # Every step copies its own inputs in and its own out/lse back; the copies run
     # on two copy streams into a second set of device buffers, so that step s+1's
     # inputs and step s-1's results move while step s computes.
+    steps = runner.inputs[2]
+    outs, lses, stream = runner.outs, runner.lses, torch.cuda.current_stream()
     h_in = [{kk: vv.pin_memory() for kk, vv in s.items()} for s in steps]
     h_out = [[torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs] for _ in range(2)]
     h_lse = [[torch.empty(l.shape, dtype=l.dtype).pin_memory() for l in lses] for _ in range(2)]
@@ -408,7 +507,7 @@ def run_ours(args, ws, rank, local):
             if step >= 2:
                 stream.wait_event(ev_out[b])  # set b's previous results have been copied out
             for di, o, l in zip(d_in[b], d_out[b], d_lse[b]):
-                call(di, o, l)
+                runner.call(di, o, l)
             ev_comp[b].record(stream)
             if step + 1 < n:
                 issue_h2d(step + 1, b ^ 1)
@@ -434,17 +533,25 @@ def run_ours(args, ws, rank, local):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "tokens_per_s": round(tokens_s, 1),
         "pct_of_bf16_peak": round(100 * value / ws / peak, 2),
-        "config": {**workload_config(args, wl),
-                   "launches_per_step": n_launch,
-                   "schedule": sorted(schedules)[0] if len(schedules) == 1 else sorted(schedules),
-                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
-                   "l2": "inputs larger than L2 (no flush)" if flush is None else
-                         "inputs smaller than L2: a 256 MB buffer is written before every timed step (cold L2); "
-                         "value_hot_l2 is the same steps back to back"},
+        "pct_of_bf16_peak_by_reference": {
+            "measured_burst": round(100 * value / ws / burst, 2),
+            "measured_sustained": round(100 * value / ws / sustained, 2),
+            "datasheet_dense": round(100 * value / ws / DATASHEET_BF16_TFLOPS, 2),
+            "note": f"measured peaks from MEASURED_PEAKS.json ({peak_src}): cuBLAS bf16 GEMM, burst {burst} and "
+                    f"sustained {sustained} TFLOP/s; datasheet: GB300 dense bf16 {DATASHEET_BF16_TFLOPS} TFLOP/s"},
+        "config": workload_config(args, wl),
+        "run": {"launches_per_step": n_launch, "schedule": runner.schedule(),
+                "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+                "l2": "inputs larger than L2 (no flush)" if not m["cold_l2"] else
+                      "inputs smaller than L2: a 256 MB buffer is written before every timed step (cold L2); "
+                      "value_hot_l2 is the same steps back to back",
+                "timed_region_s": round(m["region_s"], 4)},
         "roofline_mixed": mixed,
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside back-to-back steps)",
+                     "peak_source": f"{peak_src} {peak_key} (timed region {m['region_s']:.3f} s; the sustained "
+                                    f"figure applies from {SUSTAINED_AFTER_S:g} s on)",
+                     "frac_of_datasheet": round(achieved / DATASHEET_BF16_TFLOPS, 4),
                      "timed": "per prefill_attn_varlen call (scheduler + attention kernel), CUDA events on "
                               "the launching stream"},
         "e2e": {"value": round(e2e_val, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
@@ -452,12 +559,17 @@ def run_ours(args, ws, rank, local):
                 "note": "every step: pinned host q/k/v/metadata -> device, the call, out+lse -> pinned host "
                         "(wall clock over the steps); copies on two copy streams with a second buffer set, "
                         "overlapping the neighbouring steps' compute; KV cache stays device-resident"},
-        "gpu_launches": launches,
-        "value_hot_l2": None if hot_ms_step is None else round(flops_step / (hot_ms_step * 1e-3) / 1e12 * ws, 2),
+        "gpu_launches": m["launches"],
+        "value_hot_l2": None if m["hot_ms_step"] is None else
+        round(flops_step / (m["hot_ms_step"] * 1e-3) / 1e12 * ws, 2),
         "clocks": clocks,
     }
+    default_run = not (args.window or args.paged or args.rope or args.kv_quant) and args.workload == "long32k"
+    if rank == 0 and ws == 1 and not args.no_per_config and default_run:
+        del h_in, h_out, h_lse, d_in, d_out, d_lse
+        result["per_config"] = per_config_lines(args, binding, W, peaks, max(10, min(args.steps, 50)))
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(wl, inputs, budget_s=args.cpu_budget, window=args.window,
+        result["cpu_baseline"] = cpu_baseline(wl, runner.inputs, budget_s=args.cpu_budget, window=args.window,
                                               rope=args.rope)
     if rank == 0:
         print(json.dumps(result), flush=True)
@@ -505,7 +617,8 @@ def run_reference(args, ws, rank):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {**workload_config(args, wl), "parallelism": "host cores"},
+        "config": workload_config(args, wl),
+        "run": {"parallelism": "host cores", "launches_per_step": len(wl.steps)},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
@@ -524,6 +637,7 @@ def main():
     ap.add_argument("--rope", type=float, default=0.0, help="rotary embedding base (0: none)")
     ap.add_argument("--kv-quant", action="store_true", help="int8 KV cache with per-token fp32 scales")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true", help="skip the per-config block of the default run")
     ap.add_argument("--cpu-budget", type=float, default=25.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--ref-rows", type=int, default=128, help="oracle rows per reference step")
     args = ap.parse_args()

@@ -23,6 +23,9 @@ chunked_decode     8192-token prompt as 16 chunks of 512, each step packed with
                    GQA 32/8 heads, head_dim 128 (16 launches)
 long32k            one 32768-token prompt, 32/32 heads, head_dim 128
 long8k             one 8192-token prompt, 32/32 heads, head_dim 128
+chunk512           chunked_decode's chunk at launch 8 alone: 512 new tokens
+                   over a 4096-token cached prefix, GQA 32/8, head_dim 128
+decode64           chunked_decode's 64 decode rows at launch 8 alone
 =================  ===========================================================
 """
 from __future__ import annotations
@@ -131,6 +134,20 @@ def _chunked_decode(prompt: int = 8192, chunk: int = 512, n_decode: int = 64,
     return Workload("chunked_decode", 32, 8, 128, cap, steps, [0] + ctx, seed=4)
 
 
+def _chunk512() -> Workload:
+    # the chunk part of chunked_decode at its midpoint (launch 8): one 512-token
+    # chunk over its 4096-token cached prefix, GQA 32/8
+    return Workload("chunk512", 32, 8, 128, 4096 + 512, [Step([512], [4096])], [4096], seed=7)
+
+
+def _decode64() -> Workload:
+    # the decode part of chunked_decode at its midpoint (launch 8): its 64
+    # one-token rows over their cached contexts, GQA 32/8
+    ctx = np.random.default_rng(4).integers(256, 4096, size=64, endpoint=True).tolist()
+    pref = [c + 8 for c in ctx]
+    return Workload("decode64", 32, 8, 128, max(pref) + 1, [Step([1] * 64, pref)], pref, seed=8)
+
+
 def _long32k() -> Workload:
     return Workload("long32k", 32, 32, 128, 32768, [Step([32768], [0])], [0], seed=5)
 
@@ -148,6 +165,8 @@ WORKLOADS = {
     "chunked_decode": _chunked_decode,
     "long32k": _long32k,
     "long8k": _long8k,
+    "chunk512": _chunk512,
+    "decode64": _decode64,
 }
 
 
