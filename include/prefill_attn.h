@@ -61,13 +61,16 @@ typedef enum {
     PA_ERR_UNSUPPORTED = 2,     /* valid, but outside what this build implements */
     PA_ERR_CUDA = 3,            /* a CUDA runtime/driver call failed */
     PA_ERR_DEVICE_TIMEOUT = 4,  /* a kernel gave up waiting (bounded wait) */
-    PA_ERR_DEVICE_METADATA = 5  /* device metadata was inconsistent; sequences skipped */
+    PA_ERR_DEVICE_METADATA = 5, /* device metadata was inconsistent; sequences skipped */
+    PA_ERR_DEVICE_LAYOUT = 6    /* a kernel found its shared-memory window misaligned; it computed nothing */
 } pa_status;
 
 /* Bits of the device error word (prefill_attn_device_status). */
 #define PA_DEVERR_METADATA 0x1  /* a sequence's cu_seqlens/cache_offsets were inconsistent */
 #define PA_DEVERR_TIMEOUT 0x2   /* an mbarrier wait ran out of its iteration budget */
 #define PA_DEVERR_OVERFLOW 0x4  /* more work units than the workspace holds */
+#define PA_DEVERR_SMEM_ALIGN 0x8 /* the attention kernel's dynamic shared memory was not 1024-byte aligned
+                                  * (the swizzled TMA/MMA tiles need it); its CTAs returned at once */
 
 /*
  * prefill_attn_varlen -- causal varlen prefill attention with the KV-cache write.
@@ -259,8 +262,12 @@ pa_status prefill_attn_varlen_ex(
  * Every call uses the same array: each call first clears its header (the work
  * counter and the device error word), so calls whose work overlaps on the GPU
  * -- on different streams, or on different host threads -- race on it and must
- * be serialised by the caller.  The device error word of this variant is not
- * reported by prefill_attn_device_status.
+ * be serialised by the caller.  The error word of the array (the last call's
+ * PA_DEVERR_* bits: metadata rejected, a wait timed out, too many units) is
+ * read and cleared by prefill_attn_device_status, like a workspace's.  The
+ * address lookup is kept per CUDA context, so a device reset (which unloads
+ * the library's device code and reloads it elsewhere) is followed by a new
+ * lookup on the next call.
  */
 pa_status prefill_attn_varlen_noalloc(
     const void *q, const void *k, const void *v,
@@ -289,10 +296,14 @@ pa_status prefill_attn_varlen_validate(
 
 /*
  * prefill_attn_device_status -- synchronise `stream`, then read and clear the
- * device error word of the current device's (device, stream) workspace.
- * *flags receives the PA_DEVERR_* bits (may be NULL).  Returns PA_OK when the
- * word was zero, PA_ERR_DEVICE_TIMEOUT if the timeout bit was set, else
- * PA_ERR_DEVICE_METADATA.
+ * device error word of the current device's (device, stream) workspace, and,
+ * once prefill_attn_varlen_noalloc has run on the current device, the error
+ * word of its fixed scratch too (which holds the bits of the last such call:
+ * each call clears it; synchronise that call's stream first if it is another
+ * one).  *flags receives the union of the PA_DEVERR_* bits (may be NULL).
+ * Returns PA_OK when the words were zero; else PA_ERR_DEVICE_TIMEOUT if the
+ * timeout bit was set, PA_ERR_DEVICE_LAYOUT if the shared-memory alignment bit
+ * was, else PA_ERR_DEVICE_METADATA.
  */
 pa_status prefill_attn_device_status(pa_stream_t stream, int32_t *flags);
 

@@ -17,8 +17,8 @@ from . import build as _build
 
 PA_OK = 0
 STATUS = {0: "PA_OK", 1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED", 3: "PA_ERR_CUDA",
-          4: "PA_ERR_DEVICE_TIMEOUT", 5: "PA_ERR_DEVICE_METADATA"}
-DEVERR_METADATA, DEVERR_TIMEOUT, DEVERR_OVERFLOW = 0x1, 0x2, 0x4
+          4: "PA_ERR_DEVICE_TIMEOUT", 5: "PA_ERR_DEVICE_METADATA", 6: "PA_ERR_DEVICE_LAYOUT"}
+DEVERR_METADATA, DEVERR_TIMEOUT, DEVERR_OVERFLOW, DEVERR_SMEM_ALIGN = 0x1, 0x2, 0x4, 0x8
 
 class PaOptions(ctypes.Structure):
     """pa_options of include/prefill_attn.h."""
@@ -213,7 +213,7 @@ def prefill_attn_device_status(stream=None) -> int:
     """Synchronise, read and clear the device error word; returns its PA_DEVERR_* bits."""
     flags = ctypes.c_int32(0)
     st = load().prefill_attn_device_status(_stream_handle(stream), ctypes.byref(flags))
-    if st not in (PA_OK, 4, 5):
+    if st not in (PA_OK, 4, 5, 6):
         _check(st)
     return flags.value
 

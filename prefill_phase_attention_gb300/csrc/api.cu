@@ -1,5 +1,6 @@
 // api.cu -- the C ABI (include/prefill_attn.h): argument checks, the
 // per-(device, stream) schedule workspace, and the launch sequence.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -272,6 +273,10 @@ int sm_count(int dev, pa_status* s) {
     return sms;
 }
 
+// Device address of the allocation-free entry point's scratch array in the
+// current context, or nullptr if that entry point has not run there yet.
+void* noalloc_scratch_if_set_up();
+
 struct Scratch {
     pa::WorkspaceHeader* hdr;
     pa::SeqInfo* seqs;
@@ -390,6 +395,7 @@ const char* prefill_attn_status_string(pa_status s) {
         case PA_ERR_CUDA: return "PA_ERR_CUDA";
         case PA_ERR_DEVICE_TIMEOUT: return "PA_ERR_DEVICE_TIMEOUT";
         case PA_ERR_DEVICE_METADATA: return "PA_ERR_DEVICE_METADATA";
+        case PA_ERR_DEVICE_LAYOUT: return "PA_ERR_DEVICE_LAYOUT";
     }
     return "PA_ERR_UNKNOWN";
 }
@@ -503,20 +509,25 @@ pa_status prefill_attn_device_status(pa_stream_t stream_, int32_t* flags) {
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
     e = cudaStreamSynchronize(stream);
     if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
-    void* ptr = nullptr;
+    void* words[2] = {nullptr, noalloc_scratch_if_set_up()};  // workspace, allocation-free scratch
     {
         std::lock_guard<std::mutex> lock(g_mu);
         auto it = g_ws.find(std::make_pair(dev, stream));
-        if (it == g_ws.end() || !it->second.ptr) return PA_OK;
-        ptr = it->second.ptr;
+        if (it != g_ws.end()) words[0] = it->second.ptr;
     }
-    int32_t word = 0, zero = 0;
-    e = cudaMemcpy(&word, ptr, sizeof word, cudaMemcpyDeviceToHost);
-    if (e == cudaSuccess) e = cudaMemcpy(ptr, &zero, sizeof zero, cudaMemcpyHostToDevice);
-    if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+    int32_t word = 0;
+    for (void* ptr : words) {
+        if (!ptr) continue;
+        int32_t w = 0, zero = 0;
+        e = cudaMemcpy(&w, ptr, sizeof w, cudaMemcpyDeviceToHost);
+        if (e == cudaSuccess && w != 0) e = cudaMemcpy(ptr, &zero, sizeof zero, cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+        word |= w;
+    }
     if (flags) *flags = word;
     if (word == 0) return PA_OK;
     if (word & PA_DEVERR_TIMEOUT) return fail(PA_ERR_DEVICE_TIMEOUT, "device error word 0x%x", word);
+    if (word & PA_DEVERR_SMEM_ALIGN) return fail(PA_ERR_DEVICE_LAYOUT, "device error word 0x%x", word);
     return fail(PA_ERR_DEVICE_METADATA, "device error word 0x%x", word);
 }
 
@@ -552,24 +563,63 @@ static_assert(sizeof(pa::WorkspaceHeader) <= kNoAllocHeaderBytes, "header size")
 // comes from cudaGetSymbolAddress, once per device.
 __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
 
+// The array's address is looked up once per CUDA context, keyed by the
+// context's unique id: a device reset destroys the context (and the loaded
+// device code with it), and the next context, even on the same device, gets an
+// id of its own and so a fresh lookup.
 std::mutex g_noalloc_mu;
-std::map<int, void*> g_noalloc_addr;
+std::map<unsigned long long, void*> g_noalloc_addr;
 
-pa_status noalloc_scratch(int dev, void** out) {
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// Unique id of the current context (false if there is none or the driver lacks the call).
+bool current_context_id(unsigned long long* id) {
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<CtxGetCurrentFn>(f);
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<CtxGetIdFn>(f);
+    });
+    CUcontext ctx = nullptr;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx) return false;
+    return get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+pa_status noalloc_scratch(void** out) {
+    unsigned long long id = 0;
+    if (!current_context_id(&id)) return fail(PA_ERR_CUDA, "no current CUDA context");
     std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    auto it = g_noalloc_addr.find(dev);
+    auto it = g_noalloc_addr.find(id);
     if (it != g_noalloc_addr.end()) {
         *out = it->second;
         return PA_OK;
     }
     void* ptr = nullptr;
-    cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);  // the current device is `dev`
+    cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);  // in the current context
     if (e != cudaSuccess || !ptr) return cuda_fail(e, "cudaGetSymbolAddress(scratch)");
-    g_noalloc_addr[dev] = ptr;
+    g_noalloc_addr[id] = ptr;
     *out = ptr;
     return PA_OK;
 }
 
+}  // namespace
+
+namespace {
+void* noalloc_scratch_if_set_up() {
+    unsigned long long id = 0;
+    if (!current_context_id(&id)) return nullptr;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    auto it = g_noalloc_addr.find(id);
+    return it == g_noalloc_addr.end() ? nullptr : it->second;
+}
 }  // namespace
 
 extern "C" pa_status prefill_attn_varlen_noalloc(const void* q, const void* k, const void* v,
@@ -599,7 +649,7 @@ extern "C" pa_status prefill_attn_varlen_noalloc(const void* q, const void* k, c
         return fail(PA_ERR_UNSUPPORTED, "up to %lld work units exceed the allocation-free limit %d", units,
                     kNoAllocMaxUnits);
     void* scratch = nullptr;
-    s = noalloc_scratch(dev, &scratch);
+    s = noalloc_scratch(&scratch);
     if (s != PA_OK) return s;
     // the array keeps the previous call's contents: clear the header (error word, counters)
     e = cudaMemsetAsync(scratch, 0, kNoAllocHeaderBytes, stream);

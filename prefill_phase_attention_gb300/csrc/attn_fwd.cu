@@ -487,7 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     // (and rotary) kernels of this call before anything else
     griddep_wait();
     if (smem_u32(smem_raw) & 1023u) {  // swizzled TMA/UMMA tiles need 1024-byte alignment
-        if (threadIdx.x == 0) atomicOr(&p.hdr->error, PA_DEVERR_TIMEOUT);
+        if (threadIdx.x == 0) atomicOr(&p.hdr->error, PA_DEVERR_SMEM_ALIGN);
         return;
     }
     uint8_t* q_smem = smem_raw;                              // [kSlots] tiles

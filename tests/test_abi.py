@@ -166,3 +166,20 @@ def test_last_schedule_is_zero_without_a_launch(lib):
                                    None) == 0
     assert lib.prefill_attn_last_launch_count() == 0
     assert lib.prefill_attn_last_schedule() == 0
+
+
+def test_device_error_bits_are_distinct_and_match_the_binding():
+    """Each PA_DEVERR_* bit of the header is its own bit, the binding's constants
+    match, and the misaligned shared-memory window has a bit of its own
+    (reported as PA_ERR_DEVICE_LAYOUT, not as a wait timeout)."""
+    src = open(os.path.join(ROOT, "include", "prefill_attn.h")).read()
+    bits = {m.group(1): int(m.group(2), 16) for m in re.finditer(r"#define PA_DEVERR_(\w+) 0x([0-9a-fA-F]+)", src)}
+    assert bits == {"METADATA": 0x1, "TIMEOUT": 0x2, "OVERFLOW": 0x4, "SMEM_ALIGN": 0x8}
+    assert binding.DEVERR_METADATA == bits["METADATA"] and binding.DEVERR_TIMEOUT == bits["TIMEOUT"]
+    assert binding.DEVERR_OVERFLOW == bits["OVERFLOW"] and binding.DEVERR_SMEM_ALIGN == bits["SMEM_ALIGN"]
+    assert re.search(r"PA_ERR_DEVICE_LAYOUT = 6", src)
+    assert binding.STATUS[6] == "PA_ERR_DEVICE_LAYOUT"
+    # the kernel raises the alignment bit, never the timeout bit, for a misaligned window
+    kern = open(os.path.join(ROOT, "prefill_phase_attention_gb300", "csrc", "attn_fwd.cu")).read()
+    i = kern.index("& 1023u")
+    assert "PA_DEVERR_SMEM_ALIGN" in kern[i:i + 200] and "PA_DEVERR_TIMEOUT" not in kern[i:i + 200]

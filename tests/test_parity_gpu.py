@@ -36,7 +36,7 @@ def _run_single_step(wl, rows=None, window=0, schedule=0):
 
 
 @pytest.mark.parametrize("sched", [0, 1, 2, 3])
-@pytest.mark.parametrize("name", ["tiny_packed", "layer512", "varlen16"])
+@pytest.mark.parametrize("name", ["tiny_packed", "layer512", "varlen16", "chunk512", "decode64"])
 def test_named_workload_full(name, sched):
     """Every schedule (one-tile units splitting their KV tiles between the two
     slots; two-tile units; two-tile units with single-tile ones split) and
@@ -45,8 +45,19 @@ def test_named_workload_full(name, sched):
 
 
 def test_long32k_sampled():
+    """The headline configuration against the oracle on 6000+ of its 1,048,576
+    (token, head) rows: every head of the last 128-token Q tile (the longest
+    rows), the first and last row of every 128-row Q tile (the diagonal and
+    the tile edges) with two heads each, and 1500 random rows; the cache in full."""
     wl = W.get("long32k")
-    rows = PT.sample_rows(wl.steps[0], wl.n_heads, 96, seed=5)
+    H, T = wl.n_heads, wl.steps[0].total_q
+    rng = np.random.default_rng(5)
+    last = np.arange(T - 128, T, dtype=np.int64)[:, None] * H + np.arange(H)[None, :]
+    edges = np.concatenate([np.arange(0, T, 128), np.arange(127, T, 128)]).astype(np.int64)
+    edge_rows = np.concatenate([edges * H + rng.integers(0, H, edges.size), edges * H + rng.integers(0, H, edges.size)])
+    rand = rng.integers(0, T * H, size=1500)
+    rows = np.unique(np.concatenate([last.ravel(), edge_rows, rand]))
+    assert rows.size >= 6000
     _run_single_step(wl, rows=rows)
 
 
