@@ -52,10 +52,10 @@ std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// header | SeqInfo[max_seqs] | Unit[max_units] | int[max_seqs] (scheduler scratch)
+// header | SeqInfo[max_seqs] | Unit[max_units] | int[2][max_seqs] (scheduler scratch)
 size_t ws_bytes(int max_seqs, int max_units) {
     return align_up(sizeof(pa::WorkspaceHeader), 16) + (size_t)max_seqs * sizeof(pa::SeqInfo) +
-           (size_t)max_units * sizeof(pa::Unit) + (size_t)max_seqs * sizeof(int);
+           (size_t)max_units * sizeof(pa::Unit) + 2 * (size_t)max_seqs * sizeof(int);
 }
 
 pa::SeqInfo* ws_seqs(const Workspace& w) {
@@ -282,7 +282,7 @@ struct Scratch {
     pa::SeqInfo* seqs;
     pa::Unit* units;
     int max_units;
-    int* seq_scratch;      // int[num_seqs] for the scheduler
+    int* seq_scratch;      // int[2][num_seqs] for the scheduler
     void* rope = nullptr;  // room for the rotated q and k when the rotary embedding is on
 };
 
@@ -302,14 +302,17 @@ pa_status enqueue(const void* q, const void* k, const void* v, const int32_t* cu
     sa.seqs = scr.seqs;
     sa.units = scr.units;
     sa.seq_scratch = scr.seq_scratch;
+    sa.seq_group = scr.seq_scratch + num_seqs;
     sa.num_seqs = num_seqs;
     sa.total_q = total_q;
     sa.max_cache_len = max_cache_len;
     sa.n_kv_heads = n_kv_heads;
+    sa.head_dim = head_dim;
     sa.group = group;
     sa.causal = causal;
     sa.window = o.window;
     sa.max_units = scr.max_units;
+    sa.num_ctas = (int)std::min<long long>(sms, units_bound);
     sa.unit_slots = slots;
     sa.block_table = o.block_table;
     sa.block_size = o.block_size;
@@ -556,7 +559,7 @@ constexpr int kNoAllocMaxSeqs = 4096;
 constexpr int kNoAllocMaxUnits = 61440;
 constexpr size_t kNoAllocHeaderBytes = 16;
 constexpr size_t kNoAllocBytes = kNoAllocHeaderBytes + (size_t)kNoAllocMaxSeqs * sizeof(pa::SeqInfo) +
-                                 (size_t)kNoAllocMaxUnits * sizeof(pa::Unit) + (size_t)kNoAllocMaxSeqs * sizeof(int);
+                                 (size_t)kNoAllocMaxUnits * sizeof(pa::Unit) + 2 * (size_t)kNoAllocMaxSeqs * sizeof(int);
 static_assert(sizeof(pa::WorkspaceHeader) <= kNoAllocHeaderBytes, "header size");
 
 // In host code this name is only a stand-in for the array; its device address

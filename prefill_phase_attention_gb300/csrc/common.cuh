@@ -52,14 +52,17 @@ struct ScheduleArgs {
     SeqInfo* seqs;
     Unit* units;
     int* seq_scratch;  // [num_seqs] scheduler scratch (cost bin, then first unit of the sequence)
+    int* seq_group;    // [num_seqs] scheduler scratch (KV heads per L2 group)
     int num_seqs;
     int total_q;
     int max_cache_len;
     int n_kv_heads;
+    int head_dim;
     int group;      // n_heads / n_kv_heads
     int causal;
     int window;     // sliding window (0: none)
     int max_units;  // capacity of the unit list
+    int num_ctas;   // CTAs of the attention launch (persistent: at most one per SM)
     int unit_slots; // Q tiles per unit: 2 (plain kernel) or 1 (alternating variant)
     // paged cache (block_table == nullptr: contiguous slots)
     const int32_t* block_table;  // [num_seqs][max_blocks]

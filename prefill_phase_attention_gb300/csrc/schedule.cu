@@ -1,18 +1,20 @@
 // schedule.cu -- the longest-first tile scheduler.
 //
 // Reads cu_seqlens_q / cu_seqlens_k / cache_offsets on the device (the varlen
-// kernel "reads cu_seqlens" itself, "大模型 Prompt Prefill 阶段的高效 Batching 与算子排布",
-// §2), sanitises each sequence, cuts it into work units (query block x KV head)
-// and lays them out for the persistent attention kernel, which claims them in
-// list order: sequences by descending total cost (KV tiles visited, counting
-// sort over log-spaced cost bins), within a sequence the query blocks last to
-// first (for a causal mask, the most expensive first) with the KV heads of a
-// block adjacent.  The longest work still starts first (LPT order within a
-// sequence and across sequences; the last units claimed are the cheapest
-// blocks of the cheapest sequences), and the CTAs running at any moment work
-// on one or two sequences, whose K/V then stay in L2 (ordering by unit cost
-// alone interleaves every sequence of a varlen batch and re-reads their K/V
-// from HBM).  It also resets the attention kernel's work counter.
+// kernel takes the sequence boundaries from cu_seqlens itself, "大模型 Prompt
+// Prefill 阶段的高效 Batching 与算子排布", §2), sanitises each sequence, cuts it
+// into work units (query block x KV head) and lays them out for the persistent
+// attention kernel, which claims them in list order: sequences by descending
+// total cost (KV tiles visited, counting sort over log-spaced cost bins);
+// within a sequence its KV heads in groups, and within a group the query
+// blocks last to first (for a causal mask, the most expensive first) with the
+// group's heads adjacent.  The longest work still starts first (LPT order
+// within a group and across sequences; the last units claimed are
+// the cheapest blocks of the cheapest sequences), and the CTAs running at any
+// moment work on one or two sequences and few of their heads, whose K/V then
+// stay in L2 (ordering by unit cost alone interleaves every sequence of a
+// varlen batch, and all heads of a long prompt together outgrow L2; either
+// re-reads K/V from HBM).  It also resets the attention kernel's work counter.
 //
 // One CTA of 1024 threads; its cost is a few microseconds and it keeps the whole
 // launch free of host synchronisation.
@@ -24,6 +26,8 @@
 #include "prefill_attn.h"
 
 namespace pa {
+
+constexpr long long kL2GroupBytes = 48ll << 20;
 
 // Sort key of a sequence: its total cost in log-spaced bins (exact below 64,
 // then 64 bins per power of two), clamped to the histogram.
@@ -72,6 +76,26 @@ __device__ __forceinline__ int block_owner(const SeqInfo* seqs, int num_seqs, in
             hi = mid - 1;
     }
     return lo;
+}
+
+// KV heads of a sequence whose units run together.  Every unit of a head
+// streams that head's K/V from the start of the sequence, so while the CTAs
+// work on a group of heads, the group's K/V (keys and values of P + n tokens,
+// bf16) is what they re-read from L2; groups are sized to keep it within
+// kL2GroupBytes (a share of the 129 MB L2 that leaves room for the q, out and
+// cache-write streams and for the next group, which starts while the last
+// units of a group run).  A group must also hold at least num_ctas times the
+// sequence's longest unit of work (head_cost = the KV tiles of one head's
+// units, longest = the most of one unit): a group's longest unit starts when
+// the group does, so a smaller last group would end the launch on that one
+// unit while the other SMs idle.  That bound wins over the L2 budget.  Short
+// sequences keep all their heads in one group.
+__device__ __forceinline__ int kv_head_group(const SeqInfo& si, int head_dim, int n_kv_heads, int num_ctas,
+                                             long long head_cost, int longest) {
+    const float head_bytes = (float)(si.P + si.n) * (float)(head_dim * 4);
+    float g = floorf((float)kL2GroupBytes / fmaxf(head_bytes, 1.f));
+    if (head_cost > 0) g = fmaxf(g, ceilf((float)num_ctas * (float)longest / (float)head_cost));
+    return g >= (float)n_kv_heads ? n_kv_heads : (g < 1.f ? 1 : (int)g);
 }
 
 __global__ void __launch_bounds__(1024) build_schedule_kernel(ScheduleArgs a) {
@@ -140,18 +164,28 @@ __global__ void __launch_bounds__(1024) build_schedule_kernel(ScheduleArgs a) {
     __syncthreads();
 
     // Pass 2 (one warp per sequence): total cost of the sequence's units; the
-    // histogram counts units per cost bin, the bin waits in seq_scratch.
+    // histogram counts units per cost bin, the bin waits in seq_scratch, the
+    // sequence's KV-head group size in seq_group.
     {
         const int lane = tid & 31, nwarps = nthr >> 5;
         for (int b = tid >> 5; b < a.num_seqs; b += nwarps) {
             const SeqInfo si = a.seqs[b];
             const int nblk = (si.n + tpu - 1) / tpu;
             long long c = 0;
-            for (int i = lane; i < nblk; i += 32) c += unit_tiles(si.n, si.P, i * tpu, tpu, a.causal, a.window, paged);
-            for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+            int mx = 0;
+            for (int i = lane; i < nblk; i += 32) {
+                const int t = unit_tiles(si.n, si.P, i * tpu, tpu, a.causal, a.window, paged);
+                c += t;
+                mx = max(mx, t);
+            }
+            for (int o = 16; o > 0; o >>= 1) {
+                c += __shfl_xor_sync(0xffffffffu, c, o);
+                mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            }
             if (lane == 0 && nblk > 0) {
                 const int bin = cost_bin(c * a.n_kv_heads);
                 a.seq_scratch[b] = bin;
+                a.seq_group[b] = kv_head_group(si, a.head_dim, a.n_kv_heads, a.num_ctas, c, mx);
                 atomicAdd(&hist[bin], nblk * a.n_kv_heads);
             }
         }
@@ -183,25 +217,27 @@ __global__ void __launch_bounds__(1024) build_schedule_kernel(ScheduleArgs a) {
     __threadfence_block();
     __syncthreads();
 
-    // ... and its units go there: query blocks last to first, KV heads adjacent.
-    for (int i = tid; i < total_blocks; i += nthr) {
+    // ... and its units go there: its KV heads in groups whose K/V fit the L2
+    // budget, and within a group the query blocks last to first with the
+    // group's heads adjacent.  One unit per thread and iteration.
+    const int total_units = total_blocks * a.n_kv_heads;  // < 2^31: the host bounds the units
+    for (int w = tid; w < total_units; w += nthr) {
+        const int i = w / a.n_kv_heads, kvh = w % a.n_kv_heads;
         const int b = block_owner(a.seqs, a.num_seqs, i);
         const SeqInfo si = a.seqs[b];
         const int blk = i - si.pad;
         const int nblk = (si.n + tpu - 1) / tpu;
-        const int q0 = blk * tpu;
-        const int cost = unit_tiles(si.n, si.P, q0, tpu, a.causal, a.window, paged);
-        const int base = a.seq_scratch[b] + (nblk - 1 - blk) * a.n_kv_heads;
-        for (int kvh = 0; kvh < a.n_kv_heads; ++kvh) {
-            const int pos = base + kvh;
-            if (pos < a.max_units) {
-                Unit u;
-                u.b = b;
-                u.kvh = kvh;
-                u.q0 = q0;
-                u.ntiles = cost;
-                a.units[pos] = u;
-            }
+        const int hg = a.seq_group[b];
+        const int g0 = kvh - kvh % hg;                 // first head of kvh's group
+        const int gsize = min(hg, a.n_kv_heads - g0);  // heads in the group
+        const int pos = a.seq_scratch[b] + g0 * nblk + (nblk - 1 - blk) * gsize + (kvh - g0);
+        if (pos < a.max_units) {
+            Unit u;
+            u.b = b;
+            u.kvh = kvh;
+            u.q0 = blk * tpu;
+            u.ntiles = unit_tiles(si.n, si.P, u.q0, tpu, a.causal, a.window, paged);
+            a.units[pos] = u;
         }
     }
 }
