@@ -76,6 +76,11 @@ struct Cfg {
     static constexpr int kTileBytes = kChunks * kChunkBytes;  // 128 rows x D bf16
     static constexpr SmemSwizzle kSw = D >= 64 ? kSwizzle128B : kSwizzle64B;
     static constexpr int kSbo = 8 * kRowBytes;  // byte distance between 8-row groups
+    // Paged bf16 cache with two column chunks (d = 128): a prefix tile is
+    // staged as [8-row group][chunk][8 rows] -- one TMA box per cache block
+    // fills whole groups of both chunks -- so 8-row groups sit kGrpSbo apart
+    // and the chunks of a group kSbo apart.
+    static constexpr int kGrpSbo = kChunks * kSbo;
     static constexpr int kStagesK = D == 128 ? 2 : 4;
     static constexpr int kStagesV = D == 128 ? 3 : 4;
     static constexpr uint32_t kIdescS = idesc_bf16_f32(kBlockM, kBlockN, 0, 0);
@@ -311,17 +316,18 @@ __device__ __noinline__ void copy_tile_rows_paged(const uint8_t* tile, __nv_bflo
 }
 
 // Zeroes rows [row0, 128) of a staged tile (whole rows, so the swizzle does
-// not matter).
-template <int D>
+// not matter); kGrp: the tile is staged block by block (Cfg::kGrpSbo).
+template <int D, bool kGrp>
 __device__ __noinline__ void zero_tile_rows(uint8_t* tile, int row0, int lane) {
     using C = Cfg<D>;
     constexpr int kGran = D / 8;
     constexpr int kChunkGran = C::kChunkCols / 8;
     const int total = (kBlockN - row0) * kGran;
     for (int idx = lane; idx < total; idx += 32) {
-        const int r = row0 + idx / kGran, g = idx % kGran;
-        *reinterpret_cast<uint4*>(tile + (g / kChunkGran) * C::kChunkBytes + r * C::kRowBytes + (g % kChunkGran) * 16) =
-            make_uint4(0, 0, 0, 0);
+        const int r = row0 + idx / kGran, g = idx % kGran, c = g / kChunkGran;
+        const int off = kGrp ? (r >> 3) * C::kGrpSbo + c * C::kSbo + (r & 7) * C::kRowBytes
+                             : c * C::kChunkBytes + r * C::kRowBytes;
+        *reinterpret_cast<uint4*>(tile + off + (g % kChunkGran) * 16) = make_uint4(0, 0, 0, 0);
     }
 }
 
@@ -481,6 +487,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     // 3 stages that PV follows every slot's softmax of tile t: the ring slot is
     // free.  (bf16 caches use no scale ring.)
     constexpr int kStK = kQuant && C::kStagesK > 3 ? 3 : C::kStagesK;
+    // paged bf16 cache, two column chunks: prefix tiles staged block by block
+    constexpr bool kGrp = kPaged && !kQuant && C::kChunks == 2;
     const int unit_slots = kAlt ? p.unit_slots : kSlots;  // Q tiles of a unit
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // launched with programmatic stream serialisation: wait for the scheduler
@@ -565,10 +573,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     if (kPaged && warp == 0) {
         // ------------------------------------- paged cache: unit fetch, Q, K and V loads
         // Lanes 0-15 load K (lane 0 also fetches units and loads Q), lanes
-        // 16-31 load V.  A prefix tile is one TMA box per (cache block,
-        // 64-column chunk): lane l of a group issues boxes l and l + 16, so a
-        // tile of 16-token blocks costs each lane one or two TMA issues, and
-        // each lane loads the block ids of its boxes one tile ahead.
+        // 16-31 load V, as one code path: each pass of the loop loads one K
+        // tile and one V tile, the V group one tile behind the K group (its
+        // first pass is idle).  K tile t waits for the stage that S(t - 2)
+        // frees and V tile t - 1 for the one PV(t - 4) frees, which the tensor
+        // pipe finishes first, so a pass waits on K alone, as a K loader of
+        // its own would; V tile t beside K tile t would hold every K load back
+        // until PV(t - 3).  A prefix tile is one TMA box per cache block (both
+        // column chunks at d = 128; int8: all D columns) or per (block,
+        // 64-column chunk): lane l of a group issues boxes l and l + 16 and
+        // loads the block ids of its boxes one tile ahead.
         const bool is_v = lane >= 16;
         const int gl = lane & 15;
         const unsigned gmask = is_v ? 0xFFFF0000u : 0x0000FFFFu;
@@ -585,116 +599,157 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         const int bmask = (1 << p.block_log2) - 1;
         int last_parity[4] = {-1, -1, -1, -1};
         int last_q_parity = -1;
-        uint32_t t = 0;
-        for (int u_it = 0;; ++u_it) {
-            const int sl = u_it & 1;
-            bool ok = true;
-            if (!is_v) {
-                if (gleader) {
-                    ok = wait_bar(&ctl->unit_empty[sl], ((u_it >> 1) & 1) ^ 1, ctl, hdr);
-                    if (ok) {
-                        const int idx = atomicAdd(&hdr->counter, 1);
-                        UnitSlot us;
-                        if (idx < num_units) {
-                            us.u = p.units[idx];
-                            us.s = p.seqs[us.u.b];
-                        } else {
-                            us.u.b = -1;
+        uint32_t t = 0;          // tiles of this group's ring so far
+        int u_it = 0;            // units this group has taken so far
+        Unit u{};                // the group's current unit ...
+        SeqInfo s{};
+        UnitGeo ug{};
+        const int32_t* tab = p.block_table;
+        int j = 0, ntl = 0;      // ... its next tile and its tile count
+        bool done = false;       // end of the unit list met (or a wait failed)
+        // this lane's boxes of tile jj: box (pair / kChunks), chunk (pair % kChunks)
+        // for pair = gl and gl + 16; returns the block id of each (prefix tiles)
+        auto fetch_ids = [&](int jj, int& i0, int& i1) {
+            i0 = i1 = 0;
+            if (jj < ug.np) {
+                const int kb = kBlockN * jj;
+                const int boxes = (min(kBlockN, s.P - kb) + br - 1) / br;
+                // one box per block (int8: all D columns; bf16 at d = 128: both
+                // chunks), else one per (block, chunk)
+                const int b0 = kQuant || kGrp ? gl : gl / C::kChunks;
+                const int b1 = kQuant || kGrp ? gl + 16 : (gl + 16) / C::kChunks;
+                if (b0 < boxes) i0 = __ldg(tab + ((kb + b0 * br) >> p.block_log2));
+                if (b1 < boxes) i1 = __ldg(tab + ((kb + b1 * br) >> p.block_log2));
+            }
+        };
+        int id0 = 0, id1 = 0, nid0 = 0, nid1 = 0;
+        for (int pass = 0;; ++pass) {
+            if (!done && !(is_v && pass == 0)) {
+                // the next unit, once the current one has no tile left
+                while (!done && j == ntl) {
+                    const int sl = u_it & 1;
+                    bool ok = true;
+                    if (!is_v) {
+                        if (gleader) {
+                            ok = wait_bar(&ctl->unit_empty[sl], ((u_it >> 1) & 1) ^ 1, ctl, hdr);
+                            if (ok) {
+                                const int idx = atomicAdd(&hdr->counter, 1);
+                                UnitSlot us;
+                                if (idx < num_units) {
+                                    us.u = p.units[idx];
+                                    us.s = p.seqs[us.u.b];
+                                } else {
+                                    us.u.b = -1;
+                                }
+                                ctl->slot[sl] = us;
+                                mbar_arrive(&ctl->unit_full[sl]);
+                            }
                         }
-                        ctl->slot[sl] = us;
-                        mbar_arrive(&ctl->unit_full[sl]);
+                        ok = __shfl_sync(gmask, ok, src);
+                    } else {
+                        ok = gleader ? wait_bar(&ctl->unit_full[sl], (u_it >> 1) & 1, ctl, hdr) : true;
+                        ok = __shfl_sync(gmask, ok, src);
                     }
-                }
-                ok = __shfl_sync(gmask, ok, src);
-            } else {
-                ok = gleader ? wait_bar(&ctl->unit_full[sl], (u_it >> 1) & 1, ctl, hdr) : true;
-                ok = __shfl_sync(gmask, ok, src);
-            }
-            if (!ok) break;
-            __syncwarp(gmask);  // the slot written by lane 0 (K) / acquired by lane 16 (V) is visible
-            const Unit u = ctl->slot[sl].u;
-            const SeqInfo s = ctl->slot[sl].s;
-            __syncwarp(gmask);
-            if (is_v && gleader) mbar_arrive(&ctl->unit_empty[sl]);
-            if (u.b < 0) break;
-            if (!is_v && gleader) {
-                // the unit's Q tiles (one or two): rows (token, head-in-group) of each slot
-                ok = wait_bar(&ctl->q_empty, (u_it & 1) ^ 1, ctl, hdr);
-                if (ok) {
-                    const int nq = unit_slots == 2 && u.q0 + tps < s.n ? 2 : 1;
-                    mbar_arrive_expect_tx(&ctl->q_full, nq * G * tps * C::kRowBytes * C::kChunks);
-                    for (int i = 0; i < nq; ++i)
-                        for (int c = 0; c < C::kChunks; ++c)
-                            tma_load_3d(q_smem + i * C::kTileBytes + c * C::kChunkBytes, &p.tm_q, &ctl->q_full,
-                                        c * C::kChunkCols, u.kvh * G, s.q_start + u.q0 + i * tps);
-                    last_q_parity = u_it & 1;
-                }
-            }
-            if (!is_v && !__shfl_sync(gmask, ok, src)) break;
-            const UnitGeo ug = unit_geo<true, kAlt>(u, s, tps, p.causal, p.window, unit_slots);
-            const int32_t* tab = p.block_table + (size_t)u.b * p.max_blocks;
-            // this lane's boxes of tile jj: box (pair / kChunks), chunk (pair % kChunks)
-            // for pair = gl and gl + 16; returns the block id of each (prefix tiles)
-            auto fetch_ids = [&](int jj, int& id0, int& id1) {
-                id0 = id1 = 0;
-                if (jj < ug.np) {
-                    const int kb = kBlockN * jj;
-                    const int boxes = (min(kBlockN, s.P - kb) + br - 1) / br;
-                    // int8 cache: one box per block (all D columns); bf16: one per (block, chunk)
-                    const int b0 = kQuant ? gl : gl / C::kChunks, b1 = kQuant ? gl + 16 : (gl + 16) / C::kChunks;
-                    if (b0 < boxes) id0 = __ldg(tab + ((kb + b0 * br) >> p.block_log2));
-                    if (b1 < boxes) id1 = __ldg(tab + ((kb + b1 * br) >> p.block_log2));
-                }
-            };
-            int id0, id1, nid0 = 0, nid1 = 0;
-            fetch_ids(ug.lo, id0, id1);
-            for (int j = 0; j < ug.ntiles; ++j, ++t) {
-                const int jj = ug.lo + j;
-                if (j + 1 < ug.ntiles) fetch_ids(jj + 1, nid0, nid1);  // in flight during this tile
-                const int st = t % stages;
-                const uint32_t ph = (t / stages) & 1;
-                ok = gleader ? wait_bar(&empty[st], ph ^ 1, ctl, hdr) : true;
-                if (!__shfl_sync(gmask, ok, src)) { ok = false; break; }
-                const int kb = tile_key_base<true>(jj, s.P, ug.np);
-                uint8_t* stage = ring + st * C::kTileBytes;
-                if (kQuant && jj < ug.np) {
-                    // int8 codes, one box of br rows x D bytes per block, into the
-                    // stage's upper half (expanded to bf16 by the cache writer)
-                    const int boxes = (min(kBlockN, s.P - kb) + br - 1) / br;
-                    if (gleader) mbar_arrive_expect_tx(&full[st], boxes * br * D);
+                    if (!ok) {
+                        done = true;
+                        break;
+                    }
+                    __syncwarp(gmask);  // the slot written by lane 0 (K) / acquired by lane 16 (V) is visible
+                    u = ctl->slot[sl].u;
+                    s = ctl->slot[sl].s;
                     __syncwarp(gmask);
+                    if (is_v && gleader) mbar_arrive(&ctl->unit_empty[sl]);
+                    if (u.b < 0) {
+                        done = true;
+                        break;
+                    }
+                    if (!is_v && gleader) {
+                        // the unit's Q tiles (one or two): rows (token, head-in-group) of each slot
+                        ok = wait_bar(&ctl->q_empty, (u_it & 1) ^ 1, ctl, hdr);
+                        if (ok) {
+                            const int nq = unit_slots == 2 && u.q0 + tps < s.n ? 2 : 1;
+                            mbar_arrive_expect_tx(&ctl->q_full, nq * G * tps * C::kRowBytes * C::kChunks);
+                            for (int i = 0; i < nq; ++i)
+                                for (int c = 0; c < C::kChunks; ++c)
+                                    tma_load_3d(q_smem + i * C::kTileBytes + c * C::kChunkBytes, &p.tm_q,
+                                                &ctl->q_full, c * C::kChunkCols, u.kvh * G,
+                                                s.q_start + u.q0 + i * tps);
+                            last_q_parity = u_it & 1;
+                        }
+                    }
+                    if (!is_v && !__shfl_sync(gmask, ok, src)) {
+                        done = true;
+                        break;
+                    }
+                    ++u_it;
+                    ug = unit_geo<true, kAlt>(u, s, tps, p.causal, p.window, unit_slots);
+                    tab = p.block_table + (size_t)u.b * p.max_blocks;
+                    j = 0;
+                    ntl = ug.ntiles;
+                    if (ntl > 0) fetch_ids(ug.lo, id0, id1);
+                }
+                if (!done) {
+                    const int jj = ug.lo + j;
+                    if (j + 1 < ntl) fetch_ids(jj + 1, nid0, nid1);  // in flight during this tile
+                    const int st = t % stages;
+                    const uint32_t ph = (t / stages) & 1;
+                    const bool ok = gleader ? wait_bar(&empty[st], ph ^ 1, ctl, hdr) : true;
+                    if (!__shfl_sync(gmask, ok, src)) {
+                        done = true;
+                    } else {
+                        const int kb = tile_key_base<true>(jj, s.P, ug.np);
+                        uint8_t* stage = ring + st * C::kTileBytes;
+                        if (kQuant && jj < ug.np) {
+                            // int8 codes, one box of br rows x D bytes per block, into the
+                            // stage's upper half (expanded to bf16 by the cache writer)
+                            const int boxes = (min(kBlockN, s.P - kb) + br - 1) / br;
+                            if (gleader) mbar_arrive_expect_tx(&full[st], boxes * br * D);
+                            __syncwarp(gmask);
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int box = gl + 16 * h;
-                        if (box < boxes)
-                            tma_load_3d(stage + C::kTileBytes / 2 + box * br * D, tm_cache, &full[st], 0,
-                                        (kb + box * br) & bmask, (h ? id1 : id0) * p.n_kv_heads + u.kvh);
-                    }
-                } else if (jj < ug.np) {
-                    const int boxes = (min(kBlockN, s.P - kb) + br - 1) / br;
-                    if (gleader) mbar_arrive_expect_tx(&full[st], boxes * br * C::kRowBytes * C::kChunks);
-                    __syncwarp(gmask);
+                            for (int h = 0; h < 2; ++h) {
+                                const int box = gl + 16 * h;
+                                if (box < boxes)
+                                    tma_load_3d(stage + C::kTileBytes / 2 + box * br * D, tm_cache, &full[st], 0,
+                                                (kb + box * br) & bmask, (h ? id1 : id0) * p.n_kv_heads + u.kvh);
+                            }
+                        } else if (kGrp && jj < ug.np) {
+                            // one box per block: br rows x both chunks as whole 8-row
+                            // groups (at most 16 boxes, one per lane)
+                            const int boxes = (min(kBlockN, s.P - kb) + br - 1) / br;
+                            if (gleader) mbar_arrive_expect_tx(&full[st], boxes * br * C::kRowBytes * C::kChunks);
+                            __syncwarp(gmask);
+                            if (gl < boxes)
+                                tma_load_5d(stage + gl * br * C::kRowBytes * C::kChunks, tm_cache, &full[st], 0, 0, 0,
+                                            ((kb + gl * br) & bmask) >> 3, id0 * p.n_kv_heads + u.kvh);
+                        } else if (jj < ug.np) {
+                            const int boxes = (min(kBlockN, s.P - kb) + br - 1) / br;
+                            if (gleader) mbar_arrive_expect_tx(&full[st], boxes * br * C::kRowBytes * C::kChunks);
+                            __syncwarp(gmask);
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int pair = gl + 16 * h;
-                        const int box = pair / C::kChunks, c = pair % C::kChunks;
-                        if (box < boxes)
-                            tma_load_3d(stage + c * C::kChunkBytes + box * br * C::kRowBytes, tm_cache, &full[st],
-                                        c * C::kChunkCols, (kb + box * br) & bmask,
-                                        (h ? id1 : id0) * p.n_kv_heads + u.kvh);
+                            for (int h = 0; h < 2; ++h) {
+                                const int pair = gl + 16 * h;
+                                const int box = pair / C::kChunks, c = pair % C::kChunks;
+                                if (box < boxes)
+                                    tma_load_3d(stage + c * C::kChunkBytes + box * br * C::kRowBytes, tm_cache,
+                                                &full[st], c * C::kChunkCols, (kb + box * br) & bmask,
+                                                (h ? id1 : id0) * p.n_kv_heads + u.kvh);
+                            }
+                        } else {
+                            if (gleader) mbar_arrive_expect_tx(&full[st], C::kTileBytes);
+                            __syncwarp(gmask);
+                            if (gl < C::kChunks)
+                                tma_load_3d(stage + gl * C::kChunkBytes, tm_new, &full[st], gl * C::kChunkCols, u.kvh,
+                                            s.q_start + kb - s.P);
+                        }
+                        last_parity[st] = (int)ph;
+                        id0 = nid0;
+                        id1 = nid1;
+                        ++j;
+                        ++t;
                     }
-                } else {
-                    if (gleader) mbar_arrive_expect_tx(&full[st], C::kTileBytes);
-                    __syncwarp(gmask);
-                    if (gl < C::kChunks)
-                        tma_load_3d(stage + gl * C::kChunkBytes, tm_new, &full[st], gl * C::kChunkCols, u.kvh,
-                                    s.q_start + kb - s.P);
                 }
-                last_parity[st] = (int)ph;
-                id0 = nid0;
-                id1 = nid1;
             }
-            if (!ok) break;
+            if (__all_sync(0xFFFFFFFFu, done)) break;
         }
         if (gleader && aborted(ctl)) {
             if (!is_v) drain(&ctl->q_full, &last_q_parity, 1);
@@ -776,6 +831,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         const uint64_t q_desc = smem_desc(q_addr, 16, C::kSbo, C::kSw);
         const uint64_t k_desc = smem_desc(k_addr, 16, C::kSbo, C::kSw);
         const uint64_t v_desc = smem_desc(v_addr, C::kChunkBytes, C::kSbo, C::kSw);
+        // block-by-block staging of paged prefix tiles (kGrp)
+        const uint64_t k_desc_g = smem_desc(k_addr, 16, C::kGrpSbo, C::kSw);
+        const uint64_t v_desc_g = smem_desc(v_addr, C::kSbo, C::kGrpSbo, C::kSw);
         uint32_t t = 0;                // KV tiles of this CTA so far
         uint32_t ns[kSlots] = {0, 0};  // tiles processed per slot so far
         uint32_t no[kSlots] = {0, 0};  // units with the slot active so far
@@ -793,27 +851,37 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             return warp_wait(&ctl->k_full[kst], (tt / kStK) & 1, ctl, hdr);
         };
         bool ok = true;
-        auto issue_s = [&](int i, uint32_t tt, int qi) {  // S of slot i from Q tile qi and K tile tt
+        // S of slot i from Q tile qi and K tile tt (grp: a block-staged prefix tile)
+        auto issue_s = [&](int i, uint32_t tt, int qi, bool grp) {
             if (leader) {
                 const uint32_t koff = (tt % kStK) * C::kTileBytes;
                 const uint32_t qoff = qi * C::kTileBytes;
+                // K operand: descriptor template and chunk stride of the tile's staging
+                const bool g = kGrp && grp;
+                const uint64_t kd = g ? k_desc_g : k_desc;
+                const uint32_t kcs = g ? C::kSbo : C::kChunkBytes;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = ((kk * 16) / C::kChunkCols) * C::kChunkBytes + ((kk * 16) % C::kChunkCols) * 2;
-                    mma_ss(tmem + i * kColSlot, q_desc + ((qoff + off) >> 4), k_desc + ((koff + off) >> 4),
+                    const uint32_t koff_kk = ((kk * 16) / C::kChunkCols) * kcs + ((kk * 16) % C::kChunkCols) * 2;
+                    mma_ss(tmem + i * kColSlot, q_desc + ((qoff + off) >> 4), kd + ((koff + koff_kk) >> 4),
                            C::kIdescS, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(&ctl->s_full[i]);
             }
             __syncwarp();
         };
-        auto issue_pv = [&](int i, uint32_t tt, bool first) {
+        auto issue_pv = [&](int i, uint32_t tt, bool first, bool grp) {
             if (leader) {
                 const uint32_t voff = (tt % C::kStagesV) * C::kTileBytes;
+                // V operand: descriptor template and 16-key step of the tile's staging
+                const bool g = kGrp && grp;
+                const uint64_t vd = g ? v_desc_g : v_desc;
+                const uint32_t vstep = g ? 2 * C::kGrpSbo : 2 * C::kSbo;
 #pragma unroll
                 for (int kk = 0; kk < kBlockN / 16; ++kk)
                     mma_ts(tmem + i * kColSlot + kColO, tmem + i * kColSlot + kk * 8,
-                           v_desc + ((voff + kk * 2 * C::kSbo) >> 4), C::kIdescO, (!first || kk > 0) ? 1u : 0u);
+                           vd + ((voff + kk * vstep) >> 4), C::kIdescO, (!first || kk > 0) ? 1u : 0u);
                 mma_commit(&ctl->pv_done[i]);
             }
             __syncwarp();
@@ -848,11 +916,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 // S_0(0), S_1(1), then per tile j: PV_i(j), S_i(j + 2)
                 if (!wait_k(t, ug.lo, ug.np)) break;
                 tc_fence_after();
-                issue_s(0, t, 0);
+                issue_s(0, t, 0, ug.lo < ug.np);
                 commit(&ctl->k_empty[t % kStK]);
                 if (!wait_k(t + 1, ug.lo + 1, ug.np)) break;
                 tc_fence_after();
-                issue_s(1, t + 1, 0);
+                issue_s(1, t + 1, 0, ug.lo + 1 < ug.np);
                 commit(&ctl->k_empty[(t + 1) % kStK]);
                 if (ntiles == 2) commit(&ctl->q_empty);
                 for (int j = 0; j < ntiles && ok; ++j) {
@@ -862,11 +930,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                     if (kth == 0 && !warp_wait(&ctl->o_empty[i], (no[i] & 1) ^ 1, ctl, hdr)) { ok = false; break; }
                     if (!wait_v(tj, ug.lo + j)) { ok = false; break; }
                     tc_fence_after();
-                    issue_pv(i, tj, kth == 0);
+                    issue_pv(i, tj, kth == 0, ug.lo + j < ug.np);
                     if (j + 2 < ntiles) {
                         if (!wait_k(tj + 2, ug.lo + j + 2, ug.np)) { ok = false; break; }
                         tc_fence_after();
-                        issue_s(i, tj + 2, 0);
+                        issue_s(i, tj + 2, 0, ug.lo + j + 2 < ug.np);
                         commit(&ctl->k_empty[(tj + 2) % kStK]);
                         if (j + 3 == ntiles) commit(&ctl->q_empty);
                     }
@@ -883,7 +951,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             if (!wait_k(t, ug.lo, ug.np)) break;
             tc_fence_after();
             for (int i = 0; i < kSlots; ++i)
-                if (ug.a[i] == 0 && ug.b[i] > 0) issue_s(i, t, i);
+                if (ug.a[i] == 0 && ug.b[i] > 0) issue_s(i, t, i, ug.lo < ug.np);
             commit(&ctl->k_empty[t % kStK]);
             if (ntiles == 1) commit(&ctl->q_empty);
             for (int j = 0; j < ntiles && ok; ++j) {
@@ -915,7 +983,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                             v_ready = true;
                         }
                         tc_fence_after();
-                        issue_pv(i, tj, j == ug.a[i]);
+                        issue_pv(i, tj, j == ug.a[i], ug.lo + j < ug.np);
                     }
                     if (j + 1 >= ug.a[i] && j + 1 < ug.b[i]) {
                         // S_i(j+1) overwrites P_i(j): issued after PV_i(j) on the in-order tensor pipe
@@ -927,7 +995,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                             k_ready = true;
                             tc_fence_after();
                         }
-                        issue_s(i, tj + 1, i);
+                        issue_s(i, tj + 1, i, ug.lo + j + 1 < ug.np);
                     }
                 }
                 if (!ok) break;
@@ -1062,7 +1130,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 } else if (kPaged && !is_k && paged_tail_tile(j, us.s.P, np)) {
                     // rows from P on may hold anything (NaN included): zero them
                     // so that P = 0 there contributes exactly 0 to O
-                    zero_tile_rows<D>(ring + st * C::kTileBytes, us.s.P - kBlockN * j, lane);
+                    zero_tile_rows<D, kGrp>(ring + st * C::kTileBytes, us.s.P - kBlockN * j, lane);
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&ctl->v_fix[st]);
@@ -1588,6 +1656,24 @@ cudaError_t encode3d(CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, 
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// Paged bf16 pool [num_blocks * Hk][bs][128] as 5-D (64 columns, 8 rows, 2
+// chunks, bs / 8 row groups, num_blocks * Hk) with byte strides (256, 128,
+// 2048, bs * 256): a box of (64, 8, 2, min(bs, 128) / 8, 1) is one block's rows
+// of one KV head, landing in shared memory as [8-row group][chunk][8 rows] of
+// 128-byte rows (the staging the MMA descriptors of paged prefix tiles read).
+cudaError_t encode_pool_by_block(CUtensorMap* m, const void* ptr, uint64_t bs, uint64_t z, uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return cudaErrorNotSupported;
+    cuuint64_t dims[5] = {64, 8, 2, bs / 8, z};
+    cuuint64_t strides[4] = {256, 128, 2048, bs * 256};
+    cuuint32_t box[5] = {64, 8, 2, box_rows / 8, 1};
+    cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(ptr), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 template <int D, bool kPaged, bool kQuant, bool kAlt = false, bool kHook = false>
 cudaError_t launch_d(const FwdParams& p, int grid, cudaStream_t st) {
     constexpr int kSmem = smem_bytes<D>();
@@ -1639,6 +1725,13 @@ cudaError_t encode_fwd_maps(FwdParams& p, const void* q, int total_q, int num_se
         if (e != cudaSuccess) return e;
         return encode3d(&p.tm_cv, p.cache_v, D, bs, Z, D, bs * D, (uint32_t)D, p.box_rows, 1, CU_TENSOR_MAP_SWIZZLE_NONE,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_DATA_TYPE_UINT8);
+    }
+    if (p.block_table && D == 128) {
+        // one box per block (both column chunks); the kernel's paged d = 128 loads
+        const uint64_t bs = 1ull << p.block_log2, Z = (uint64_t)num_blocks * Hk;
+        e = encode_pool_by_block(&p.tm_ck, p.cache_k, bs, Z, (uint32_t)p.box_rows);
+        if (e != cudaSuccess) return e;
+        return encode_pool_by_block(&p.tm_cv, p.cache_v, bs, Z, (uint32_t)p.box_rows);
     }
     if (p.block_table) {
         // pool [num_blocks, Hk, bs, D] viewed (D, bs, num_blocks * Hk)
