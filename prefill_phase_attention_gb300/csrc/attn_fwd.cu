@@ -596,10 +596,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         const CUtensorMap* tm_new = is_v ? &p.tm_v : &p.tm_k;
         const int num_units = hdr->num_units;
         const int br = p.box_rows;
+        const int br_log2 = min(p.block_log2, 7);  // box_rows = 1 << br_log2
         const int bmask = (1 << p.block_log2) - 1;
-        int last_parity[4] = {-1, -1, -1, -1};
+        // ring position of the group's next tile, and per stage whether a copy
+        // was started on it (bit of lp_set) with which parity (bit of lp_par)
+        int st = 0;
+        uint32_t ph = 0, lp_set = 0, lp_par = 0;
         int last_q_parity = -1;
-        uint32_t t = 0;          // tiles of this group's ring so far
         int u_it = 0;            // units this group has taken so far
         Unit u{};                // the group's current unit ...
         SeqInfo s{};
@@ -613,7 +616,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             i0 = i1 = 0;
             if (jj < ug.np) {
                 const int kb = kBlockN * jj;
-                const int boxes = (min(kBlockN, s.P - kb) + br - 1) / br;
+                const int boxes = (min(kBlockN, s.P - kb) + br - 1) >> br_log2;
                 // one box per block (int8: all D columns; bf16 at d = 128: both
                 // chunks), else one per (block, chunk)
                 const int b0 = kQuant || kGrp ? gl : gl / C::kChunks;
@@ -691,8 +694,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 if (!done) {
                     const int jj = ug.lo + j;
                     if (j + 1 < ntl) fetch_ids(jj + 1, nid0, nid1);  // in flight during this tile
-                    const int st = t % stages;
-                    const uint32_t ph = (t / stages) & 1;
                     const bool ok = gleader ? wait_bar(&empty[st], ph ^ 1, ctl, hdr) : true;
                     if (!__shfl_sync(gmask, ok, src)) {
                         done = true;
@@ -702,7 +703,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                         if (kQuant && jj < ug.np) {
                             // int8 codes, one box of br rows x D bytes per block, into the
                             // stage's upper half (expanded to bf16 by the cache writer)
-                            const int boxes = (min(kBlockN, s.P - kb) + br - 1) / br;
+                            const int boxes = (min(kBlockN, s.P - kb) + br - 1) >> br_log2;
                             if (gleader) mbar_arrive_expect_tx(&full[st], boxes * br * D);
                             __syncwarp(gmask);
 #pragma unroll
@@ -715,14 +716,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                         } else if (kGrp && jj < ug.np) {
                             // one box per block: br rows x both chunks as whole 8-row
                             // groups (at most 16 boxes, one per lane)
-                            const int boxes = (min(kBlockN, s.P - kb) + br - 1) / br;
+                            const int boxes = (min(kBlockN, s.P - kb) + br - 1) >> br_log2;
                             if (gleader) mbar_arrive_expect_tx(&full[st], boxes * br * C::kRowBytes * C::kChunks);
                             __syncwarp(gmask);
                             if (gl < boxes)
                                 tma_load_5d(stage + gl * br * C::kRowBytes * C::kChunks, tm_cache, &full[st], 0, 0, 0,
                                             ((kb + gl * br) & bmask) >> 3, id0 * p.n_kv_heads + u.kvh);
                         } else if (jj < ug.np) {
-                            const int boxes = (min(kBlockN, s.P - kb) + br - 1) / br;
+                            const int boxes = (min(kBlockN, s.P - kb) + br - 1) >> br_log2;
                             if (gleader) mbar_arrive_expect_tx(&full[st], boxes * br * C::kRowBytes * C::kChunks);
                             __syncwarp(gmask);
 #pragma unroll
@@ -741,17 +742,23 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                                 tma_load_3d(stage + gl * C::kChunkBytes, tm_new, &full[st], gl * C::kChunkCols, u.kvh,
                                             s.q_start + kb - s.P);
                         }
-                        last_parity[st] = (int)ph;
+                        lp_set |= 1u << st;
+                        lp_par = (lp_par & ~(1u << st)) | (ph << st);
                         id0 = nid0;
                         id1 = nid1;
                         ++j;
-                        ++t;
+                        if (++st == stages) {
+                            st = 0;
+                            ph ^= 1;
+                        }
                     }
                 }
             }
             if (__all_sync(0xFFFFFFFFu, done)) break;
         }
         if (gleader && aborted(ctl)) {
+            int last_parity[4];
+            for (int i = 0; i < 4; ++i) last_parity[i] = (lp_set >> i) & 1 ? (int)((lp_par >> i) & 1) : -1;
             if (!is_v) drain(&ctl->q_full, &last_q_parity, 1);
             drain(full, last_parity, stages);
         }
