@@ -66,6 +66,18 @@ def test_paged_random_shapes(seed):
     _run_paged(wl, bs, seed, window=window, schedule=(seed // 5) % 4)
 
 
+@pytest.mark.parametrize("bs", [8, 64, 512, 1024])
+def test_paged_d128_block_sizes(bs):
+    """head_dim 128, where a prefix tile is one TMA box per cache block staged
+    by 8-row groups, at the block sizes the random cases above leave out for
+    d = 128: prefixes over many blocks (or many tiles of one block) with partial
+    last blocks, GQA 4, every schedule."""
+    for sched in (1, 2, 3):
+        wl = W.random_workload(900 + bs + sched, head_dim=128, group=4, n_kv_heads=2, max_len=300,
+                               max_prefix=2500)
+        _run_paged(wl, bs, bs + sched, schedule=sched)
+
+
 @pytest.mark.parametrize("bs", [16, 128])
 def test_paged_long_prefix_sampled(bs):
     """A 1024-token chunk over a 7000-token cached prefix (GQA 32/8, d 128), plus
