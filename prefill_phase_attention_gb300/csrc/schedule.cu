@@ -28,6 +28,10 @@
 namespace pa {
 
 constexpr long long kL2GroupBytes = 48ll << 20;
+// Batches of up to this many sequences keep the per-sequence tables the passes
+// below hand to one another (SeqInfo, cost bin / list position, KV-head group)
+// in shared memory; larger ones go through the workspace in global memory.
+constexpr int kSmemSeqs = 1024;
 
 // Sort key of a sequence: its total cost in log-spaced bins (exact below 64,
 // then 64 bins per power of two), clamped to the histogram.
@@ -101,12 +105,20 @@ __device__ __forceinline__ int kv_head_group(const SeqInfo& si, int head_dim, in
 __global__ void __launch_bounds__(1024) build_schedule_kernel(ScheduleArgs a) {
     __shared__ int hist[kCostBins];
     __shared__ int warp_sums[32];
+    __shared__ SeqInfo s_seqs[kSmemSeqs];
+    __shared__ int s_scratch[kSmemSeqs], s_group[kSmemSeqs];
     const int tid = threadIdx.x;
     const int nthr = blockDim.x;
     const int tpu = a.unit_slots * (kBlockM / a.group);  // query tokens per unit
     // the next kernel (launched with programmatic stream serialisation) may
     // start its prologue now; it waits for this kernel before reading the list
     griddep_launch();
+    // where the passes keep their per-sequence tables (the attention kernel
+    // reads the sequences from a.seqs, which pass 1 always writes)
+    const bool small = a.num_seqs <= kSmemSeqs;
+    SeqInfo* const seqs = small ? s_seqs : a.seqs;
+    int* const seq_scratch = small ? s_scratch : a.seq_scratch;
+    int* const seq_group = small ? s_group : a.seq_group;
 
     for (int i = tid; i < kCostBins; i += nthr) hist[i] = 0;
 
@@ -126,7 +138,7 @@ __global__ void __launch_bounds__(1024) build_schedule_kernel(ScheduleArgs a) {
                 bad |= blk < 0 || blk >= a.num_blocks;
             }
             bad = __any_sync(0xffffffffu, bad);
-            if (lane == 0) a.seqs[b].pad = bad ? 1 : 0;
+            if (lane == 0) seqs[b].pad = bad ? 1 : 0;
         }
         __threadfence_block();
         __syncthreads();
@@ -146,7 +158,7 @@ __global__ void __launch_bounds__(1024) build_schedule_kernel(ScheduleArgs a) {
             const long long n = (long long)q_end - q_start;
             const bool ok = q_start >= 0 && n >= 0 && (long long)q_end <= a.total_q && P >= 0 &&
                             (long long)lk == (long long)P + n && (long long)P + n <= a.max_cache_len &&
-                            (b > 0 || q_start == 0) && !(paged && a.seqs[b].pad != 0);
+                            (b > 0 || q_start == 0) && !(paged && seqs[b].pad != 0);
             if (!ok) atomicOr(&a.hdr->error, PA_DEVERR_METADATA);
             si.q_start = ok ? q_start : 0;
             si.n = ok ? (int)n : 0;
@@ -156,7 +168,10 @@ __global__ void __launch_bounds__(1024) build_schedule_kernel(ScheduleArgs a) {
         int chunk_total;
         const int excl = block_exclusive_scan(nblk, warp_sums, &chunk_total);
         si.pad = blocks_before + excl;
-        if (b < a.num_seqs) a.seqs[b] = si;
+        if (b < a.num_seqs) {
+            a.seqs[b] = si;
+            if (small) s_seqs[b] = si;
+        }
         blocks_before += chunk_total;
     }
     const int total_blocks = blocks_before;
@@ -169,7 +184,7 @@ __global__ void __launch_bounds__(1024) build_schedule_kernel(ScheduleArgs a) {
     {
         const int lane = tid & 31, nwarps = nthr >> 5;
         for (int b = tid >> 5; b < a.num_seqs; b += nwarps) {
-            const SeqInfo si = a.seqs[b];
+            const SeqInfo si = seqs[b];
             const int nblk = (si.n + tpu - 1) / tpu;
             long long c = 0;
             int mx = 0;
@@ -184,8 +199,8 @@ __global__ void __launch_bounds__(1024) build_schedule_kernel(ScheduleArgs a) {
             }
             if (lane == 0 && nblk > 0) {
                 const int bin = cost_bin(c * a.n_kv_heads);
-                a.seq_scratch[b] = bin;
-                a.seq_group[b] = kv_head_group(si, a.head_dim, a.n_kv_heads, a.num_ctas, c, mx);
+                seq_scratch[b] = bin;
+                seq_group[b] = kv_head_group(si, a.head_dim, a.n_kv_heads, a.num_ctas, c, mx);
                 atomicAdd(&hist[bin], nblk * a.n_kv_heads);
             }
         }
@@ -211,8 +226,8 @@ __global__ void __launch_bounds__(1024) build_schedule_kernel(ScheduleArgs a) {
 
     // Pass 3: each sequence claims its range of the list from its bin ...
     for (int b = tid; b < a.num_seqs; b += nthr) {
-        const int nblk = (a.seqs[b].n + tpu - 1) / tpu;
-        if (nblk > 0) a.seq_scratch[b] = atomicAdd(&hist[a.seq_scratch[b]], nblk * a.n_kv_heads);
+        const int nblk = (seqs[b].n + tpu - 1) / tpu;
+        if (nblk > 0) seq_scratch[b] = atomicAdd(&hist[seq_scratch[b]], nblk * a.n_kv_heads);
     }
     __threadfence_block();
     __syncthreads();
@@ -223,14 +238,14 @@ __global__ void __launch_bounds__(1024) build_schedule_kernel(ScheduleArgs a) {
     const int total_units = total_blocks * a.n_kv_heads;  // < 2^31: the host bounds the units
     for (int w = tid; w < total_units; w += nthr) {
         const int i = w / a.n_kv_heads, kvh = w % a.n_kv_heads;
-        const int b = block_owner(a.seqs, a.num_seqs, i);
-        const SeqInfo si = a.seqs[b];
+        const int b = block_owner(seqs, a.num_seqs, i);
+        const SeqInfo si = seqs[b];
         const int blk = i - si.pad;
         const int nblk = (si.n + tpu - 1) / tpu;
-        const int hg = a.seq_group[b];
+        const int hg = seq_group[b];
         const int g0 = kvh - kvh % hg;                 // first head of kvh's group
         const int gsize = min(hg, a.n_kv_heads - g0);  // heads in the group
-        const int pos = a.seq_scratch[b] + g0 * nblk + (nblk - 1 - blk) * gsize + (kvh - g0);
+        const int pos = seq_scratch[b] + g0 * nblk + (nblk - 1 - blk) * gsize + (kvh - g0);
         if (pos < a.max_units) {
             Unit u;
             u.b = b;
