@@ -491,13 +491,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     constexpr bool kGrp = kPaged && !kQuant && C::kChunks == 2;
     const int unit_slots = kAlt ? p.unit_slots : kSlots;  // Q tiles of a unit
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    // launched with programmatic stream serialisation: wait for the scheduler
-    // (and rotary) kernels of this call before anything else
-    griddep_wait();
-    if (smem_u32(smem_raw) & 1023u) {  // swizzled TMA/UMMA tiles need 1024-byte alignment
-        if (threadIdx.x == 0) atomicOr(&p.hdr->error, PA_DEVERR_SMEM_ALIGN);
-        return;
-    }
+    // swizzled TMA/UMMA tiles need 1024-byte alignment (reported below)
+    const bool misaligned = (smem_u32(smem_raw) & 1023u) != 0;
     uint8_t* q_smem = smem_raw;                              // [kSlots] tiles
     uint8_t* k_smem = q_smem + kSlots * C::kTileBytes;       // [kStagesK] tiles
     uint8_t* v_smem = k_smem + C::kStagesK * C::kTileBytes;  // [kStagesV] tiles
@@ -509,7 +504,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     const int G = p.group;
     const int tps = kBlockM / G;  // query tokens per slot
 
-    if (threadIdx.x == 0) {
+    // The prologue (barriers, TMEM, tensor-map prefetch) reads nothing the
+    // previous kernels of the call write, so it runs before the wait below and
+    // overlaps their tail (programmatic stream serialisation).
+    if (!misaligned && threadIdx.x == 0) {
         mbar_init(&ctl->q_full, 1);
         mbar_init(&ctl->q_empty, 1);
         for (int s = 0; s < kStK; ++s) {
@@ -545,9 +543,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         prefetch_tmap(&p.tm_ck);
         prefetch_tmap(&p.tm_cv);
     }
-    if (warp == 1) {
+    if (!misaligned && warp == 1) {
         tmem_alloc(&ctl->tmem_base, 512);
         tmem_relinquish();
+    }
+    // wait for the scheduler (and rotary) kernels of this call before reading
+    // or writing anything of theirs or of the caller's
+    griddep_wait();
+    if (misaligned) {
+        if (threadIdx.x == 0) atomicOr(&p.hdr->error, PA_DEVERR_SMEM_ALIGN);
+        return;
     }
     tc_fence_before();
     __syncthreads();
