@@ -181,5 +181,6 @@ def test_device_error_bits_are_distinct_and_match_the_binding():
     assert binding.STATUS[6] == "PA_ERR_DEVICE_LAYOUT"
     # the kernel raises the alignment bit, never the timeout bit, for a misaligned window
     kern = open(os.path.join(ROOT, "prefill_phase_attention_gb300", "csrc", "attn_fwd.cu")).read()
-    i = kern.index("& 1023u")
+    assert re.search(r"const bool misaligned = \(smem_u32\(smem_raw\) & 1023u\) != 0;", kern)
+    i = kern.index("if (misaligned) {")
     assert "PA_DEVERR_SMEM_ALIGN" in kern[i:i + 200] and "PA_DEVERR_TIMEOUT" not in kern[i:i + 200]

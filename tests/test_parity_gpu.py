@@ -179,6 +179,21 @@ def test_many_sequences_sampled():
     _run_single_step(wl, rows=rows)
 
 
+@pytest.mark.parametrize("B", [1024, 1025])
+def test_scheduler_table_boundary(B):
+    """1024 sequences (the device scheduler keeps its per-sequence tables in
+    shared memory) and 1025 (they go through the workspace): decode rows, short
+    prompts and empty sequences over cached prefixes, every row checked under
+    every schedule."""
+    rng = np.random.default_rng(B)
+    lens = rng.choice([0, 1, 1, 2, 9, 40], size=B).tolist()
+    pref = rng.integers(0, 200, size=B).tolist()
+    cap = max(p + n for p, n in zip(pref, lens)) + 1
+    wl = W.Workload(f"seqs{B}", 8, 2, 64, cap, [W.Step(lens, pref)], pref, seed=B)
+    for sched in (0, 1, 2, 3):
+        _run_single_step(wl, schedule=sched)
+
+
 def test_single_token_total():
     """total_q = 1: one decode row, nothing else."""
     wl = W.Workload("one_tok", 8, 2, 64, 70, [W.Step([1], [64])], [64], seed=80)
