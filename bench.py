@@ -60,12 +60,19 @@ def load_peaks():
 
 
 def kernel_sha256() -> str:
-    """Hash of the attention kernel's sources (ties stored ncu counters to a kernel version)."""
+    """Hash of the attention kernel's code (ties stored ncu counters to a kernel
+    version): its sources with comments and blank lines removed, so that an
+    edit of a comment does not orphan the counters of an unchanged kernel."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for f in ("attn_fwd.cu", "ptx.cuh", "common.cuh"):
-        with open(os.path.join(ROOT, "prefill_phase_attention_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "prefill_phase_attention_gb300", "csrc", f), encoding="utf-8") as fh:
+            src = fh.read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)      # block comments
+        src = re.sub(r"//[^\n]*", "", src)                    # line comments (no '//' in the strings here)
+        lines = [ln.rstrip() for ln in src.splitlines()]
+        h.update("\n".join(ln for ln in lines if ln).encode())
     return h.hexdigest()
 
 
@@ -468,7 +475,7 @@ def run_ours(args, ws, rank, local):
     tpath = os.path.join(ROOT, "profiles", f"traffic_{wl.name}{variant}.json")
     if os.path.exists(tpath):
         rec = json.load(open(tpath))
-        if rec.get("kernel_sha256") == kernel_sha256():  # counters of this very kernel source only
+        if rec.get("kernel_sha256") == kernel_sha256():  # counters of this very kernel code only
             traffic = rec.get("bytes_per_launch")
 
     # end to end through the public API: pinned host inputs -> device -> call -> host result.

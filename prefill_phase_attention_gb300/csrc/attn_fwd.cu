@@ -36,12 +36,14 @@
 //                   (its TMEM lane), fp32 running max/sum in registers, exp2
 //                   on the MUFU, lazy O rescale, epilogue out = O / l (bf16)
 //                   and LSE.
-// Variants (template arguments): a paged cache (block table), an int8 cache
-// (codes expanded in shared memory), and the tile-splitting schedule, in which
-// a unit whose rows fit one Q tile gives its even KV tiles to slot 0 and its
-// odd ones to slot 1 and merges the two partial results (decode rows, short
-// launches of one-tile units); there the softmax is column-split: the two
-// warps of a sub-partition take half of every row's columns for both slots.
+// Variants (template arguments): a paged cache (block table; warp 0's two
+// lane halves load K and V, V one tile behind, one TMA box per cache block),
+// an int8 cache (codes expanded in shared memory), and the tile-splitting
+// schedule, in which a unit whose rows fit one Q tile gives its even KV tiles
+// to slot 0 and its odd ones to slot 1 and merges the two partial results
+// (decode rows, short launches of one-tile units); there the softmax is
+// column-split: the two warps of a sub-partition take half of every row's
+// columns for both slots.
 // Every wait is bounded in time; on timeout the CTA records PA_DEVERR_TIMEOUT,
 // drains its in-flight copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
