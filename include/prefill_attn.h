@@ -41,6 +41,16 @@
  *   - out must not alias q, k or v; the caches must not alias k or v.
  *   - Inputs are assumed finite.  Cache entries outside [0, P_b) of each slot are
  *     never read, so an uninitialised cache is fine.
+ *   - CUDA graphs: prefill_attn_varlen / _ex calls enqueue only kernels and
+ *     device copies, so they may be captured into a graph, on a stream that
+ *     already ran a call (outside the capture) with at least the same
+ *     num_seqs and work units (and the same rotary sizes when rope_theta > 0):
+ *     under capture nothing is allocated, and a call whose workspace would have
+ *     to grow returns PA_ERR_UNSUPPORTED.  A replay reruns the call with the
+ *     sizes and pointers of the capture; the device metadata (cu_seqlens_*,
+ *     cache_offsets) and the data in the buffers are read at replay time, so
+ *     they may change between replays within those sizes.
+ *     prefill_attn_varlen_noalloc allocates nothing at all.
  */
 #ifndef PREFILL_ATTN_H
 #define PREFILL_ATTN_H

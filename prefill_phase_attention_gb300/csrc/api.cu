@@ -66,7 +66,15 @@ pa::Unit* ws_units(const Workspace& w) { return reinterpret_cast<pa::Unit*>(ws_s
 
 int* ws_seq_scratch(const Workspace& w) { return reinterpret_cast<int*>(ws_units(w) + w.max_units); }
 
-// Returns the workspace of (device, stream), growing it (stream-ordered) when needed.
+// True while `st` is being captured into a CUDA graph.
+bool capturing(cudaStream_t st) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    return cudaStreamIsCapturing(st, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive;
+}
+
+// Returns the workspace of (device, stream), growing it (stream-ordered) when
+// needed.  Under graph capture nothing is allocated: the stream must already
+// hold a workspace big enough (from a call outside the capture).
 pa_status get_workspace(int dev, cudaStream_t st, int num_seqs, int max_units, Workspace** out) {
     std::lock_guard<std::mutex> lock(g_mu);
     Workspace& w = g_ws[std::make_pair(dev, st)];
@@ -74,6 +82,11 @@ pa_status get_workspace(int dev, cudaStream_t st, int num_seqs, int max_units, W
         *out = &w;
         return PA_OK;
     }
+    if (capturing(st))
+        return fail(PA_ERR_UNSUPPORTED,
+                    "graph capture: the stream's workspace would have to grow (%d sequences, %d work units); "
+                    "run a call of at least these sizes on this stream before capturing",
+                    num_seqs, max_units);
     Workspace nw;
     nw.max_seqs = std::max(num_seqs, std::max(w.max_seqs, 64));
     nw.max_units = std::max(max_units, std::max(w.max_units, 4096));
@@ -98,6 +111,11 @@ pa_status get_workspace(int dev, cudaStream_t st, int num_seqs, int max_units, W
 // Grows (stream-ordered) the rotated-q/k scratch of a workspace to `bytes`.
 pa_status get_rope_scratch(Workspace* w, cudaStream_t st, size_t bytes, void** out) {
     std::lock_guard<std::mutex> lock(g_mu);
+    if (w->rope_bytes < bytes && capturing(st))
+        return fail(PA_ERR_UNSUPPORTED,
+                    "graph capture: the stream's rotary scratch would have to grow (%zu bytes); run a call with "
+                    "rope_theta of at least these sizes on this stream before capturing",
+                    bytes);
     if (w->rope_bytes < bytes) {
         void* nptr = nullptr;
         cudaError_t e = cudaMallocAsync(&nptr, bytes, st);
