@@ -366,6 +366,35 @@ def measure(runner, steps, ws=1, local=0, sampler=None):
             "region_s": ms_total * 1e-3 if flush is not None else t_wall}
 
 
+def graph_ms_step(runner, steps):
+    """The step captured once into a CUDA graph (on a stream of its own, after an
+    uncaptured step sized that stream's workspace) and replayed `steps` times
+    back to back: the step's device time with no host time between launches
+    (warm L2), as a serving loop that replays captured steps sees it."""
+    import torch
+    st = torch.cuda.Stream()
+    with torch.cuda.stream(st):
+        runner.step()
+    st.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=st):
+        runner.step()
+    for _ in range(10):  # the first replays of a new graph run slower
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(st):
+        e0.record(st)
+        for _ in range(steps):
+            g.replay()
+        e1.record(st)
+    torch.cuda.synchronize()
+    if runner.binding.prefill_attn_device_status() != 0:
+        raise RuntimeError(f"device error word set during the graph replays of {runner.wl.name}")
+    del g
+    return e0.elapsed_time(e1) / steps
+
+
 def algorithmic_bytes(wl, kv_quant=False):
     """q, k, v read; out, lse and the new cache rows written; the cached prefix read once."""
     kv_row = wl.n_kv_heads * wl.head_dim * (1 if kv_quant else 2) + (4 * wl.n_kv_heads if kv_quant else 0)
@@ -424,6 +453,10 @@ def per_config_lines(args, binding, W, peaks, steps):
             "l2": "cold (256 MB written before every step)" if m["cold_l2"] else "inputs larger than L2",
             "value_hot_l2": None if m["hot_ms_step"] is None else
             round(wl.flops() / (m["hot_ms_step"] * 1e-3) / 1e12, 2)}
+        # launch-bound configurations: the same step replayed from a CUDA graph
+        g_ms = graph_ms_step(r, n)
+        lines[name]["value_graph_hot_l2"] = round(wl.flops() / (g_ms * 1e-3) / 1e12, 2)
+        lines[name]["ms_per_step_graph_hot_l2"] = round(g_ms, 5)
         del r
         torch.cuda.synchronize()
         torch.cuda.empty_cache()
